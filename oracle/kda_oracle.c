@@ -1,0 +1,116 @@
+/*
+ * kda_oracle.c -- float64 CPU oracle for the gated delta rule.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the GPU library links, includes or
+ * calls this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline use it.  It shares no code, header or constant with the CUDA path.
+ *
+ * What it computes (one head at a time, token by token, in float64):
+ *
+ *   a_t  = exp(-exp(log_alpha_t))     per key channel (vector over dk),
+ *                                     one scalar per token, or 1 (no decay)
+ *   S    = Diag(a_t) S                decay first: row i of S is scaled by a_t[i]
+ *   u_t  = beta_t (v_t - S^T k_t)     read the decayed memory at key k_t
+ *   S    = S + k_t u_t^T              write the correction along k_t
+ *   o_t  = S^T q_t                    read-out after the write
+ *
+ * Sources, by page title and section:
+ *  - "22,580: From GPT-2 to Kimi K3" (yichencityu.github.io), section 5.2
+ *    "The delta rule: erase first, then write": v_old = k S, u = beta (v - v_old),
+ *    S <- S + k^T u, o = q S (row-vector form; S^T q above is the same product
+ *    written for column vectors, with S stored [dk][dv]).
+ *  - same page, section 6.1: the token-by-token prefill loop that collects
+ *    q_t S_t after each write, so the output includes the current token.
+ *  - "22580: From GPT-2 to Kimi3, Explained" (zharfai.com), "Gated DeltaNet
+ *    adds controlled forgetting": S_t = a_t (I - b_t k_t k_t^T) S_{t-1} + b_t k_t v_t^T.
+ *    With a per-channel a_t the decay is applied first, as Diag(a_t) S_{t-1},
+ *    and the delta read and write act on the decayed state.
+ *  - "22580: From GPT-2 to Kimi K3, Explained" (lukebest.github.io),
+ *    "KDA (per-channel alpha)": alpha = exp(-exp(log_alpha)), one value per
+ *    channel; the channel is the key axis (rows of S).
+ *
+ * Inputs are float32 arrays (bf16 inputs arrive already widened, which is
+ * exact); every value is widened to double on read and nothing is rounded
+ * back.  Layout per head: q,k [T][dk], v [T][dv], beta [T],
+ * log_alpha [T][dk] (mode 2) or [T] (mode 1) or unused (mode 0),
+ * h0 and hT [dk][dv] (double), o [T][dv] (double).
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_ALPHA_NONE 0
+#define ORACLE_ALPHA_SCALAR 1
+#define ORACLE_ALPHA_CHANNEL 2
+
+/* Returns 0 on success, -1 on bad arguments, -2 if scratch allocation fails. */
+int kda_oracle_recurrent(const float *q, const float *k, const float *v,
+                         const float *beta, const float *log_alpha,
+                         int alpha_mode, const double *h0, long T, int dk,
+                         int dv, double *o, double *hT) {
+  if (T < 0 || dk <= 0 || dv <= 0 || !o || !hT) return -1;
+  if (alpha_mode < 0 || alpha_mode > 2) return -1;
+  if (alpha_mode != ORACLE_ALPHA_NONE && !log_alpha) return -1;
+  if (T > 0 && (!q || !k || !v || !beta)) return -1;
+
+  double *S = hT; /* the state lives in the output buffer */
+  double *a = (double *)malloc(sizeof(double) * (size_t)dk);
+  double *kd = (double *)malloc(sizeof(double) * (size_t)dk);
+  double *u = (double *)malloc(sizeof(double) * (size_t)dv);
+  if (!a || !kd || !u) {
+    free(a); free(kd); free(u);
+    return -2;
+  }
+  if (h0)
+    memcpy(S, h0, sizeof(double) * (size_t)dk * (size_t)dv);
+  else
+    memset(S, 0, sizeof(double) * (size_t)dk * (size_t)dv);
+
+  for (long t = 0; t < T; ++t) {
+    const float *qt = q + t * dk;
+    const float *kt = k + t * dk;
+    const float *vt = v + t * dv;
+    const double bt = (double)beta[t];
+
+    /* decay: a = exp(-exp(log_alpha)) */
+    for (int i = 0; i < dk; ++i) {
+      if (alpha_mode == ORACLE_ALPHA_CHANNEL)
+        a[i] = exp(-exp((double)log_alpha[t * dk + i]));
+      else if (alpha_mode == ORACLE_ALPHA_SCALAR)
+        a[i] = exp(-exp((double)log_alpha[t]));
+      else
+        a[i] = 1.0;
+      kd[i] = (double)kt[i];
+    }
+    /* S <- Diag(a) S */
+    for (int i = 0; i < dk; ++i) {
+      double *row = S + (size_t)i * dv;
+      for (int j = 0; j < dv; ++j) row[j] *= a[i];
+    }
+    /* u = beta (v - S^T k) */
+    for (int j = 0; j < dv; ++j) u[j] = 0.0;
+    for (int i = 0; i < dk; ++i) {
+      const double *row = S + (size_t)i * dv;
+      for (int j = 0; j < dv; ++j) u[j] += kd[i] * row[j];
+    }
+    for (int j = 0; j < dv; ++j) u[j] = bt * ((double)vt[j] - u[j]);
+    /* S <- S + k u^T */
+    for (int i = 0; i < dk; ++i) {
+      double *row = S + (size_t)i * dv;
+      for (int j = 0; j < dv; ++j) row[j] += kd[i] * u[j];
+    }
+    /* o_t = S^T q */
+    double *ot = o + t * dv;
+    for (int j = 0; j < dv; ++j) ot[j] = 0.0;
+    for (int i = 0; i < dk; ++i) {
+      const double *row = S + (size_t)i * dv;
+      const double qi = (double)qt[i];
+      for (int j = 0; j < dv; ++j) ot[j] += qi * row[j];
+    }
+  }
+  free(a); free(kd); free(u);
+  return 0;
+}
+
+/* Interface version, so the Python side can refuse a stale build. */
+int kda_oracle_version(void) { return 1; }
