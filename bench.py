@@ -1,0 +1,495 @@
+#!/usr/bin/env python3
+"""Benchmark of the gated delta-rule hot path on GB300.
+
+One JSON line on stdout (rank 0).  The headline workload is the KDA
+long-context chunked prefill (B=1, H=32, T=131072, dk=dv=128, C=64, bf16
+q/k/v, float32 state, per-channel decay): ``value`` is tokens/s (B*T tokens,
+all heads) with inputs already resident in HBM.  The same run measures the
+KDA decode step (256 sequences x 32 heads, d=128, float32 state updated in
+place, 1000 steps over a cycled pool of 16 token sets) and reports its state
+GB/s under ``decode``.
+
+Timing: W warm-up calls, then K timed calls bracketed by a barrier and
+``torch.cuda.synchronize()`` on both sides, CUDA events on the launching
+stream, max over ranks.  Inputs (6.4 GB per prefill call, 0.54 GB of decode
+state) are larger than the 129 MB L2, so no flush is needed between calls.
+
+``--impl reference`` times the float64 CPU oracle instead (the reference arm:
+this method has no reference implementation, so the oracle, as it stands, is
+the comparison program), on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import platform
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "KDA chunked prefill tokens/s (H=32,d=128); decode-step state GB/s vs HBM peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ---------------------------------------------------------------- workload accounting
+
+def prefill_algorithmic_bytes(w):
+    """Bytes a prefill call must move at least: q, k, v and o once each in
+    their storage type, beta and log_alpha once, h0 / hT once each."""
+    es = 2 if w.dtype == "bf16" else 4
+    per_token_head = es * (2 * w.dk + w.dv) + 4 + es * w.dv
+    per_token_head += {"none": 0, "scalar": 4, "channel": 4 * w.dk}[w.alpha]
+    state = 4 * w.dk * w.dv * (2 if w.h0_sd > 0 else 1)
+    return w.B * w.H * (w.T * per_token_head + state)
+
+
+def prefill_algorithmic_flops(w):
+    """Triangle-exploited flop count per call: 6 d^2 + 5 C d + C^2/3 per
+    token-head (state products W S, Q S, K^T u at 2 dk dv each; A, W, U, M,
+    M u at about C d each with the triangles skipped; the C x C solve)."""
+    d = w.dk
+    return w.B * w.H * w.T * (6 * d * d + 5 * w.C * d + w.C * w.C / 3.0)
+
+
+def decode_algorithmic_bytes(w):
+    es = 2 if w.dtype == "bf16" else 4
+    la = {"none": 0, "scalar": 4, "channel": 4 * w.dk}[w.alpha]
+    per_state = 2 * 4 * w.dk * w.dv + es * (2 * w.dk + w.dv) + la + 4 + es * w.dv
+    return w.N * w.H * per_state
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "gated_delta_rule_wise_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, src_hash):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel)
+    if not e or e.get("source_hash") != src_hash:
+        return None
+    return e.get("bytes_per_launch")
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return None
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]),
+                                 power=float(parts[3]) if parts[3] not in ("[N/A]", "") else 0.0,
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], swp=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        busy = [r for r in rows if r["power"] > 0.25 * max(x["power"] for x in rows)] or rows
+        reasons = sorted({name for r in rows for name, key in
+                          (("hw_slowdown", "hw"), ("hw_thermal_slowdown", "hwt"),
+                           ("sw_thermal_slowdown", "swt"), ("sw_power_cap", "swp"))
+                          if r[key].lower() == "active"})
+        return {"sm_mhz": float(np.median([r["sm"] for r in busy])),
+                "sm_max_mhz": max(r["smax"] for r in rows), "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(r["power"] for r in rows)}
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, 0, None
+    import torch.distributed as dist
+    rank = int(os.environ["RANK"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    import torch
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if backend == "nccl":
+        torch.cuda.set_device(local)
+    dist.init_process_group(backend=backend)
+    return rank, ws, local, dist
+
+
+def barrier(dist, torch_mod=None):
+    if torch_mod is not None and torch_mod.cuda.is_available():
+        torch_mod.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    if torch_mod is not None and torch_mod.cuda.is_available():
+        torch_mod.cuda.synchronize()
+
+
+def max_over_ranks(x, dist, device=None):
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- oracle timing
+
+def oracle_prefill_rate(w, heads, T_sample, threads):
+    """Tokens/s of the float64 oracle on ``heads`` x the first T_sample tokens
+    of workload ``w``, one thread per head; scaled to whole tokens (all H
+    heads per token)."""
+    import oracle
+    oracle.build()
+    x = W.prefill_inputs(w.with_(T=T_sample), heads=heads)
+    la = x["log_alpha"]
+    t0 = time.perf_counter()
+    oracle.recurrent_heads(x["q"][:, None], x["k"][:, None], x["v"][:, None], x["beta"][:, None],
+                           None if la is None else la[:, None],
+                           None if x["h0"] is None else x["h0"][:, None], threads=threads)
+    dt = time.perf_counter() - t0
+    token_heads = len(heads) * T_sample
+    return token_heads / dt / w.H, dt, token_heads
+
+
+def cpu_info():
+    model = platform.processor() or platform.machine()
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                model = line.split(":", 1)[1].strip()
+                break
+    except OSError:
+        pass
+    return model
+
+
+def run_reference(args, rank, world, dist):
+    """The reference arm: the float64 oracle on host cores, rank 0 only."""
+    if rank != 0:
+        return 0
+    w = W.KDA_PREFILL_BF16
+    threads = max(1, min(os.cpu_count() or 1, w.H))
+    heads = [(0, h) for h in range(threads)]
+    T_s = args.ref_tokens
+    rates, times = [], []
+    for i in range(args.warmup + args.steps):
+        r, dt, n = oracle_prefill_rate(w, heads, T_s, threads)
+        if i >= args.warmup:
+            rates.append(r)
+            times.append(dt)
+    value = float(np.median(rates))
+    sample = (f"{threads} of {w.H} heads x first {T_s} of {w.T} tokens per step "
+              f"({threads * T_s} token-heads), float64, one thread per head; tokens/s = "
+              f"token-heads/s / H")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * float(np.median(times)), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{w.name}: B={w.B} H={w.H} T={w.T} dk=dv={w.dk} C={w.C} "
+                                   f"bf16 inputs, per-channel decay (oracle on a sample)"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
+                             "kind": "oracle", "sample": sample, "cpu": cpu_info()},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+
+def fill_prefill_host(w, torch):
+    """Pinned host tensors holding the workload in its storage types."""
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    B, H, T = w.B, w.H, w.T
+    h = dict(q=torch.empty((B, H, T, w.dk), dtype=dt, pin_memory=True),
+             k=torch.empty((B, H, T, w.dk), dtype=dt, pin_memory=True),
+             v=torch.empty((B, H, T, w.dv), dtype=dt, pin_memory=True),
+             beta=torch.empty((B, H, T), dtype=torch.float32, pin_memory=True))
+    if w.alpha == "channel":
+        h["log_alpha"] = torch.empty((B, H, T, w.dk), dtype=torch.float32, pin_memory=True)
+    elif w.alpha == "scalar":
+        h["log_alpha"] = torch.empty((B, H, T), dtype=torch.float32, pin_memory=True)
+    else:
+        h["log_alpha"] = None
+    h["h0"] = (torch.empty((B, H, w.dk, w.dv), dtype=torch.float32, pin_memory=True)
+               if w.h0_sd > 0 else None)
+
+    def sink(b, hh, d):
+        for key, t in h.items():
+            if t is not None:
+                t[b, hh].copy_(torch.from_numpy(d[key]).to(t.dtype))
+
+    W.prefill_inputs(w, sink=sink)
+    return h
+
+
+def run_ours(args, rank, world, local, dist):
+    import torch
+
+    import gated_delta_rule_wise_gb300 as kda
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    kda.load_library()
+    stream = torch.cuda.current_stream(dev)
+    peaks, peak_src = load_peaks()
+    w = W.KDA_PREFILL_BF16
+    wd = W.KDA_DECODE_BF16
+
+    # ---- inputs
+    t0 = time.perf_counter()
+    host = fill_prefill_host(w, torch)
+    log(f"[bench] generated {w.name} inputs in {time.perf_counter() - t0:.1f}s")
+    d = {k: (None if v is None else v.to(dev, non_blocking=False)) for k, v in host.items()}
+    o = torch.empty((w.B, w.H, w.T, w.dv), dtype=torch.bfloat16, device=dev)
+    hT = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
+    ws = kda.workspace_for(d["q"], d["v"], w.C, d["log_alpha"])
+    meta = (w.B, w.H, w.T, w.dk, w.dv, w.C, kda.KDA_BF16, kda.KDA_ALPHA_CHANNEL)
+    launches_per_call = kda.kda_chunk_fwd_launches(*meta)
+    knames = kda.kda_chunk_fwd_kernel_names(*meta)
+
+    def prefill(events=None):
+        kda.kda_chunk_fwd_ex(d["q"], d["k"], d["v"], d["beta"], d["log_alpha"], d["h0"], o, hT,
+                             w.C, ws, stream, kda.KDA_PATH_AUTO, events)
+
+    # per-step events: one before each kernel launch of the call, one after the last
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(launches_per_call + 1)]
+          for _ in range(args.steps)]
+    for row in ev:           # create the CUDA events (torch creates them on first record)
+        for e in row:
+            e.record(stream)
+    for _ in range(args.warmup):
+        prefill()
+    kda.kda_chunk_fwd_status(ws, stream)
+
+    with ClockSampler(local) as clk:
+        barrier(dist, torch)
+        for i in range(args.steps):
+            prefill(ev[i])
+        barrier(dist, torch)
+    kda.kda_chunk_fwd_status(ws, stream)
+    step_ms = [ev[i][0].elapsed_time(ev[i][-1]) for i in range(args.steps)]
+    per_kernel = {n: float(np.mean([ev[i][j].elapsed_time(ev[i][j + 1])
+                                    for i in range(args.steps)]))
+                  for j, n in enumerate(knames)}
+    ms_step = max_over_ranks(float(np.mean(step_ms)), dist, dev)
+    tokens = w.B * w.T
+    value = world * tokens / (ms_step * 1e-3)
+    clocks = clk.summary()
+
+    # ---- roofline of the dominant kernel, timed inside the timed region
+    alg_bytes = prefill_algorithmic_bytes(w)
+    alg_flops = prefill_algorithmic_flops(w)
+    kname, kms = max(per_kernel.items(), key=lambda kv: kv[1])
+    src_hash = kernel_source_hash(kda.kernel_sources(kname))
+    roof = {"kernel": kname, "bound": "hbm", "unit": "GB/s",
+            "achieved": alg_bytes / (kms * 1e-3) / 1e9,
+            "peak": peaks["hbm_gbs"], "peak_source": f"{peak_src} hbm_gbs (burst copy)",
+            "traffic": recorded_traffic(kname, src_hash),
+            "kernel_ms": kms, "kernel_ms_all": per_kernel,
+            "algorithmic_bytes_per_launch": alg_bytes,
+            "algorithmic_flops_per_launch": alg_flops,
+            "tensor_tflops_per_call": alg_flops / (ms_step * 1e-3) / 1e12}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+
+    # ---- end to end through the public API with host buffers
+    h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
+    o_host = torch.empty_like(o, device="cpu").pin_memory()
+    hT_host = torch.empty_like(hT, device="cpu").pin_memory()
+    d2h = o_host.numel() * o_host.element_size() + hT_host.numel() * hT_host.element_size()
+
+    def e2e_step():
+        for key, t in host.items():
+            if t is not None:
+                d[key].copy_(t, non_blocking=True)
+        prefill()
+        o_host.copy_(o, non_blocking=True)
+        hT_host.copy_(hT, non_blocking=True)
+
+    for _ in range(min(2, args.warmup)):
+        e2e_step()
+    e2e_steps = max(1, min(args.steps, 5))
+    barrier(dist, torch)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier(dist, torch)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, dev)
+    e2e = {"value": world * tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+           "steps": e2e_steps}
+    del d, host, o, hT, ws, o_host, hT_host
+    torch.cuda.empty_cache()
+
+    # ---- decode
+    dec = None
+    if args.decode_steps > 0:
+        S = torch.from_numpy(W.decode_state(wd)).to(dev)
+        pool = []
+        for i in range(wd.pool):
+            tk = W.decode_tokens(wd, i)
+            pool.append({k: (None if v is None else torch.from_numpy(v).to(dev).to(
+                torch.bfloat16 if k in ("q", "k", "v") else torch.float32))
+                for k, v in tk.items()})
+        od = torch.empty((wd.N, wd.H, wd.dv), dtype=torch.bfloat16, device=dev)
+
+        def dstep(i):
+            p = pool[i % wd.pool]
+            kda.kda_decode_step(p["q"], p["k"], p["v"], p["beta"], p["log_alpha"], S, od, stream)
+
+        for i in range(max(3, args.warmup)):
+            dstep(i)
+        with ClockSampler(local) as dclk:
+            barrier(dist, torch)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for i in range(args.decode_steps):
+                dstep(i)
+            b.record(stream)
+            barrier(dist, torch)
+        dms = max_over_ranks(a.elapsed_time(b) / args.decode_steps, dist, dev)
+        dbytes = decode_algorithmic_bytes(wd)
+        dsrc = kernel_source_hash(["kda_decode.cu", "kda_internal.cuh"])
+        dec = {"workload": f"{wd.name}: N={wd.N} H={wd.H} dk=dv={wd.dk} fp32 state "
+                           f"({4 * wd.N * wd.H * wd.dk * wd.dv / 1e6:.0f} MB) in place, bf16 q/k/v, "
+                           f"per-channel decay, {args.decode_steps} steps over {wd.pool} token sets",
+               "value": world * dbytes / (dms * 1e-3) / 1e9, "unit": "GB/s",
+               "ms_per_step": dms, "tokens_per_s": world * wd.N / (dms * 1e-3),
+               "gpu_launches": args.decode_steps,
+               "roofline": {"kernel": "decode_step_kernel", "bound": "hbm", "unit": "GB/s",
+                            "achieved": dbytes / (dms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+                            "frac": dbytes / (dms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                            "peak_source": f"{peak_src} hbm_gbs (burst copy)",
+                            "traffic": recorded_traffic("decode_step_kernel", dsrc),
+                            "algorithmic_bytes_per_launch": dbytes},
+               "clocks": dclk.summary()}
+        del S, pool, od
+        torch.cuda.empty_cache()
+
+    # ---- CPU baseline (rank 0, one GPU only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = max(1, min(os.cpu_count() or 1, w.H))
+        heads = [(0, h) for h in range(threads)]
+        rate, dt, n = oracle_prefill_rate(w, heads, args.cpu_tokens, threads)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"{threads} of {w.H} heads x first {args.cpu_tokens} tokens "
+                         f"({n} token-heads) in {dt:.1f}s, float64, one thread per head; "
+                         f"tokens/s = token-heads/s / H",
+               "cpu": cpu_info()}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": f"{w.name}: B={w.B} H={w.H} T={w.T} dk=dv={w.dk} "
+                                       f"C={w.C}, bf16 q/k/v, fp32 state, per-channel decay "
+                                       f"log_alpha~N({w.la_mu},{w.la_sd}), h0=0, seed {w.seed}",
+                           "per_gpu_tokens": tokens,
+                           "l2": f"inputs larger than L2 ({alg_bytes / 1e9:.1f} GB per call); "
+                                 f"no flush",
+                           "parallelism": f"replicas x{world}"},
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": launches_per_call * args.steps,
+                "clocks": clocks, "decode": dec}
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--decode-steps", type=int, default=1000)
+    ap.add_argument("--cpu-tokens", type=int, default=131072,
+                    help="tokens per head in the CPU-baseline sample")
+    ap.add_argument("--ref-tokens", type=int, default=16384,
+                    help="tokens per head in each reference-arm step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local, dist = dist_setup()
+    try:
+        if args.impl == "reference":
+            return run_reference(args, rank, world, dist)
+        return run_ours(args, rank, world, local, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,206 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) gated delta-rule library (libkda.so).
+ *
+ * The library computes the gated delta rule behind DeltaNet, Gated DeltaNet
+ * and Kimi Delta Attention (KDA), one level below the token mixer's
+ * projections.  For each (batch, head), with column vectors, a state
+ * S in R^{dk x dv} (row i belongs to key channel i) and t = 0 .. T-1:
+ *
+ *     a_t = exp(-exp(log_alpha_t))            per key channel, per token, or 1
+ *     S   = (I - beta_t k_t k_t^T) Diag(a_t) S + beta_t k_t v_t^T
+ *     o_t = S^T q_t                           read-out after the write
+ *
+ * Sources, by page title and section:
+ *  - delta rule, read / correct / write, read-out without a normaliser:
+ *    "22,580: From GPT-2 to Kimi K3" (yichencityu.github.io), section 5.2.
+ *  - gated form S_t = a_t (I - b_t k_t k_t^T) S_{t-1} + b_t k_t v_t^T:
+ *    "22580: From GPT-2 to Kimi3, Explained" (zharfai.com), "Gated DeltaNet
+ *    adds controlled forgetting"; decay applied first for a per-channel a_t.
+ *  - per-channel decay alpha = exp(-exp(log_alpha)): "22580: From GPT-2 to
+ *    Kimi K3, Explained" (lukebest.github.io), "KDA (per-channel alpha)".
+ *  - the chunk-wise parallel form (WY representation, forward substitution on
+ *    a C x C unit lower-triangular matrix, W = T K_beta, U = T V_beta, then a
+ *    sequential pass over chunks): "22,580: From GPT-2 to Kimi K3"
+ *    (yichencityu.github.io), section 6.3.
+ *  - the state is the cache handed from call to call ("state in, state out"):
+ *    same page, section 5.2, forward(x, cache) -> (o, S).
+ *
+ * Conventions for every entry point
+ *  - All tensors are dense, contiguous, row-major, in DEVICE memory unless
+ *    stated; the caller allocates and owns them.  The library allocates no
+ *    device memory and keeps no state between calls.
+ *  - Every device pointer must be 16-byte aligned; the workspace 256-byte
+ *    aligned.  Misaligned pointers return KDA_ERR_INVALID_ARG.
+ *  - Calls are asynchronous on `stream` (NULL = legacy default stream) and
+ *    never synchronise, except kda_chunk_fwd_status.  Arguments are checked
+ *    before anything is launched; on an error status nothing was launched.
+ *  - Outputs must not overlap inputs, except as stated (h0 == hT; the decode
+ *    state is updated in place).
+ *  - No C++ exception crosses this interface.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream; declared here so that including this
+ * header needs no CUDA include path. */
+struct CUstream_st;
+typedef struct CUstream_st *kda_stream_t;
+
+typedef enum {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARG = 1, /* null / misaligned pointer, negative size, bad enum */
+  KDA_ERR_UNSUPPORTED = 2, /* valid but outside the supported shapes */
+  KDA_ERR_CUDA = 3,        /* a CUDA launch or runtime call failed */
+  KDA_ERR_TIMEOUT = 4      /* a bounded on-device wait expired (see kda_chunk_fwd_status) */
+} kda_status;
+
+/* Storage type of q, k, v and o.  beta, log_alpha, h0, hT and the decode
+ * state are always float32. */
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+/* Decay mode, i.e. the shape of log_alpha. */
+typedef enum {
+  KDA_ALPHA_NONE = 0,    /* a = 1 (DeltaNet); log_alpha must be NULL        */
+  KDA_ALPHA_SCALAR = 1,  /* one value per token and head (Gated DeltaNet)   */
+  KDA_ALPHA_CHANNEL = 2  /* one value per token, head and key channel (KDA) */
+} kda_alpha_mode;
+
+/* Implementation choice for kda_chunk_fwd_ex. */
+typedef enum {
+  KDA_PATH_AUTO = 0,     /* tensor-core path where supported, else CUDA cores */
+  KDA_PATH_CUDA_CORE = 1,/* fp32 FFMA chunked kernel (every supported shape)   */
+  KDA_PATH_TENSOR = 2    /* tcgen05 prep + scan (bf16, C = 64, dk,dv in {64,128});
+                            KDA_ERR_UNSUPPORTED elsewhere                       */
+} kda_path;
+
+/* ABI version of this header; kda_abi_version() returns the library's. */
+#define KDA_ABI_VERSION 1
+int kda_abi_version(void);
+
+/* Human-readable name of a status; never NULL; static storage. */
+const char *kda_status_string(kda_status s);
+
+/*
+ * Bytes of device workspace kda_chunk_fwd needs for this problem (>= 256).
+ * Returns 0 if the arguments are invalid or unsupported.  The workspace holds
+ * a device error word (first 256 bytes) and, on the tensor-core path, the
+ * per-chunk intermediates of the prep kernel (corrected keys and values,
+ * decayed queries, the intra-chunk mask and decay factors).
+ */
+size_t kda_chunk_fwd_workspace_size(int B, int H, int T, int dk, int dv, int C,
+                                    kda_dtype dt, kda_alpha_mode am);
+size_t kda_chunk_fwd_workspace_size_ex(int B, int H, int T, int dk, int dv, int C,
+                                       kda_dtype dt, kda_alpha_mode am, kda_path path);
+
+/*
+ * Chunk-wise parallel prefill of the gated delta rule ("22,580: From GPT-2 to
+ * Kimi K3" (yichencityu.github.io), section 6.3, extended with the cumulative
+ * per-channel decay).
+ *
+ *   q, k      [B, H, T, dk]  dtype dt            (device)
+ *   v         [B, H, T, dv]  dtype dt            (device)
+ *   beta      [B, H, T]      float32             (device)
+ *   log_alpha [B, H, T] (SCALAR) or [B, H, T, dk] (CHANNEL) float32, NULL for NONE
+ *   h0        [B, H, dk, dv] float32, or NULL for a zero initial state
+ *   o         [B, H, T, dv]  dtype dt            (device, written)
+ *   hT        [B, H, dk, dv] float32, or NULL    (device, written; may equal h0)
+ *   B, H >= 0; T >= 0 (any length: a partial last chunk is handled);
+ *   dk, dv in {16, 32, 64, 128}; C in {16, 32, 64} (chunk length);
+ *   workspace: >= kda_chunk_fwd_workspace_size(...) bytes of device memory,
+ *   256-byte aligned, owned by the caller, not shared with a concurrent call.
+ *
+ * No scaling is applied to q.k (the caller normalises q and k).  o_t includes
+ * token t's own write.  Precision: the CUDA-core path computes in float32;
+ * the tensor path uses bf16 operands with float32 accumulation and a float32
+ * state.  Returns KDA_OK once the work is enqueued.  Device-side failures
+ * (a bounded wait that expired) are reported by kda_chunk_fwd_status.
+ */
+kda_status kda_chunk_fwd(const void *q, const void *k, const void *v,
+                         const float *beta, const float *log_alpha,
+                         const float *h0, void *o, float *hT,
+                         int B, int H, int T, int dk, int dv, int C,
+                         kda_dtype dt, kda_alpha_mode am,
+                         void *workspace, size_t workspace_bytes,
+                         kda_stream_t stream);
+
+/*
+ * kda_chunk_fwd with an explicit implementation choice and optional launch
+ * timing.  `events` (may be NULL when n_events == 0) holds cudaEvent_t
+ * handles created by the caller; when n_events >= launches + 1 (launches =
+ * kda_chunk_fwd_launches(...)), events[i] is recorded on `stream` just before
+ * kernel launch i and events[launches] after the last one, so the caller can
+ * time each kernel of the call.  Recording changes no work.  Fewer events
+ * than needed: KDA_ERR_INVALID_ARG.
+ */
+kda_status kda_chunk_fwd_ex(const void *q, const void *k, const void *v,
+                            const float *beta, const float *log_alpha,
+                            const float *h0, void *o, float *hT,
+                            int B, int H, int T, int dk, int dv, int C,
+                            kda_dtype dt, kda_alpha_mode am,
+                            void *workspace, size_t workspace_bytes,
+                            kda_stream_t stream, kda_path path,
+                            void *const *events, int n_events);
+
+/* Number of kernel launches one kda_chunk_fwd_ex call makes for this problem
+ * (0 for an empty problem), or -1 if the arguments are invalid/unsupported. */
+int kda_chunk_fwd_launches(int B, int H, int T, int dk, int dv, int C,
+                           kda_dtype dt, kda_alpha_mode am, kda_path path);
+
+/* Name of kernel launch `i` of such a call (static storage), or NULL. */
+const char *kda_chunk_fwd_kernel_name(int B, int H, int T, int dk, int dv, int C,
+                                      kda_dtype dt, kda_alpha_mode am,
+                                      kda_path path, int i);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word of
+ * `workspace`.  KDA_OK if every call enqueued with this workspace finished
+ * normally; KDA_ERR_TIMEOUT if an on-device wait gave up (the outputs of that
+ * call are then undefined); KDA_ERR_CUDA if the synchronisation failed.
+ */
+kda_status kda_chunk_fwd_status(void *workspace, kda_stream_t stream);
+
+/*
+ * One recurrent decode step for N x H independent states, in place
+ * ("22,580: From GPT-2 to Kimi K3" (yichencityu.github.io), section 5.2, with
+ * t = 1 and the cached state; decay as in kda_chunk_fwd):
+ *
+ *   S = Diag(a) S;  u = beta (v - S^T k);  S = S + k u^T;  o = S^T q
+ *
+ *   q, k      [N, H, dk]  dtype dt
+ *   v         [N, H, dv]  dtype dt
+ *   beta      [N, H]      float32
+ *   log_alpha [N, H] (SCALAR) or [N, H, dk] (CHANNEL) float32, NULL for NONE
+ *   S_inout   [N, H, dk, dv] float32, read and overwritten in place
+ *   o         [N, H, dv]  dtype dt (written)
+ *   N, H >= 0; dk, dv in {16, 32, 64, 128}.
+ * The state is read once and written once (float32 arithmetic throughout).
+ */
+kda_status kda_decode_step(const void *q, const void *k, const void *v,
+                           const float *beta, const float *log_alpha,
+                           float *S_inout, void *o,
+                           int N, int H, int dk, int dv,
+                           kda_dtype dt, kda_alpha_mode am, kda_stream_t stream);
+
+/*
+ * Device self-test of the bounded-wait mechanism: launches one block that
+ * waits on an mbarrier nothing will ever complete, with a wait limit of
+ * `spin_limit` polls.  The wait gives up, the kernel records
+ * KDA_ERR_TIMEOUT in the workspace's error word and returns normally, so the
+ * CUDA context stays usable.  Read the result with kda_chunk_fwd_status.
+ * spin_limit must be in [1, 1<<20].
+ */
+kda_status kda_selftest_wait_timeout(void *workspace, size_t workspace_bytes,
+                                     unsigned spin_limit, kda_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,147 @@
+"""Host-side checks of the C ABI (no GPU needed, nothing is launched).
+
+- libkda.so builds, loads and exports every function include/kda.h declares;
+- status strings, ABI version, workspace sizing;
+- argument validation rejects bad calls before any launch (the pointers used
+  here are never dereferenced: every case fails a host-side check first).
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gated_delta_rule_wise_gb300 import build
+    build.build()
+    import gated_delta_rule_wise_gb300 as kda
+    return kda.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("kda_chunk_fwd", "kda_decode_step", "kda_chunk_fwd_workspace_size",
+                 "kda_status_string", "kda_chunk_fwd_status"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from gated_delta_rule_wise_gb300 import library_path
+    out = subprocess.run(["nm", "-D", "--defined-only", library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (kda_[a-z0-9_]+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, f"declared but not exported: {missing}"
+    for n in declared_functions():
+        assert getattr(lib, n) is not None
+
+
+def test_header_compiles_as_plain_c(tmp_path):
+    src = tmp_path / "use.c"
+    src.write_text('#include "kda.h"\nint main(void){ return kda_abi_version() == KDA_ABI_VERSION ? 0 : 1; }\n')
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-c", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-o", str(tmp_path / "use.o")], check=True)
+
+
+def test_status_strings_and_version(lib):
+    import gated_delta_rule_wise_gb300 as kda
+    assert kda.kda_abi_version() == kda.ABI_VERSION
+    for code in range(5):
+        s = kda.kda_status_string(code)
+        assert s.startswith("KDA_")
+    assert "unknown" in kda.kda_status_string(99)
+
+
+def test_workspace_size(lib):
+    import gated_delta_rule_wise_gb300 as kda
+    ws = kda.kda_chunk_fwd_workspace_size
+    assert ws(1, 1, 64, 16, 16, 16, kda.KDA_F32, kda.KDA_ALPHA_CHANNEL) >= 256
+    assert ws(1, 32, 131072, 128, 128, 64, kda.KDA_BF16, kda.KDA_ALPHA_CHANNEL) >= 256
+    assert ws(1, 1, 64, 24, 16, 16, kda.KDA_F32, kda.KDA_ALPHA_NONE) == 0      # dk unsupported
+    assert ws(1, 1, 64, 16, 16, 8, kda.KDA_F32, kda.KDA_ALPHA_NONE) == 0       # C unsupported
+    assert ws(-1, 1, 64, 16, 16, 16, kda.KDA_F32, kda.KDA_ALPHA_NONE) == 0     # negative
+    assert ws(1, 1, 64, 16, 16, 16, 7, kda.KDA_ALPHA_NONE) == 0                # bad dtype
+    assert ws(1, 1, 64, 16, 16, 16, kda.KDA_F32, 9) == 0                       # bad mode
+    assert ws(1, 1, 64, 16, 16, 16, kda.KDA_F32, kda.KDA_ALPHA_NONE, 5) == 0   # bad path
+
+
+FAKE = 0x7f0000000000  # 256-byte aligned, never dereferenced by these cases
+
+
+def _chunk(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, beta=FAKE, la=FAKE, h0=None, o=FAKE, hT=FAKE,
+             B=1, H=1, T=64, dk=16, dv=16, C=16, dt=0, am=2, ws=FAKE, wsb=1 << 20, st=None, path=0,
+             ev=None, nev=0)
+    a.update(kw)
+    return lib.kda_chunk_fwd_ex(a["q"], a["k"], a["v"], a["beta"], a["la"], a["h0"], a["o"],
+                                a["hT"], a["B"], a["H"], a["T"], a["dk"], a["dv"], a["C"],
+                                a["dt"], a["am"], a["ws"], a["wsb"], a["st"], a["path"],
+                                a["ev"], a["nev"])
+
+
+def test_chunk_argument_validation(lib):
+    INV, UNS, OK = 1, 2, 0
+    assert _chunk(lib, q=None) == INV
+    assert _chunk(lib, o=None) == INV
+    assert _chunk(lib, k=FAKE + 8) == INV            # misaligned
+    assert _chunk(lib, ws=FAKE + 16) == INV          # workspace must be 256-aligned
+    assert _chunk(lib, wsb=16) == INV                # workspace too small
+    assert _chunk(lib, la=None) == INV               # decay mode needs log_alpha
+    assert _chunk(lib, am=0) == INV                  # ... and NONE forbids it
+    assert _chunk(lib, dk=48) == UNS
+    assert _chunk(lib, dv=256) == UNS
+    assert _chunk(lib, C=128) == UNS
+    assert _chunk(lib, B=-1) == INV
+    assert _chunk(lib, dt=3) == INV
+    assert _chunk(lib, B=70000, H=1) == UNS
+    assert _chunk(lib, path=2, dt=0) == UNS          # tensor path needs bf16
+    assert _chunk(lib, nev=2) == INV                 # events requested but NULL
+    one = (ctypes.c_void_p * 1)(FAKE)
+    assert _chunk(lib, ev=one, nev=1) == INV         # fewer events than launches + 1
+    assert _chunk(lib, B=0) == OK                    # nothing to do, nothing launched
+    assert _chunk(lib, H=0, q=None, k=None, v=None) == OK
+
+
+def test_decode_argument_validation(lib):
+    f = lib.kda_decode_step
+    args = lambda **kw: [kw.get(n, d) for n, d in (
+        ("q", FAKE), ("k", FAKE), ("v", FAKE), ("beta", FAKE), ("la", FAKE), ("S", FAKE),
+        ("o", FAKE), ("N", 4), ("H", 2), ("dk", 128), ("dv", 128), ("dt", 1), ("am", 2),
+        ("st", None))]
+    assert f(*args(S=None)) == 1
+    assert f(*args(S=FAKE + 4)) == 1
+    assert f(*args(la=None)) == 1
+    assert f(*args(am=0)) == 1
+    assert f(*args(dk=100)) == 2
+    assert f(*args(N=-3)) == 1
+    assert f(*args(N=0)) == 0
+
+
+def test_launch_queries(lib):
+    import gated_delta_rule_wise_gb300 as kda
+    assert kda.kda_chunk_fwd_launches(1, 1, 64, 16, 16, 16, kda.KDA_F32, 2) >= 1
+    assert kda.kda_chunk_fwd_launches(0, 1, 64, 16, 16, 16, kda.KDA_F32, 2) == 0
+    assert kda.kda_chunk_fwd_launches(1, 1, 64, 24, 16, 16, kda.KDA_F32, 2) == -1
+    names = kda.kda_chunk_fwd_kernel_names(1, 32, 131072, 128, 128, 64, kda.KDA_BF16, 2)
+    assert names and all(n in kda.KERNEL_SOURCES for n in names)
+    for n, files in kda.KERNEL_SOURCES.items():
+        for f in files:
+            assert os.path.exists(os.path.join(ROOT, "gated_delta_rule_wise_gb300", "csrc", f))
+
+
+def test_status_and_selftest_validation(lib):
+    assert lib.kda_chunk_fwd_status(None, None) == 1
+    assert lib.kda_selftest_wait_timeout(FAKE, 256, 0, None) == 1
+    assert lib.kda_selftest_wait_timeout(FAKE, 16, 10, None) == 1

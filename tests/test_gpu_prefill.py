@@ -1,0 +1,188 @@
+"""GPU parity of kda_chunk_fwd against the float64 oracle.
+
+Bar: max|o_gpu - o_ref| <= tol * max|o_ref| and the same for hT, with
+tol = 1e-4 for float32 workloads and 2e-2 for bf16-input / float32-state ones.
+Small problems are checked on every element; the full-size workloads run on
+the GPU in full and are checked on a seeded sample of heads that the oracle
+steps through the whole sequence.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gated_delta_rule_wise_gb300 as kda
+import oracle
+import workloads as W
+from _gpu_helpers import (DEV, TOL_BF16, TOL_F32, device_inputs, device_inputs_streamed, put,
+                          rel_err, tdtype, tol_for)
+
+pytestmark = pytest.mark.gpu
+
+PATHS = {"auto": kda.KDA_PATH_AUTO, "cuda_core": kda.KDA_PATH_CUDA_CORE,
+         "tensor": kda.KDA_PATH_TENSOR}
+
+
+def tensor_path_ok(w):
+    return kda.kda_chunk_fwd_workspace_size(w.B, w.H, w.T, w.dk, w.dv, w.C,
+                                            kda.KDA_BF16 if w.dtype == "bf16" else kda.KDA_F32,
+                                            {"none": 0, "scalar": 1, "channel": 2}[w.alpha],
+                                            kda.KDA_PATH_TENSOR) > 0
+
+
+def run(w, d, path="auto", hT_out=True, h0=None):
+    o, hT = kda.chunk_fwd(d["q"], d["k"], d["v"], d["beta"], d["log_alpha"],
+                          d["h0"] if h0 is None else h0, C=w.C, output_final_state=hT_out,
+                          path=PATHS[path])
+    torch.cuda.synchronize()
+    return o, hT
+
+
+def check_full(w, path="auto", x=None):
+    x = x if x is not None else W.prefill_inputs(w)
+    d = device_inputs(w, x)
+    o, hT = run(w, d, path)
+    o_ref, h_ref = oracle.recurrent_heads(x["q"], x["k"], x["v"], x["beta"], x["log_alpha"],
+                                          x["h0"])
+    tol = tol_for(w.dtype)
+    eo = rel_err(o.float().cpu().numpy().reshape(o_ref.shape), o_ref)
+    eh = rel_err(hT.cpu().numpy().reshape(h_ref.shape), h_ref)
+    assert eo <= tol and eh <= tol, f"{w.name} [{path}]: o {eo:.3e} hT {eh:.3e} (tol {tol})"
+    return eo, eh
+
+
+# ---------------------------------------------------------------- the five workloads
+
+def test_tiny_kda_fp32():
+    check_full(W.TINY_KDA_FP32)
+
+
+@pytest.mark.parametrize("path", ["auto", "cuda_core"])
+def test_deltanet_bf16(path):
+    check_full(W.DELTANET_BF16, path)
+
+
+def _sampled(w, n_heads, path="auto", seed=0):
+    d = device_inputs_streamed(w)
+    o, hT = run(w, d, path)
+    rng = np.random.default_rng(seed)
+    all_heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    pick = [all_heads[i] for i in sorted(rng.choice(len(all_heads), n_heads, replace=False))]
+    x = W.prefill_inputs(w, heads=pick)
+    o_ref, h_ref = oracle.recurrent_heads(x["q"][:, None], x["k"][:, None], x["v"][:, None],
+                                          x["beta"][:, None],
+                                          None if x["log_alpha"] is None else x["log_alpha"][:, None],
+                                          None if x["h0"] is None else x["h0"][:, None])
+    og = torch.stack([o[b, h] for b, h in pick]).float().cpu().numpy()
+    hg = torch.stack([hT[b, h] for b, h in pick]).cpu().numpy()
+    tol = tol_for(w.dtype)
+    eo, eh = rel_err(og, o_ref), rel_err(hg, h_ref)
+    assert eo <= tol and eh <= tol, f"{w.name} [{path}] sampled: o {eo:.3e} hT {eh:.3e}"
+
+
+def test_gdn_bf16_sampled_heads():
+    _sampled(W.GDN_BF16, 12)
+
+
+@pytest.mark.slow
+def test_kda_prefill_bf16_full_size_sampled_heads():
+    _sampled(W.KDA_PREFILL_BF16, 8, seed=1)
+
+
+# ---------------------------------------------------------------- shapes and edge cases
+
+SHAPES = [(16, 16, 16), (32, 16, 16), (16, 64, 32), (64, 64, 64), (128, 64, 64),
+          (64, 128, 64), (128, 128, 64), (128, 32, 32), (32, 128, 16)]
+
+
+@pytest.mark.parametrize("dk,dv,C", SHAPES)
+@pytest.mark.parametrize("alpha", ["none", "scalar", "channel"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_shapes_modes_ragged_tail(dk, dv, C, alpha, dtype):
+    """Several chunks plus a partial last chunk, two heads, initial state."""
+    w = W.Prefill("shape", B=1, H=2, T=3 * C + C // 2 + 1, dk=dk, dv=dv, C=C, dtype=dtype,
+                  alpha=alpha, la_mu=-3.5, h0_sd=0.05, seed=dk * 7 + dv + C)
+    check_full(w, "auto")
+    if dtype == "bf16":
+        check_full(w, "cuda_core")
+
+
+@pytest.mark.parametrize("T", [1, 5, 63, 64, 65, 130])
+def test_lengths_around_the_chunk(T):
+    check_full(W.KDA_PREFILL_BF16.with_(B=2, H=1, T=T, h0_sd=0.02, seed=T))
+
+
+def test_empty_sequence_copies_initial_state():
+    w = W.GDN_BF16.with_(B=2, H=3, T=0)
+    x = W.prefill_inputs(w)
+    d = device_inputs(w, x)
+    o, hT = run(w, d)
+    assert o.numel() == 0
+    np.testing.assert_array_equal(hT.cpu().numpy(), x["h0"])
+
+
+def test_in_place_state_and_split_resume():
+    """h0 == hT is allowed; [0, T1) then [T1, T) from the carried state equals one call."""
+    w = W.KDA_PREFILL_BF16.with_(B=1, H=3, T=320, h0_sd=0.02, seed=77)
+    x = W.prefill_inputs(w)
+    d = device_inputs(w, x)
+    o_full, h_full = run(w, d)
+    T1 = 192
+    sl = lambda t, a, b: None if t is None else t[:, :, a:b].contiguous()
+    S = d["h0"].clone()
+    outs = []
+    for a, b in ((0, T1), (T1, w.T)):
+        part = dict(q=sl(d["q"], a, b), k=sl(d["k"], a, b), v=sl(d["v"], a, b),
+                    beta=sl(d["beta"], a, b), log_alpha=sl(d["log_alpha"], a, b))
+        o = torch.empty_like(part["v"])
+        ws = kda.workspace_for(part["q"], part["v"], w.C, part["log_alpha"])
+        kda.kda_chunk_fwd(part["q"], part["k"], part["v"], part["beta"], part["log_alpha"],
+                          S, o, S, w.C, ws)           # in place: h0 is hT
+        outs.append(o)
+    torch.cuda.synchronize()
+    o_split = torch.cat(outs, dim=2)
+    assert rel_err(o_split.float().cpu().numpy(), o_full.float().cpu().numpy()) <= 1e-2
+    assert rel_err(S.cpu().numpy(), h_full.cpu().numpy()) <= 1e-2
+    o_ref, h_ref = oracle.recurrent_heads(x["q"], x["k"], x["v"], x["beta"], x["log_alpha"], x["h0"])
+    assert rel_err(S.cpu().numpy().reshape(h_ref.shape), h_ref) <= TOL_BF16
+
+
+def test_prefill_then_decode_equals_longer_prefill():
+    w = W.KDA_PREFILL_BF16.with_(B=2, H=2, T=129, seed=5)
+    x = W.prefill_inputs(w)
+    d = device_inputs(w, x)
+    o_long, h_long = run(w, d)
+    T0 = w.T - 1
+    sl = lambda t: None if t is None else t[:, :, :T0].contiguous()
+    o_p, S = kda.chunk_fwd(sl(d["q"]), sl(d["k"]), sl(d["v"]), sl(d["beta"]), sl(d["log_alpha"]),
+                           None, C=w.C)
+    last = lambda t: None if t is None else t[:, :, T0].contiguous()
+    o_d = kda.decode_step(last(d["q"]), last(d["k"]), last(d["v"]), last(d["beta"]),
+                          last(d["log_alpha"]), S)
+    torch.cuda.synchronize()
+    assert rel_err(o_d.float().cpu().numpy(), o_long[:, :, T0].float().cpu().numpy()) <= 1e-2
+    assert rel_err(S.cpu().numpy(), h_long.cpu().numpy()) <= 1e-2
+
+
+def test_identity_and_no_decay_limits():
+    """beta = 0 with no decay leaves S = h0; log_alpha = -inf equals no decay."""
+    w = W.GDN_BF16.with_(B=1, H=2, T=200, seed=3)
+    x = W.prefill_inputs(w)
+    x0 = dict(x, beta=np.zeros_like(x["beta"]), log_alpha=None)
+    d = device_inputs(w.with_(alpha="none"), x0)
+    o, hT = run(w, d)
+    np.testing.assert_allclose(hT.cpu().numpy(), x["h0"], rtol=0, atol=1e-6)
+    xi = dict(x, log_alpha=np.full_like(x["log_alpha"], -np.inf))
+    o1, h1 = run(w, device_inputs(w, xi))
+    o2, h2 = run(w.with_(alpha="none"), device_inputs(w.with_(alpha="none"), dict(x, log_alpha=None)))
+    assert rel_err(h1.cpu().numpy(), h2.cpu().numpy()) <= 1e-5
+    assert rel_err(o1.float().cpu().numpy(), o2.float().cpu().numpy()) <= 1e-2
+
+
+def test_timeout_selftest_reports_and_context_survives():
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    kda.kda_selftest_wait_timeout(ws, spin_limit=64)
+    with pytest.raises(kda.KdaError) as e:
+        kda.kda_chunk_fwd_status(ws)
+    assert e.value.status == 4  # KDA_ERR_TIMEOUT
+    kda.kda_chunk_fwd_status(ws)  # cleared by the read
+    check_full(W.TINY_KDA_FP32)   # the context still works
