@@ -418,7 +418,7 @@ def run_ours(args, rank, world, local, dist):
             barrier(dist, torch)
         dms = max_over_ranks(a.elapsed_time(b) / args.decode_steps, dist, dev)
         dbytes = decode_algorithmic_bytes(wd)
-        dsrc = kernel_source_hash(["kda_decode.cu", "kda_internal.cuh"])
+        dsrc = kernel_source_hash(kda.kernel_sources("decode_step_kernel"))
         dec = {"workload": f"{wd.name}: N={wd.N} H={wd.H} dk=dv={wd.dk} fp32 state "
                            f"({4 * wd.N * wd.H * wd.dk * wd.dv / 1e6:.0f} MB) in place, bf16 q/k/v, "
                            f"per-channel decay, {args.decode_steps} steps over {wd.pool} token sets",

@@ -2,7 +2,7 @@
 // choice, workspace layout and status reporting.  No kernel arithmetic here.
 #include <stdint.h>
 
-#include "kda_internal.cuh"
+#include "kda_launch.cuh"
 #include "kda_ptx.cuh"
 
 namespace kda {

@@ -25,7 +25,7 @@
 //
 // A partial last chunk is padded with k = q = v = 0, beta = 0 and a = 1:
 // such rows add nothing to A, W, U or u and leave the decay unchanged.
-#include "kda_internal.cuh"
+#include "kda_launch.cuh"
 
 namespace kda {
 namespace {

@@ -1,5 +1,5 @@
 // kda_chunk_tc.cu -- tensor-core (tcgen05) chunked prefill: not built yet.
-#include "kda_internal.cuh"
+#include "kda_launch.cuh"
 
 namespace kda {
 

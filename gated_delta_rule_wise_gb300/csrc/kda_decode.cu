@@ -15,7 +15,7 @@
 // registers with 128-bit streaming loads, forms the two column reductions
 // S'^T k and S'^T q, and writes S' + k u^T back with 128-bit streaming stores.
 // One read and one write of the state, nothing else touches HBM in bulk.
-#include "kda_internal.cuh"
+#include "kda_launch.cuh"
 
 namespace kda {
 namespace {

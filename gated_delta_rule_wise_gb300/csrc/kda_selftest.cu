@@ -4,7 +4,7 @@
 // and waits on it with a poll limit.  The wait gives up, the kernel records
 // KDA_ERR_TIMEOUT in the workspace's error word and returns normally: no
 // trap, no fault, the context stays usable.
-#include "kda_internal.cuh"
+#include "kda_launch.cuh"
 #include "kda_ptx.cuh"
 
 namespace kda {
