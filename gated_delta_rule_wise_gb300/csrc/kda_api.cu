@@ -86,7 +86,7 @@ const char *kda_chunk_fwd_kernel_name(int B, int H, int T, int dk, int dv, int C
                                       kda_alpha_mode am, kda_path path, int i) {
   if (check_chunk_shape(B, H, T, dk, dv, C, dt, am, path) != KDA_OK) return nullptr;
   if (i < 0 || i >= kda_chunk_fwd_launches(B, H, T, dk, dv, C, dt, am, path)) return nullptr;
-  return use_tensor(dk, dv, C, dt, path) ? chunk_tc_kernel_name(i) : chunk_ffma_kernel_name(i);
+  return use_tensor(dk, dv, C, dt, path) ? chunk_tc_kernel_name(T, i) : chunk_ffma_kernel_name(i);
 }
 
 kda_status kda_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *beta,

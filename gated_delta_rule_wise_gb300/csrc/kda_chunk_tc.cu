@@ -1,17 +1,720 @@
-// kda_chunk_tc.cu -- tensor-core (tcgen05) chunked prefill: not built yet.
+// kda_chunk_tc.cu -- tensor-core (tcgen05) chunked prefill of the gated delta
+// rule for bf16 inputs, C = 64, dk = dv = D in {64, 128}.
+//
+// Method.  Per chunk of C tokens, with g the running sum of log(a) =
+// -exp(log_alpha) from the chunk start (per key channel), gamma = exp(g) and
+// gamma_C its value at the chunk end, the chunked form of the recurrence is
+//   A  = strict_lower(diag(beta) (K*gamma) (K/gamma)^T),   T = (I + A)^-1
+//   W  = T diag(beta) (K*gamma),   U = T diag(beta) V
+//   u  = U - W S;   o = (Q*gamma) S + M u;   S' = Diag(gamma_C) S + Kbar^T u
+// with M = lower_incl((Q*gamma)(K/gamma)^T) and Kbar = K*gamma_C/gamma.  For no
+// decay it is the chunked DeltaNet loop of "22,580: From GPT-2 to Kimi K3"
+// (yichencityu.github.io), section 6.3 (forward substitution on the C x C unit
+// lower-triangular matrix; W = T K_beta; U = T V_beta; u = U - W S;
+// o = q S + tril(q k^T) u; S += k^T u); the decay factors are the cumulative
+// products the gated form needs ("22580: From GPT-2 to Kimi3, Explained"
+// (zharfai.com), "Gated DeltaNet adds controlled forgetting"), per key channel
+// as in "22580: From GPT-2 to Kimi K3, Explained" (lukebest.github.io),
+// "KDA (per-channel alpha)".
+//
+// Substituting u, the pass over chunks needs one product with the state:
+//   S' = (Diag(gamma_C) + Ap) S + Kbar^T U,      Ap = -Kbar^T W   (D x D)
+//   o  = Qp S + M U,                              Qp = Q*gamma - M W  (C x D)
+// Everything except S is known per chunk before the pass starts, so
+//  - kda_prep_kernel (one CTA per chunk, fully parallel) computes the decay
+//    prefix, the decayed tiles, A and M (one tcgen05 MMA), T by forward
+//    substitution in shared memory, W and U (tcgen05), Ap and M W (tcgen05),
+//    and writes Ap, Qp, Kbar^T, M, U^T and gamma_C for the chunk to the
+//    workspace, already in the swizzled operand layout;
+//  - kda_scan_kernel (one CTA per (head, block of NB value columns)) keeps S
+//    in tensor memory as float32 and, per chunk, scales it by gamma_C in
+//    place, writes a bf16 copy as the MMA operand, and runs
+//    S += Ap S + Kbar^T U and o = Qp S + M U as tcgen05 MMAs on operands
+//    double-buffered by bulk copies.  One MMA round trip per chunk sits on
+//    the serial path.
+// A partial last chunk is padded with k = q = v = 0, beta = 0, a = 1, which
+// adds nothing; padded rows of o are not stored.
 #include "kda_launch.cuh"
+#include "kda_ptx.cuh"
+#include "kda_umma.cuh"
 
 namespace kda {
+namespace {
 
-bool chunk_tc_supported(int, int, int, kda_dtype) { return false; }
-size_t chunk_tc_workspace_bytes(int, int, int, int, int, int) { return 0; }
-kda_status launch_chunk_tc(const void *, const void *, const void *, const float *,
-                           const float *, const float *, void *, float *, int, int, int, int,
-                           int, int, kda_alpha_mode, void *, size_t, cudaStream_t,
-                           LaunchTimer &) {
-  return KDA_ERR_UNSUPPORTED;
+constexpr int kC = 64;                 // chunk length on this path
+constexpr uint32_t kWaitLimit = 1u << 24;  // polls before a wait gives up (~1 s)
+
+// Per-chunk intermediate record in the workspace (and its shared-memory image).
+template <int D>
+struct Blob {
+  static constexpr uint32_t AP = 0;                     // Ap    [D rows][D]    K-major SW128
+  static constexpr uint32_t QP = AP + D * D * 2;        // Qp    [C rows][D]
+  static constexpr uint32_t KBT = QP + kC * D * 2;      // Kbar^T[D rows][C]
+  static constexpr uint32_t MM = KBT + D * kC * 2;      // M     [C rows][C]
+  static constexpr uint32_t UT = MM + kC * kC * 2;      // U^T   [D rows][C]
+  static constexpr uint32_t GC = UT + D * kC * 2;       // gamma_C [D] float
+  static constexpr uint32_t BYTES = GC + D * 4;
+  static constexpr uint32_t PRE = UT;                   // Ap | Qp | Kbar^T | M
+};
+
+__host__ __device__ constexpr uint32_t align1k(uint32_t x) { return (x + 1023u) & ~1023u; }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&p);
 }
-int chunk_tc_launches(int, int, bool) { return 0; }
-const char *chunk_tc_kernel_name(int) { return nullptr; }
+__device__ __forceinline__ void st_bf16(uint8_t *base, uint32_t off, float x) {
+  *reinterpret_cast<__nv_bfloat16 *>(base + off) = __float2bfloat16_rn(x);
+}
+__device__ __forceinline__ float ld_bf16(const uint8_t *base, uint32_t off) {
+  return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(base + off));
+}
+// 8 consecutive K values of one row -> one 16-byte chunk.
+__device__ __forceinline__ void st_chunk(uint8_t *tile, int row, int c8, int rows, const float *v) {
+  uint4 u;
+  u.x = pack_bf16x2(v[0], v[1]);
+  u.y = pack_bf16x2(v[2], v[3]);
+  u.z = pack_bf16x2(v[4], v[5]);
+  u.w = pack_bf16x2(v[6], v[7]);
+  *reinterpret_cast<uint4 *>(tile + umma::sw128_chunk(row, c8, rows)) = u;
+}
+__device__ __forceinline__ void ld_chunk(const uint8_t *tile, int row, int c8, int rows, float *v) {
+  const uint4 u = *reinterpret_cast<const uint4 *>(tile + umma::sw128_chunk(row, c8, rows));
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 p = *reinterpret_cast<const __nv_bfloat162 *>(&w[i]);
+    v[2 * i] = __low2float(p);
+    v[2 * i + 1] = __high2float(p);
+  }
+}
+
+// ============================================================== prep kernel
+
+template <int D>
+struct PrepSmem {
+  using B = Blob<D>;
+  static constexpr uint32_t BLOB = 0;
+  static constexpr uint32_t X1 = align1k(B::BYTES);        // [K_beta; Q*gamma] [128 rows][D]
+  static constexpr uint32_t TT = X1 + 128 * D * 2;         // T                 [C rows][C]
+  static constexpr uint32_t WT = TT + kC * kC * 2;         // W^T               [D rows][C]
+  static constexpr uint32_t AS = WT + D * kC * 2;          // A, float          [C][C] swizzled
+  // D = 128 reuses the Ap and Qp slots of the record for X2 and Khat (both dead
+  // before Ap and Qp are written); D = 64 gives them their own space.
+  static constexpr uint32_t X2 = (D == 128) ? B::AP : AS + kC * kC * 4;   // [K_beta^T; (beta V)^T] [2D rows][C]
+  static constexpr uint32_t KH = (D == 128) ? B::QP : X2 + 2 * D * kC * 2; // K/gamma  [C rows][D]
+  static constexpr uint32_t SMALL = (D == 128) ? AS + kC * kC * 4 : KH + kC * D * 2;
+  static constexpr uint32_t PART = SMALL;                  // float [4][D] partial decay sums
+  static constexpr uint32_t BAR = PART + 4 * D * 4;        // mbarrier
+  static constexpr uint32_t TMEMP = BAR + 8;               // TMEM base address
+  static constexpr uint32_t BYTES = TMEMP + 8;
+  static constexpr uint32_t TMEM_COLS = (D == 128) ? 256 : 128;
+};
+
+template <int D>
+__global__ void __launch_bounds__(256, 1)
+kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+                const __nv_bfloat16 *__restrict__ v, const float *__restrict__ beta,
+                const float *__restrict__ log_alpha, int alpha_mode, int T, int NC,
+                uint8_t *__restrict__ ws) {
+  using B = Blob<D>;
+  using L = PrepSmem<D>;
+  constexpr int Q4 = 256 / D;          // threads per key channel
+  constexpr int R = kC / Q4;           // rows per thread in the elementwise phase
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                            ~static_cast<uintptr_t>(1023));
+  uint8_t *blob = sm + L::BLOB;
+  uint8_t *X1 = sm + L::X1;
+  uint8_t *TT = sm + L::TT;
+  uint8_t *WT = sm + L::WT;
+  float *AS = reinterpret_cast<float *>(sm + L::AS);
+  uint8_t *X2 = sm + L::X2;
+  uint8_t *KH = sm + L::KH;
+  float *part = reinterpret_cast<float *>(sm + L::PART);
+  uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::BAR);
+  uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(sm + L::TMEMP);
+  WorkspaceHeader *hdr = reinterpret_cast<WorkspaceHeader *>(ws);
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int n = blockIdx.x, bh = blockIdx.y;
+  const int t0 = n * kC;
+  const int valid = min(kC, T - t0);
+  bool ok = true;
+
+  if (tid == 0) {
+    ptx::mbar_init(bar, 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc(tmem_ptr, L::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+
+  // ---- (1) decay prefix and decayed tiles: thread owns key channel c over R rows
+  const int c = tid % D, qtr = tid / D, r0 = qtr * R;
+  float ld[R], bt[R];
+  {
+    const size_t row0 = (size_t)bh * T + t0;
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      const int r = r0 + i;
+      float x = 0.f, b = 0.f;
+      if (r < valid) {
+        b = beta[row0 + r];
+        if (alpha_mode == KDA_ALPHA_CHANNEL)
+          x = -__expf(log_alpha[(row0 + r) * D + c]);
+        else if (alpha_mode == KDA_ALPHA_SCALAR)
+          x = -__expf(log_alpha[row0 + r]);
+      }
+      ld[i] = x;
+      bt[i] = b;
+    }
+  }
+  float psum = 0.f;
+#pragma unroll
+  for (int i = 0; i < R; ++i) psum += ld[i];
+  part[qtr * D + c] = psum;
+  __syncthreads();
+  float g = 0.f, gC = 0.f;
+#pragma unroll
+  for (int j = 0; j < Q4; ++j) {
+    const float p = part[j * D + c];
+    gC += p;
+    if (j < qtr) g += p;
+  }
+  const float egC = __expf(gC);
+  {
+    const size_t e0 = ((size_t)bh * T + t0) * D + c;
+    float kbT[8], kbarT[8], vbT[8];
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      const int r = r0 + i;
+      float kv = 0.f, qv = 0.f, vv = 0.f;
+      if (r < valid) {
+        kv = __bfloat162float(k[e0 + (size_t)r * D]);
+        qv = __bfloat162float(q[e0 + (size_t)r * D]);
+        vv = __bfloat162float(v[e0 + (size_t)r * D]);
+      }
+      g += ld[i];
+      const float eg = __expf(g), eng = __expf(-g);
+      const float kb = bt[i] * kv * eg;
+      st_bf16(X1, umma::sw128_off(r, c, 128), kb);               // K_beta
+      st_bf16(X1, umma::sw128_off(kC + r, c, 128), qv * eg);     // Q * gamma
+      st_bf16(KH, umma::sw128_off(r, c, kC), kv * eng);          // K / gamma
+      kbT[i & 7] = kb;
+      kbarT[i & 7] = kv * eng * egC;
+      vbT[i & 7] = bt[i] * vv;
+      if ((i & 7) == 7) {
+        const int c8 = (r0 + i) >> 3;
+        st_chunk(X2, c, c8, 2 * D, kbT);                          // K_beta^T
+        st_chunk(X2, D + c, c8, 2 * D, vbT);                      // (beta V)^T
+        st_chunk(blob + B::KBT, c, c8, D, kbarT);                 // Kbar^T (output)
+      }
+    }
+    if (qtr == 0) reinterpret_cast<float *>(blob + B::GC)[c] = egC;
+  }
+  ptx::fence_proxy_async_smem();
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_ptr;
+  const uint32_t sX1 = ptx::smem_u32(X1), sKH = ptx::smem_u32(KH), sX2 = ptx::smem_u32(X2);
+  const uint32_t sTT = ptx::smem_u32(TT), sWT = ptx::smem_u32(WT);
+  const uint32_t sKBT = ptx::smem_u32(blob + B::KBT), sMM = ptx::smem_u32(blob + B::MM);
+
+  // ---- (2) [A_full; M_full] = [K_beta; Q*gamma] (K/gamma)^T  -> TMEM cols [0, 64)
+  if (tid == 0) {
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks)
+      ptx::mma_bf16_ss(tmem, umma::sdesc_k(sX1, 128, ks), umma::sdesc_k(sKH, kC, ks),
+                       umma::idesc_bf16(128, kC), ks > 0);
+    ptx::mma_commit(bar);
+  }
+  if (!ptx::mbar_wait(bar, 0, kWaitLimit)) {
+    ok = false;
+    report_error(hdr, KDA_ERR_TIMEOUT, 0x101u);
+  }
+  ptx::tc_fence_after();
+
+  // ---- (3) rows 0..63: A (strict lower) to shared memory; rows 64..127: M
+  if (warp < 4) {
+    const int lane_row = tid;  // TMEM lane
+    const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16);
+#pragma unroll
+    for (int cb = 0; cb < kC; cb += 16) {
+      float x[16];
+      ptx::tmem_ld16(ta + cb, x);
+      ptx::tmem_ld_wait();
+      if (lane_row < kC) {
+        const int r = lane_row;
+#pragma unroll
+        for (int j4 = 0; j4 < 4; ++j4) {
+          const int m0 = cb + 4 * j4;
+          float4 a;
+          a.x = (m0 + 0 < r) ? x[4 * j4 + 0] : 0.f;
+          a.y = (m0 + 1 < r) ? x[4 * j4 + 1] : 0.f;
+          a.z = (m0 + 2 < r) ? x[4 * j4 + 2] : 0.f;
+          a.w = (m0 + 3 < r) ? x[4 * j4 + 3] : 0.f;
+          reinterpret_cast<float4 *>(AS)[r * 16 + ((m0 >> 2) ^ (r & 15))] = a;
+        }
+      } else {
+        const int r = lane_row - kC;
+        float mrow[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) mrow[j] = (cb + j <= r) ? x[j] : 0.f;
+        st_chunk(blob + B::MM, r, cb >> 3, kC, mrow);
+        st_chunk(blob + B::MM, r, (cb >> 3) + 1, kC, mrow + 8);
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- (4) T = (I + A)^-1 by forward substitution, one column per thread
+  if (tid < kC) {
+    const int j = tid;
+    float t[kC];
+#pragma unroll
+    for (int i = 0; i < kC; ++i) {
+      float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+      for (int b = 0; b < (i + 3) / 4; ++b) {
+        const float4 a = reinterpret_cast<const float4 *>(AS)[i * 16 + (b ^ (i & 15))];
+        if (4 * b + 0 < i) acc0 += a.x * t[4 * b + 0];
+        if (4 * b + 1 < i) acc1 += a.y * t[4 * b + 1];
+        if (4 * b + 2 < i) acc0 += a.z * t[4 * b + 2];
+        if (4 * b + 3 < i) acc1 += a.w * t[4 * b + 3];
+      }
+      t[i] = (i == j) ? 1.f : -(acc0 + acc1);
+    }
+#pragma unroll
+    for (int i = 0; i < kC; ++i) st_bf16(TT, umma::sw128_off(i, j, kC), t[i]);
+  }
+  ptx::fence_proxy_async_smem();
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+
+  // ---- (5) [W^T; U^T] = [K_beta^T; (beta V)^T] T^T  -> TMEM cols [64, 192) or [64, 128)
+  if (tid == 0) {
+#pragma unroll
+    for (int h = 0; h < 2 * D / 128; ++h)
+#pragma unroll
+      for (int ks = 0; ks < kC / 16; ++ks)
+        ptx::mma_bf16_ss(tmem + 64 + 64 * h, umma::sdesc_k(sX2 + h * 128 * 128, 2 * D, ks),
+                         umma::sdesc_k(sTT, kC, ks), umma::idesc_bf16(128, kC), ks > 0);
+    ptx::mma_commit(bar);
+  }
+  if (ok && !ptx::mbar_wait(bar, 1, kWaitLimit)) {
+    ok = false;
+    report_error(hdr, KDA_ERR_TIMEOUT, 0x102u);
+  }
+  ptx::tc_fence_after();
+
+  // ---- (6) W^T -> operand tile, U^T -> record
+  if (warp < 4) {
+    const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16);
+#pragma unroll
+    for (int h = 0; h < 2 * D / 128; ++h) {
+#pragma unroll
+      for (int cb = 0; cb < kC; cb += 16) {
+        float x[16];
+        ptx::tmem_ld16(ta + 64 + 64 * h + cb, x);
+        ptx::tmem_ld_wait();
+        // D = 128: h = 0 holds W^T rows (= lane), h = 1 U^T rows.
+        // D = 64:  lanes 0..63 W^T rows, lanes 64..127 U^T rows.
+        const int lane_row = tid;
+        const bool isW = (D == 128) ? (h == 0) : (lane_row < D);
+        const int row = (D == 128) ? lane_row : (lane_row % D);
+        uint8_t *dst = isW ? WT : blob + B::UT;
+        st_chunk(dst, row, cb >> 3, D, x);
+        st_chunk(dst, row, (cb >> 3) + 1, D, x + 8);
+      }
+    }
+  }
+  ptx::fence_proxy_async_smem();
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+
+  // ---- (7) Kbar^T W  (and M W)  -> TMEM
+  if (tid == 0) {
+    if (D == 128) {
+      // cols [0, 128): Kbar^T W  (M = 128, N = 128)
+#pragma unroll
+      for (int ks = 0; ks < kC / 16; ++ks)
+        ptx::mma_bf16_ss(tmem, umma::sdesc_k(sKBT, D, ks), umma::sdesc_k(sWT, D, ks),
+                         umma::idesc_bf16(128, D), ks > 0);
+      // cols [128, 192): (M W)^T = W^T M^T  (M = 128, N = 64)
+#pragma unroll
+      for (int ks = 0; ks < kC / 16; ++ks)
+        ptx::mma_bf16_ss(tmem + 128, umma::sdesc_k(sWT, D, ks), umma::sdesc_k(sMM, kC, ks),
+                         umma::idesc_bf16(128, kC), ks > 0);
+    } else {
+      // cols [0, 64): [Kbar^T; M] W  (Kbar^T and M are adjacent in the record)
+#pragma unroll
+      for (int ks = 0; ks < kC / 16; ++ks)
+        ptx::mma_bf16_ss(tmem, umma::sdesc_k(sKBT, 128, ks), umma::sdesc_k(sWT, D, ks),
+                         umma::idesc_bf16(128, D), ks > 0);
+    }
+    ptx::mma_commit(bar);
+  }
+  if (ok && !ptx::mbar_wait(bar, 0, kWaitLimit)) {
+    ok = false;
+    report_error(hdr, KDA_ERR_TIMEOUT, 0x103u);
+  }
+  ptx::tc_fence_after();
+
+  // ---- (8) Ap = -Kbar^T W;  Qp = Q*gamma - M W
+  if (warp < 4) {
+    const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16);
+    const int lane_row = tid;
+    if (D == 128) {
+#pragma unroll
+      for (int cb = 0; cb < D; cb += 16) {
+        float x[16];
+        ptx::tmem_ld16(ta + cb, x);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) x[j] = -x[j];
+        st_chunk(blob + B::AP, lane_row, cb >> 3, D, x);
+        st_chunk(blob + B::AP, lane_row, (cb >> 3) + 1, D, x + 8);
+      }
+      // (M W)^T: lane = key channel cc, column = token r
+      const int cc = lane_row;
+#pragma unroll
+      for (int cb = 0; cb < kC; cb += 16) {
+        float x[16];
+        ptx::tmem_ld16(ta + 128 + cb, x);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int r = cb + j;
+          const float qg = ld_bf16(X1, umma::sw128_off(kC + r, cc, 128));
+          st_bf16(blob + B::QP, umma::sw128_off(r, cc, kC), qg - x[j]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int cb = 0; cb < D; cb += 16) {
+        float x[16];
+        ptx::tmem_ld16(ta + cb, x);
+        ptx::tmem_ld_wait();
+        if (lane_row < D) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) x[j] = -x[j];
+          st_chunk(blob + B::AP, lane_row, cb >> 3, D, x);
+          st_chunk(blob + B::AP, lane_row, (cb >> 3) + 1, D, x + 8);
+        } else {
+          const int r = lane_row - D;
+          float qg[16];
+          ld_chunk(X1, kC + r, cb >> 3, 128, qg);
+          ld_chunk(X1, kC + r, (cb >> 3) + 1, 128, qg + 8);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) qg[j] -= x[j];
+          st_chunk(blob + B::QP, r, cb >> 3, kC, qg);
+          st_chunk(blob + B::QP, r, (cb >> 3) + 1, kC, qg + 8);
+        }
+      }
+    }
+  }
+  ptx::fence_proxy_async_smem();
+  ptx::tc_fence_before();
+  __syncthreads();
+
+  // ---- (9) record -> workspace (one bulk copy), release TMEM
+  if (tid == 0) {
+    uint8_t *dst = ws + sizeof(WorkspaceHeader) + ((size_t)bh * NC + n) * B::BYTES;
+    ptx::bulk_s2g(dst, blob, B::BYTES);
+    ptx::bulk_commit();
+    ptx::bulk_wait_all();
+  }
+  if (warp == 0) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, L::TMEM_COLS);
+  }
+}
+
+// ============================================================== scan kernel
+
+template <int D, int NB>
+struct ScanSmem {
+  using B = Blob<D>;
+  static constexpr uint32_t STAGE_BYTES = B::PRE + NB * 128 + D * 4;  // Ap|Qp|Kbar^T|M, U^T block, gamma_C
+  static constexpr uint32_t STAGE = align1k(STAGE_BYTES);
+  static constexpr uint32_t SB = 2 * STAGE;                 // bf16 state operand [NB rows][D]
+  static constexpr uint32_t BAR = SB + NB * D * 2;          // full[2], mma
+  static constexpr uint32_t TMEMP = BAR + 3 * 8;
+  static constexpr uint32_t BYTES = TMEMP + 8;
+  static constexpr uint32_t TMEM_COLS = (D == 128) ? ((2 * NB <= 32) ? 32 : (2 * NB <= 64 ? 64 : 128)) : (NB <= 32 ? 32 : 64);
+};
+
+template <int D, int NB>
+__global__ void __launch_bounds__(128, 1)
+kda_scan_kernel(const float *__restrict__ h0, __nv_bfloat16 *__restrict__ o,
+                float *__restrict__ hT, int T, int NC, uint8_t *__restrict__ ws) {
+  using B = Blob<D>;
+  using L = ScanSmem<D, NB>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                            ~static_cast<uintptr_t>(1023));
+  uint8_t *SB = sm + L::SB;
+  uint64_t *full = reinterpret_cast<uint64_t *>(sm + L::BAR);
+  uint64_t *mbar = full + 2;
+  uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(sm + L::TMEMP);
+  WorkspaceHeader *hdr = reinterpret_cast<WorkspaceHeader *>(ws);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.y, j0 = blockIdx.x * NB;
+  const int dv = D;
+  const uint8_t *rec0 = ws + sizeof(WorkspaceHeader) + (size_t)bh * NC * B::BYTES;
+  bool ok = true;
+
+  if (tid == 0) {
+    ptx::mbar_init(&full[0], 1);
+    ptx::mbar_init(&full[1], 1);
+    ptx::mbar_init(mbar, 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc(tmem_ptr, L::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_ptr;
+  const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+  const uint32_t tS = t_lane;                       // state columns [0, NB)
+  const uint32_t tO = t_lane + (D == 128 ? NB : 0); // output columns (D = 64: same as state)
+  const bool state_row = (D == 128) || (tid < D);   // this thread's lane holds a state row
+  const int srow = tid;                              // key channel of that row
+
+  auto issue_loads = [&](int chunk, int s) {
+    uint8_t *st = sm + s * L::STAGE;
+    const uint8_t *rec = rec0 + (size_t)chunk * B::BYTES;
+    ptx::fence_proxy_async_smem();
+    ptx::mbar_arrive_expect_tx(&full[s], L::STAGE_BYTES);
+    ptx::bulk_g2s(st, rec, B::PRE, &full[s]);
+    ptx::bulk_g2s(st + B::PRE, rec + B::UT + (size_t)j0 * 128, NB * 128, &full[s]);
+    ptx::bulk_g2s(st + B::PRE + NB * 128, rec + B::GC, D * 4, &full[s]);
+  };
+
+  // initial state -> TMEM (rows that are not state rows get zeros)
+  {
+    const size_t s0 = (size_t)bh * D * dv;
+#pragma unroll
+    for (int cb = 0; cb < NB; cb += 16) {
+      float x[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        x[j] = (state_row && h0) ? h0[s0 + (size_t)srow * dv + j0 + cb + j] : 0.f;
+      ptx::tmem_st16(tS + cb, x);
+    }
+    ptx::tmem_st_wait();
+  }
+  if (tid == 0 && NC > 0) issue_loads(0, 0);
+  ptx::tc_fence_before();
+  __syncthreads();
+
+  auto store_o_rows = [&](int chunk) {
+    // D = 128: output rows sit in lanes 32w + (0..15) (M = 64 layout); D = 64: lanes 64..127.
+    const bool has = (D == 128) ? (lane < 16) : (tid >= D);
+    const int r = (D == 128) ? (warp * 16 + lane) : (tid - D);
+    const int t = chunk * kC + r;
+#pragma unroll
+    for (int cb = 0; cb < NB; cb += 16) {
+      float x[16];
+      ptx::tmem_ld16(tO + cb, x);
+      ptx::tmem_ld_wait();
+      if (has && t < T) {
+        uint4 *dst = reinterpret_cast<uint4 *>(o + ((size_t)bh * T + t) * dv + j0 + cb);
+        uint4 a, b;
+        a.x = pack_bf16x2(x[0], x[1]); a.y = pack_bf16x2(x[2], x[3]);
+        a.z = pack_bf16x2(x[4], x[5]); a.w = pack_bf16x2(x[6], x[7]);
+        b.x = pack_bf16x2(x[8], x[9]); b.y = pack_bf16x2(x[10], x[11]);
+        b.z = pack_bf16x2(x[12], x[13]); b.w = pack_bf16x2(x[14], x[15]);
+        dst[0] = a;
+        dst[1] = b;
+      }
+    }
+  };
+
+  for (int i = 0; i < NC; ++i) {
+    const int s = i & 1;
+    uint8_t *st = sm + s * L::STAGE;
+    if (i > 0 && ok && !ptx::mbar_wait(mbar, (i - 1) & 1, kWaitLimit)) {
+      ok = false;
+      report_error(hdr, KDA_ERR_TIMEOUT, 0x201u);
+    }
+    ptx::tc_fence_after();
+    if (tid == 0 && i + 1 < NC) issue_loads(i + 1, (i + 1) & 1);
+    if (ok && !ptx::mbar_wait(&full[s], (i >> 1) & 1, kWaitLimit)) {
+      ok = false;
+      report_error(hdr, KDA_ERR_TIMEOUT, 0x202u);
+    }
+    // state row: bf16 copy as the MMA operand, then scale by gamma_C in place
+    if (state_row) {
+      const float gam = reinterpret_cast<const float *>(st + B::PRE + NB * 128)[srow];
+#pragma unroll
+      for (int cb = 0; cb < NB; cb += 16) {
+        float x[16];
+        ptx::tmem_ld16(tS + cb, x);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          st_bf16(SB, umma::sw128_off(cb + j, srow, NB), x[j]);
+          x[j] *= gam;
+        }
+        ptx::tmem_st16(tS + cb, x);
+      }
+    }
+    if (i > 0) store_o_rows(i - 1);
+    if (D == 64 && !state_row) {  // output lanes restart from zero each chunk
+      float z[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) z[j] = 0.f;
+#pragma unroll
+      for (int cb = 0; cb < NB; cb += 16) ptx::tmem_st16(tO + cb, z);
+    }
+    ptx::tmem_st_wait();
+    ptx::fence_proxy_async_smem();
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      ptx::tc_fence_after();
+      const uint32_t sAP = ptx::smem_u32(st + B::AP), sQP = ptx::smem_u32(st + B::QP);
+      const uint32_t sKB = ptx::smem_u32(st + B::KBT), sMM = ptx::smem_u32(st + B::MM);
+      const uint32_t sUT = ptx::smem_u32(st + B::PRE), sSB = ptx::smem_u32(SB);
+      if (D == 128) {
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          ptx::mma_bf16_ss(tmem, umma::sdesc_k(sAP, D, ks), umma::sdesc_k(sSB, NB, ks),
+                           umma::idesc_bf16(128, NB), 1);
+#pragma unroll
+        for (int ks = 0; ks < kC / 16; ++ks)
+          ptx::mma_bf16_ss(tmem, umma::sdesc_k(sKB, D, ks), umma::sdesc_k(sUT, NB, ks),
+                           umma::idesc_bf16(128, NB), 1);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          ptx::mma_bf16_ss(tmem + NB, umma::sdesc_k(sQP, kC, ks), umma::sdesc_k(sSB, NB, ks),
+                           umma::idesc_bf16(64, NB), ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < kC / 16; ++ks)
+          ptx::mma_bf16_ss(tmem + NB, umma::sdesc_k(sMM, kC, ks), umma::sdesc_k(sUT, NB, ks),
+                           umma::idesc_bf16(64, NB), 1);
+      } else {
+        // [Ap; Qp] and [Kbar^T; M] are adjacent 64-row tiles: one M = 128 operand each
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          ptx::mma_bf16_ss(tmem, umma::sdesc_k(sAP, 128, ks), umma::sdesc_k(sSB, NB, ks),
+                           umma::idesc_bf16(128, NB), 1);
+#pragma unroll
+        for (int ks = 0; ks < kC / 16; ++ks)
+          ptx::mma_bf16_ss(tmem, umma::sdesc_k(sKB, 128, ks), umma::sdesc_k(sUT, NB, ks),
+                           umma::idesc_bf16(128, NB), 1);
+      }
+      ptx::mma_commit(mbar);
+    }
+  }
+
+  // epilogue: last chunk's output, final state
+  if (NC > 0) {
+    if (ok && !ptx::mbar_wait(mbar, (NC - 1) & 1, kWaitLimit)) {
+      ok = false;
+      report_error(hdr, KDA_ERR_TIMEOUT, 0x203u);
+    }
+    ptx::tc_fence_after();
+    store_o_rows(NC - 1);
+  }
+  if (hT) {
+    const size_t s0 = (size_t)bh * D * dv;
+#pragma unroll
+    for (int cb = 0; cb < NB; cb += 16) {
+      float x[16];
+      ptx::tmem_ld16(tS + cb, x);
+      ptx::tmem_ld_wait();
+      if (state_row) {
+        float4 *dst = reinterpret_cast<float4 *>(hT + s0 + (size_t)srow * dv + j0 + cb);
+#pragma unroll
+        for (int j4 = 0; j4 < 4; ++j4)
+          dst[j4] = make_float4(x[4 * j4], x[4 * j4 + 1], x[4 * j4 + 2], x[4 * j4 + 3]);
+      }
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, L::TMEM_COLS);
+  }
+}
+
+// ============================================================== launch
+
+template <int D>
+constexpr int scan_nb() { return 32; }
+
+template <int D>
+kda_status launch_d(const void *q, const void *k, const void *v, const float *beta,
+                    const float *log_alpha, const float *h0, void *o, float *hT, int BH, int T,
+                    kda_alpha_mode am, uint8_t *ws, cudaStream_t st, LaunchTimer &timer) {
+  constexpr int NB = scan_nb<D>();
+  const int NC = (T + kC - 1) / kC;
+  const uint32_t prep_smem = PrepSmem<D>::BYTES + 1024;
+  const uint32_t scan_smem = ScanSmem<D, NB>::BYTES + 1024;
+  if (cudaFuncSetAttribute(kda_prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)prep_smem) != cudaSuccess ||
+      cudaFuncSetAttribute(kda_scan_kernel<D, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)scan_smem) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  if (NC > 0) {
+    timer.mark();
+    kda_prep_kernel<D><<<dim3(NC, BH), 256, prep_smem, st>>>(
+        static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
+        static_cast<const __nv_bfloat16 *>(v), beta, log_alpha, (int)am, T, NC, ws);
+  }
+  timer.mark();
+  kda_scan_kernel<D, NB><<<dim3(D / NB, BH), 128, scan_smem, st>>>(
+      h0, static_cast<__nv_bfloat16 *>(o), hT, T, NC, ws);
+  timer.mark();
+  return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+}  // namespace
+
+bool chunk_tc_supported(int dk, int dv, int C, kda_dtype dt) {
+  return dt == KDA_BF16 && C == kC && dk == dv && (dk == 64 || dk == 128);
+}
+
+size_t chunk_tc_workspace_bytes(int B, int H, int T, int dk, int dv, int C) {
+  if (dk != dv || C != kC) return 0;
+  const size_t NC = (size_t)(T + kC - 1) / kC;
+  const size_t rec = dk == 128 ? Blob<128>::BYTES : Blob<64>::BYTES;
+  return (size_t)B * H * NC * rec;
+}
+
+int chunk_tc_launches(int BH, int T, bool has_hT) {
+  if (BH == 0 || (T == 0 && !has_hT)) return 0;
+  return T > 0 ? 2 : 1;
+}
+
+const char *chunk_tc_kernel_name(int T, int i) {
+  if (T == 0) return i == 0 ? "kda_scan_kernel" : nullptr;
+  return i == 0 ? "kda_prep_kernel" : (i == 1 ? "kda_scan_kernel" : nullptr);
+}
+
+kda_status launch_chunk_tc(const void *q, const void *k, const void *v, const float *beta,
+                           const float *log_alpha, const float *h0, void *o, float *hT, int B,
+                           int H, int T, int dk, int /*dv*/, int /*C*/, kda_alpha_mode am,
+                           void *workspace, size_t /*ws_bytes*/, cudaStream_t stream,
+                           LaunchTimer &timer) {
+  const int BH = B * H;
+  if (chunk_tc_launches(BH, T, hT != nullptr) == 0) return KDA_OK;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  if (dk == 128)
+    return launch_d<128>(q, k, v, beta, log_alpha, h0, o, hT, BH, T, am, ws, stream, timer);
+  return launch_d<64>(q, k, v, beta, log_alpha, h0, o, hT, BH, T, am, ws, stream, timer);
+}
 
 }  // namespace kda

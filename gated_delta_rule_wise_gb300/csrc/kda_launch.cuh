@@ -36,7 +36,7 @@ kda_status launch_chunk_ffma(const void *q, const void *k, const void *v, const 
 int chunk_ffma_launches(int BH, int T, bool has_hT);
 const char *chunk_ffma_kernel_name(int i);
 int chunk_tc_launches(int BH, int T, bool has_hT);
-const char *chunk_tc_kernel_name(int i);
+const char *chunk_tc_kernel_name(int T, int i);
 bool chunk_tc_supported(int dk, int dv, int C, kda_dtype dt);
 size_t chunk_tc_workspace_bytes(int B, int H, int T, int dk, int dv, int C);
 kda_status launch_chunk_tc(const void *q, const void *k, const void *v, const float *beta,

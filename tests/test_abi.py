@@ -141,6 +141,17 @@ def test_launch_queries(lib):
             assert os.path.exists(os.path.join(ROOT, "gated_delta_rule_wise_gb300", "csrc", f))
 
 
+def test_tensor_path_is_what_auto_picks_for_bf16_c64(lib):
+    import gated_delta_rule_wise_gb300 as kda
+    names = kda.kda_chunk_fwd_kernel_names(1, 32, 131072, 128, 128, 64, kda.KDA_BF16,
+                                           kda.KDA_ALPHA_CHANNEL)
+    assert names == ["kda_prep_kernel", "kda_scan_kernel"]
+    assert kda.kda_chunk_fwd_kernel_names(1, 1, 0, 128, 128, 64, kda.KDA_BF16, 2) == ["kda_scan_kernel"]
+    assert kda.kda_chunk_fwd_kernel_names(1, 1, 64, 16, 16, 16, kda.KDA_F32, 2) == ["chunk_ffma_kernel"]
+    big = kda.kda_chunk_fwd_workspace_size(1, 32, 131072, 128, 128, 64, kda.KDA_BF16, 2)
+    assert big == 256 + 32 * 2048 * 90624     # one 90624-byte record per (head, chunk)
+
+
 def test_status_and_selftest_validation(lib):
     assert lib.kda_chunk_fwd_status(None, None) == 1
     assert lib.kda_selftest_wait_timeout(FAKE, 256, 0, None) == 1
