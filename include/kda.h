@@ -159,6 +159,39 @@ const char *kda_chunk_fwd_kernel_name(int B, int H, int T, int dk, int dv, int C
                                       kda_path path, int i);
 
 /*
+ * kda_chunk_fwd without a caller-provided workspace, for callers that cannot
+ * allocate device memory: code behind a plugin or host interface that is
+ * handed only its input and output buffers, or a serving loop that must not
+ * call cudaMalloc on its hot path because the call can synchronise the
+ * device.  The pages describe no such entry point; it has no counterpart
+ * there.
+ *
+ * Same arguments, meaning and results as kda_chunk_fwd, minus the workspace.
+ * The scratch lives in one fixed 64 MiB array inside the library (a
+ * file-scope __device__ array that every GPU which loads libkda holds until
+ * the process exits).  Problems whose kda_chunk_fwd_workspace_size exceeds
+ * 64 MiB (67108864 bytes) are rejected with KDA_ERR_UNSUPPORTED before
+ * anything is launched; for the d = 128 tensor path that is about 740
+ * (head, 64-token chunk) pairs, e.g. B*H = 8 heads of up to 5,888 tokens.
+ * Nothing is allocated: no cudaMalloc, no cudaFree, no allocating library call.
+ *
+ * The first call on a device looks up the array's device address on the
+ * device that is current at the time (once per device; the device of
+ * `stream` must be the current device); make that first call before any
+ * stream capture.  Every call clears the array's error word and overwrites
+ * the records it uses, but all calls share the one array: calls whose
+ * kernels overlap on the GPU (other streams, other host threads) race on it
+ * and give undefined results; serialise them.  Device-side wait timeouts are
+ * recorded in the shared error word only and are not reported by this call.
+ */
+kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
+                                 const float *beta, const float *log_alpha,
+                                 const float *h0, void *o, float *hT,
+                                 int B, int H, int T, int dk, int dv, int C,
+                                 kda_dtype dt, kda_alpha_mode am,
+                                 kda_stream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device error word of
  * `workspace`.  KDA_OK if every call enqueued with this workspace finished
  * normally; KDA_ERR_TIMEOUT if an on-device wait gave up (the outputs of that
