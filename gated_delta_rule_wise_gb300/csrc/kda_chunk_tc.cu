@@ -105,8 +105,18 @@ struct PrepSmem {
   static constexpr uint32_t KH = (D == 128) ? B::QP : X2 + 2 * D * kC * 2; // K/gamma  [C rows][D]
   static constexpr uint32_t SMALL = (D == 128) ? AS + kC * kC * 4 : KH + kC * D * 2;
   static constexpr uint32_t PART = SMALL;                  // float [4][D] partial decay sums
-  static constexpr uint32_t BAR = PART + 4 * D * 4;        // mbarrier
-  static constexpr uint32_t TMEMP = BAR + 8;               // TMEM base address
+  static constexpr uint32_t BAR = PART + 4 * D * 4;        // mbarrier (MMA commits)
+  static constexpr uint32_t LBAR = BAR + 8;                // mbarrier (raw loads)
+  static constexpr uint32_t TMEMP = LBAR + 8;              // TMEM base address
+  // Raw q, k, v rows of the chunk ([C][D] bf16, row-major) during phase (1)
+  // only, in regions first written after it: the M and U^T record slots, the
+  // T and W^T tiles, and the float A tile.
+  static constexpr uint32_t RAWQ = B::MM;
+  static constexpr uint32_t RAWK = TT;
+  static constexpr uint32_t RAWV = AS;
+  static_assert(B::GC - B::MM >= kC * D * 2, "raw q must fit the M and U^T slots");
+  static_assert(AS - TT >= kC * D * 2, "raw k must fit the T and W^T tiles");
+  static_assert(kC * kC * 4 >= kC * D * 2, "raw v must fit the A tile");
   static constexpr uint32_t BYTES = TMEMP + 8;
   static constexpr uint32_t TMEM_COLS = (D == 128) ? 256 : 128;
 };
@@ -133,6 +143,7 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
   uint8_t *KH = sm + L::KH;
   float *part = reinterpret_cast<float *>(sm + L::PART);
   uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::BAR);
+  uint64_t *lbar = reinterpret_cast<uint64_t *>(sm + L::LBAR);
   uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(sm + L::TMEMP);
   WorkspaceHeader *hdr = reinterpret_cast<WorkspaceHeader *>(ws);
 
@@ -144,31 +155,50 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
 
   if (tid == 0) {
     ptx::mbar_init(bar, 1);
+    ptx::mbar_init(lbar, 1);
     ptx::fence_mbar_init();
   }
   if (warp == 0) {
     ptx::tmem_alloc(tmem_ptr, L::TMEM_COLS);
     ptx::tmem_relinquish();
   }
+  __syncthreads();  // barriers initialised before anyone waits on them
 
-  // ---- (1) decay prefix and decayed tiles: thread owns key channel c over R rows
+  // ---- (1) raw chunk rows of q, k, v -> shared memory (bulk copies into
+  // regions that are free until later phases), decay inputs -> registers
   const int c = tid % D, qtr = tid / D, r0 = qtr * R;
+  const size_t row0 = (size_t)bh * T + t0;
+  uint8_t *rawq = sm + L::RAWQ, *rawk = sm + L::RAWK, *rawv = sm + L::RAWV;
+  if (tid == 0) {
+    const uint32_t bytes = (uint32_t)valid * D * 2;
+    ptx::mbar_arrive_expect_tx(lbar, 3 * bytes);
+    ptx::bulk_g2s(rawq, q + row0 * D, bytes, lbar);
+    ptx::bulk_g2s(rawk, k + row0 * D, bytes, lbar);
+    ptx::bulk_g2s(rawv, v + row0 * D, bytes, lbar);
+  }
+  for (int idx = valid * D + tid; idx < kC * D; idx += 256) {  // zero the padded rows
+    reinterpret_cast<__nv_bfloat16 *>(rawq)[idx] = __float2bfloat16_rn(0.f);
+    reinterpret_cast<__nv_bfloat16 *>(rawk)[idx] = __float2bfloat16_rn(0.f);
+    reinterpret_cast<__nv_bfloat16 *>(rawv)[idx] = __float2bfloat16_rn(0.f);
+  }
   float ld[R], bt[R];
   {
-    const size_t row0 = (size_t)bh * T + t0;
+    float la[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) {  // unconditional (clamped) loads: all in flight at once
+      const int rr = min(r0 + i, valid - 1);
+      bt[i] = beta[row0 + rr];
+      la[i] = 0.f;
+      if (alpha_mode == KDA_ALPHA_CHANNEL)
+        la[i] = log_alpha[(row0 + rr) * D + c];
+      else if (alpha_mode == KDA_ALPHA_SCALAR)
+        la[i] = log_alpha[row0 + rr];
+    }
 #pragma unroll
     for (int i = 0; i < R; ++i) {
-      const int r = r0 + i;
-      float x = 0.f, b = 0.f;
-      if (r < valid) {
-        b = beta[row0 + r];
-        if (alpha_mode == KDA_ALPHA_CHANNEL)
-          x = -__expf(log_alpha[(row0 + r) * D + c]);
-        else if (alpha_mode == KDA_ALPHA_SCALAR)
-          x = -__expf(log_alpha[row0 + r]);
-      }
-      ld[i] = x;
-      bt[i] = b;
+      const bool live = r0 + i < valid;
+      ld[i] = (live && alpha_mode != KDA_ALPHA_NONE) ? -__expf(la[i]) : 0.f;
+      bt[i] = live ? bt[i] : 0.f;
     }
   }
   float psum = 0.f;
@@ -184,18 +214,18 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
     if (j < qtr) g += p;
   }
   const float egC = __expf(gC);
+  if (!ptx::mbar_wait(lbar, 0, kWaitLimit)) {
+    ok = false;
+    report_error(hdr, KDA_ERR_TIMEOUT, 0x100u);
+  }
   {
-    const size_t e0 = ((size_t)bh * T + t0) * D + c;
     float kbT[8], kbarT[8], vbT[8];
 #pragma unroll
     for (int i = 0; i < R; ++i) {
       const int r = r0 + i;
-      float kv = 0.f, qv = 0.f, vv = 0.f;
-      if (r < valid) {
-        kv = __bfloat162float(k[e0 + (size_t)r * D]);
-        qv = __bfloat162float(q[e0 + (size_t)r * D]);
-        vv = __bfloat162float(v[e0 + (size_t)r * D]);
-      }
+      const float kv = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(rawk)[r * D + c]);
+      const float qv = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(rawq)[r * D + c]);
+      const float vv = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(rawv)[r * D + c]);
       g += ld[i];
       const float eg = __expf(g), eng = __expf(-g);
       const float kb = bt[i] * kv * eg;
@@ -427,7 +457,7 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
     uint8_t *dst = ws + sizeof(WorkspaceHeader) + ((size_t)bh * NC + n) * B::BYTES;
     ptx::bulk_s2g(dst, blob, B::BYTES);
     ptx::bulk_commit();
-    ptx::bulk_wait_all();
+    ptx::bulk_wait_read_all();  // shared memory may be released once read
   }
   if (warp == 0) {
     ptx::tc_fence_after();
