@@ -48,7 +48,7 @@ constexpr uint32_t kWaitLimit = 1u << 24;  // polls before a wait gives up (~1 s
 template <int D>
 struct Blob {
   static constexpr uint32_t AP = 0;                     // Ap    [D rows][D]    K-major SW128
-  static constexpr uint32_t QP = AP + D * D * 2;        // Qp    [C rows][D]
+  static constexpr uint32_t QP = AP + D * D * 2;        // Qp^T [D rows][C] (D = 128), Qp [C rows][D] (D = 64)
   static constexpr uint32_t KBT = QP + kC * D * 2;      // Kbar^T[D rows][C]
   static constexpr uint32_t MM = KBT + D * kC * 2;      // M     [C rows][C]
   static constexpr uint32_t UT = MM + kC * kC * 2;      // U^T   [D rows][C]
@@ -96,36 +96,99 @@ struct PrepSmem {
   using B = Blob<D>;
   static constexpr uint32_t BLOB = 0;
   static constexpr uint32_t X1 = align1k(B::BYTES);        // [K_beta; Q*gamma] [128 rows][D]
-  static constexpr uint32_t TT = X1 + 128 * D * 2;         // T                 [C rows][C]
-  static constexpr uint32_t WT = TT + kC * kC * 2;         // W^T               [D rows][C]
-  static constexpr uint32_t AS = WT + D * kC * 2;          // A, float          [C][C] swizzled
+  static constexpr uint32_t TT = X1 + 128 * D * 2;         // T bf16 [C rows][C]; solve scratch before
+  static constexpr uint32_t WT = TT + kC * kC * 2;         // W^T [D rows][C]
+  static constexpr uint32_t AS = WT + D * kC * 2;          // A float [C][C], chunk-swizzled rows
   // D = 128 reuses the Ap and Qp slots of the record for X2 and Khat (both dead
   // before Ap and Qp are written); D = 64 gives them their own space.
-  static constexpr uint32_t X2 = (D == 128) ? B::AP : AS + kC * kC * 4;   // [K_beta^T; (beta V)^T] [2D rows][C]
-  static constexpr uint32_t KH = (D == 128) ? B::QP : X2 + 2 * D * kC * 2; // K/gamma  [C rows][D]
-  static constexpr uint32_t SMALL = (D == 128) ? AS + kC * kC * 4 : KH + kC * D * 2;
-  static constexpr uint32_t PART = SMALL;                  // float [4][D] partial decay sums
+  static constexpr uint32_t X2 = (D == 128) ? B::AP : AS + kC * kC * 4;     // [K_beta^T; (beta V)^T] [2D rows][C]
+  static constexpr uint32_t KH = (D == 128) ? B::QP : X2 + 2 * D * kC * 2;  // K/gamma  [C rows][D]
+  // D = 128: [I | -M], the B operand of Qp^T = [(Q*gamma)^T | W^T] [I | -M]^T, in the
+  // Qp slot between Khat's last use and Qp^T's write.
+  static constexpr uint32_t IM = B::QP;
+  // T as float during the blocked solve: in the W^T tile (D = 128) or its own space.
+  static constexpr uint32_t TF = (D == 128) ? WT : KH + kC * D * 2;
+  static constexpr uint32_t RAW = (D == 128) ? AS + kC * kC * 4 : TF + kC * kC * 4;  // q | k | v [C][D] bf16
+  static constexpr uint32_t PART = RAW + 3 * kC * D * 2;   // float [4][D] partial decay sums
   static constexpr uint32_t BAR = PART + 4 * D * 4;        // mbarrier (MMA commits)
   static constexpr uint32_t LBAR = BAR + 8;                // mbarrier (raw loads)
   static constexpr uint32_t TMEMP = LBAR + 8;              // TMEM base address
-  // Raw q, k, v rows of the chunk ([C][D] bf16, row-major) during phase (1)
-  // only, in regions first written after it: the M and U^T record slots, the
-  // T and W^T tiles, and the float A tile.
-  static constexpr uint32_t RAWQ = B::MM;
-  static constexpr uint32_t RAWK = TT;
-  static constexpr uint32_t RAWV = AS;
-  static_assert(B::GC - B::MM >= kC * D * 2, "raw q must fit the M and U^T slots");
-  static_assert(AS - TT >= kC * D * 2, "raw k must fit the T and W^T tiles");
-  static_assert(kC * kC * 4 >= kC * D * 2, "raw v must fit the A tile");
   static constexpr uint32_t BYTES = TMEMP + 8;
   static constexpr uint32_t TMEM_COLS = (D == 128) ? 256 : 128;
+  static_assert(D != 128 || D * kC * 2 >= kC * kC * 4, "T float must fit the W^T tile");
+  static_assert(BYTES + 1024 <= 232448, "prep shared memory");
 };
+
+// A float [C][C]: row r, 4-float chunk (c / 4) stored at chunk (c / 4) ^ (r % 16).
+__device__ __forceinline__ int as_idx(int r, int c) {
+  return r * kC + ((((c >> 2) ^ (r & 15)) << 2) | (c & 3));
+}
+
+// T = (I + A)^-1 for the strictly lower A in AS (float), by blocks of 16:
+// the four diagonal blocks by forward substitution (one column per thread),
+// then T_ij = -T_ii sum_{m=j}^{i-1} A_im T_mj along the sub-diagonals.
+// Leaves T (float, row-major, lower blocks only) in TF and T (bf16, zeros
+// above the diagonal) as a K-major [C][C] tile in TT.  Called by all 256
+// threads; XS (3 x 256 floats) is scratch inside TT.
+__device__ __forceinline__ void blocked_unit_lower_inverse(const float *AS, float *TF, uint8_t *TT,
+                                                           int tid) {
+  float *XS = reinterpret_cast<float *>(TT);
+  if (tid < kC) {
+    const int b = tid >> 4, j = tid & 15, o = b * 16;
+    float t[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) t[i] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float acc = 0.f;
+#pragma unroll
+      for (int m = 0; m < i; ++m) acc += AS[as_idx(o + i, o + m)] * t[m];
+      t[i] = (i == j) ? 1.f : -acc;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) TF[(o + i) * kC + o + j] = t[i];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int d = 1; d < 4; ++d) {
+    const int np = 4 - d;
+    for (int w = tid; w < np * 256; w += 256) {  // X_p = sum_m A_{p+d, m} T_{m, p}
+      const int pp = w >> 8, e = w & 255, r = e >> 4, c = e & 15;
+      const int bi = pp + d, bj = pp;
+      float acc = 0.f;
+      for (int bm = bj; bm < bi; ++bm)
+#pragma unroll
+        for (int s2 = 0; s2 < 16; ++s2)
+          acc += AS[as_idx(bi * 16 + r, bm * 16 + s2)] * TF[(bm * 16 + s2) * kC + bj * 16 + c];
+      XS[w] = acc;
+    }
+    __syncthreads();
+    for (int w = tid; w < np * 256; w += 256) {  // T_{p+d, p} = -T_{p+d, p+d} X_p
+      const int pp = w >> 8, e = w & 255, r = e >> 4, c = e & 15;
+      const int bi = pp + d, bj = pp;
+      float acc = 0.f;
+#pragma unroll
+      for (int s2 = 0; s2 < 16; ++s2)
+        acc += TF[(bi * 16 + r) * kC + bi * 16 + s2] * XS[pp * 256 + s2 * 16 + c];
+      TF[(bi * 16 + r) * kC + bj * 16 + c] = -acc;
+    }
+    __syncthreads();
+  }
+  for (int u = tid; u < kC * 8; u += 256) {  // bf16 operand tile, zeros above the diagonal blocks
+    const int row = u >> 3, c8 = u & 7;
+    float x[8];
+    const bool lower = (row >> 4) >= (c8 >> 1);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = lower ? TF[row * kC + c8 * 8 + e] : 0.f;
+    st_chunk(TT, row, c8, kC, x);
+  }
+}
 
 template <int D>
 __global__ void __launch_bounds__(256, 1)
 kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                 const __nv_bfloat16 *__restrict__ v, const float *__restrict__ beta,
-                const float *__restrict__ log_alpha, int alpha_mode, int T, int NC,
+                const float *__restrict__ log_alpha, int alpha_mode, int T, int NC, int total,
                 uint8_t *__restrict__ ws) {
   using B = Blob<D>;
   using L = PrepSmem<D>;
@@ -139,8 +202,11 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
   uint8_t *TT = sm + L::TT;
   uint8_t *WT = sm + L::WT;
   float *AS = reinterpret_cast<float *>(sm + L::AS);
+  float *TF = reinterpret_cast<float *>(sm + L::TF);
   uint8_t *X2 = sm + L::X2;
   uint8_t *KH = sm + L::KH;
+  uint8_t *IM = sm + L::IM;
+  uint8_t *rawq = sm + L::RAW, *rawk = rawq + kC * D * 2, *rawv = rawk + kC * D * 2;
   float *part = reinterpret_cast<float *>(sm + L::PART);
   uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::BAR);
   uint64_t *lbar = reinterpret_cast<uint64_t *>(sm + L::LBAR);
@@ -148,10 +214,19 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
   WorkspaceHeader *hdr = reinterpret_cast<WorkspaceHeader *>(ws);
 
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int n = blockIdx.x, bh = blockIdx.y;
-  const int t0 = n * kC;
-  const int valid = min(kC, T - t0);
+  const int c = tid % D, qtr = tid / D, r0 = qtr * R;
   bool ok = true;
+
+  auto issue_raw = [&](int idx) {  // bulk copies of one chunk's q, k, v rows
+    const int bh = idx / NC, t0 = (idx % NC) * kC;
+    const int valid = min(kC, T - t0);
+    const size_t row0 = (size_t)bh * T + t0;
+    const uint32_t bytes = (uint32_t)valid * D * 2;
+    ptx::mbar_arrive_expect_tx(lbar, 3 * bytes);
+    ptx::bulk_g2s(rawq, q + row0 * D, bytes, lbar);
+    ptx::bulk_g2s(rawk, k + row0 * D, bytes, lbar);
+    ptx::bulk_g2s(rawv, v + row0 * D, bytes, lbar);
+  };
 
   if (tid == 0) {
     ptx::mbar_init(bar, 1);
@@ -162,303 +237,304 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
     ptx::tmem_alloc(tmem_ptr, L::TMEM_COLS);
     ptx::tmem_relinquish();
   }
-  __syncthreads();  // barriers initialised before anyone waits on them
-
-  // ---- (1) raw chunk rows of q, k, v -> shared memory (bulk copies into
-  // regions that are free until later phases), decay inputs -> registers
-  const int c = tid % D, qtr = tid / D, r0 = qtr * R;
-  const size_t row0 = (size_t)bh * T + t0;
-  uint8_t *rawq = sm + L::RAWQ, *rawk = sm + L::RAWK, *rawv = sm + L::RAWV;
-  if (tid == 0) {
-    const uint32_t bytes = (uint32_t)valid * D * 2;
-    ptx::mbar_arrive_expect_tx(lbar, 3 * bytes);
-    ptx::bulk_g2s(rawq, q + row0 * D, bytes, lbar);
-    ptx::bulk_g2s(rawk, k + row0 * D, bytes, lbar);
-    ptx::bulk_g2s(rawv, v + row0 * D, bytes, lbar);
-  }
-  for (int idx = valid * D + tid; idx < kC * D; idx += 256) {  // zero the padded rows
-    reinterpret_cast<__nv_bfloat16 *>(rawq)[idx] = __float2bfloat16_rn(0.f);
-    reinterpret_cast<__nv_bfloat16 *>(rawk)[idx] = __float2bfloat16_rn(0.f);
-    reinterpret_cast<__nv_bfloat16 *>(rawv)[idx] = __float2bfloat16_rn(0.f);
-  }
-  float ld[R], bt[R];
-  {
-    float la[R];
-#pragma unroll
-    for (int i = 0; i < R; ++i) {  // unconditional (clamped) loads: all in flight at once
-      const int rr = min(r0 + i, valid - 1);
-      bt[i] = beta[row0 + rr];
-      la[i] = 0.f;
-      if (alpha_mode == KDA_ALPHA_CHANNEL)
-        la[i] = log_alpha[(row0 + rr) * D + c];
-      else if (alpha_mode == KDA_ALPHA_SCALAR)
-        la[i] = log_alpha[row0 + rr];
-    }
-#pragma unroll
-    for (int i = 0; i < R; ++i) {
-      const bool live = r0 + i < valid;
-      ld[i] = (live && alpha_mode != KDA_ALPHA_NONE) ? -__expf(la[i]) : 0.f;
-      bt[i] = live ? bt[i] : 0.f;
-    }
-  }
-  float psum = 0.f;
-#pragma unroll
-  for (int i = 0; i < R; ++i) psum += ld[i];
-  part[qtr * D + c] = psum;
-  __syncthreads();
-  float g = 0.f, gC = 0.f;
-#pragma unroll
-  for (int j = 0; j < Q4; ++j) {
-    const float p = part[j * D + c];
-    gC += p;
-    if (j < qtr) g += p;
-  }
-  const float egC = __expf(gC);
-  if (!ptx::mbar_wait(lbar, 0, kWaitLimit)) {
-    ok = false;
-    report_error(hdr, KDA_ERR_TIMEOUT, 0x100u);
-  }
-  {
-    float kbT[8], kbarT[8], vbT[8];
-#pragma unroll
-    for (int i = 0; i < R; ++i) {
-      const int r = r0 + i;
-      const float kv = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(rawk)[r * D + c]);
-      const float qv = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(rawq)[r * D + c]);
-      const float vv = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(rawv)[r * D + c]);
-      g += ld[i];
-      const float eg = __expf(g), eng = __expf(-g);
-      const float kb = bt[i] * kv * eg;
-      st_bf16(X1, umma::sw128_off(r, c, 128), kb);               // K_beta
-      st_bf16(X1, umma::sw128_off(kC + r, c, 128), qv * eg);     // Q * gamma
-      st_bf16(KH, umma::sw128_off(r, c, kC), kv * eng);          // K / gamma
-      kbT[i & 7] = kb;
-      kbarT[i & 7] = kv * eng * egC;
-      vbT[i & 7] = bt[i] * vv;
-      if ((i & 7) == 7) {
-        const int c8 = (r0 + i) >> 3;
-        st_chunk(X2, c, c8, 2 * D, kbT);                          // K_beta^T
-        st_chunk(X2, D + c, c8, 2 * D, vbT);                      // (beta V)^T
-        st_chunk(blob + B::KBT, c, c8, D, kbarT);                 // Kbar^T (output)
-      }
-    }
-    if (qtr == 0) reinterpret_cast<float *>(blob + B::GC)[c] = egC;
-  }
-  ptx::fence_proxy_async_smem();
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_ptr;
   const uint32_t sX1 = ptx::smem_u32(X1), sKH = ptx::smem_u32(KH), sX2 = ptx::smem_u32(X2);
-  const uint32_t sTT = ptx::smem_u32(TT), sWT = ptx::smem_u32(WT);
-  const uint32_t sKBT = ptx::smem_u32(blob + B::KBT), sMM = ptx::smem_u32(blob + B::MM);
+  const uint32_t sTT = ptx::smem_u32(TT), sWT = ptx::smem_u32(WT), sIM = ptx::smem_u32(IM);
+  const uint32_t sKBT = ptx::smem_u32(blob + B::KBT);
+  if (tid == 0 && (int)blockIdx.x < total) issue_raw(blockIdx.x);
+  uint32_t mma_phase = 0;
 
-  // ---- (2) [A_full; M_full] = [K_beta; Q*gamma] (K/gamma)^T  -> TMEM cols [0, 64)
-  if (tid == 0) {
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks)
-      ptx::mma_bf16_ss(tmem, umma::sdesc_k(sX1, 128, ks), umma::sdesc_k(sKH, kC, ks),
-                       umma::idesc_bf16(128, kC), ks > 0);
-    ptx::mma_commit(bar);
-  }
-  if (!ptx::mbar_wait(bar, 0, kWaitLimit)) {
-    ok = false;
-    report_error(hdr, KDA_ERR_TIMEOUT, 0x101u);
-  }
-  ptx::tc_fence_after();
+  for (int idx = blockIdx.x, it = 0; idx < total; idx += gridDim.x, ++it) {
+    const int bh = idx / NC, n = idx % NC;
+    const int t0 = n * kC;
+    const int valid = min(kC, T - t0);
+    const size_t row0 = (size_t)bh * T + t0;
 
-  // ---- (3) rows 0..63: A (strict lower) to shared memory; rows 64..127: M
-  if (warp < 4) {
-    const int lane_row = tid;  // TMEM lane
-    const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16);
+    // ---- (1) decay inputs (all in flight at once), then the raw rows
+    float ld[R], bt[R];
+    {
+      float la[R];
 #pragma unroll
-    for (int cb = 0; cb < kC; cb += 16) {
-      float x[16];
-      ptx::tmem_ld16(ta + cb, x);
-      ptx::tmem_ld_wait();
-      if (lane_row < kC) {
-        const int r = lane_row;
+      for (int i = 0; i < R; ++i) {
+        const int rr = min(r0 + i, valid - 1);
+        bt[i] = beta[row0 + rr];
+        la[i] = 0.f;
+        if (alpha_mode == KDA_ALPHA_CHANNEL)
+          la[i] = log_alpha[(row0 + rr) * D + c];
+        else if (alpha_mode == KDA_ALPHA_SCALAR)
+          la[i] = log_alpha[row0 + rr];
+      }
 #pragma unroll
-        for (int j4 = 0; j4 < 4; ++j4) {
-          const int m0 = cb + 4 * j4;
-          float4 a;
-          a.x = (m0 + 0 < r) ? x[4 * j4 + 0] : 0.f;
-          a.y = (m0 + 1 < r) ? x[4 * j4 + 1] : 0.f;
-          a.z = (m0 + 2 < r) ? x[4 * j4 + 2] : 0.f;
-          a.w = (m0 + 3 < r) ? x[4 * j4 + 3] : 0.f;
-          reinterpret_cast<float4 *>(AS)[r * 16 + ((m0 >> 2) ^ (r & 15))] = a;
+      for (int i = 0; i < R; ++i) {
+        const bool live = r0 + i < valid;
+        ld[i] = (live && alpha_mode != KDA_ALPHA_NONE) ? -__expf(la[i]) : 0.f;
+        bt[i] = live ? bt[i] : 0.f;
+      }
+    }
+    float psum = 0.f;
+#pragma unroll
+    for (int i = 0; i < R; ++i) psum += ld[i];
+    part[qtr * D + c] = psum;
+    if (tid == 0) ptx::bulk_wait_read_all();  // the previous record has left shared memory
+    if (ok && !ptx::mbar_wait(lbar, it & 1, kWaitLimit)) {
+      ok = false;
+      report_error(hdr, KDA_ERR_TIMEOUT, 0x100u);
+    }
+    for (int idx2 = valid * D + tid; idx2 < kC * D; idx2 += 256) {  // zero the padded rows
+      reinterpret_cast<__nv_bfloat16 *>(rawq)[idx2] = __float2bfloat16_rn(0.f);
+      reinterpret_cast<__nv_bfloat16 *>(rawk)[idx2] = __float2bfloat16_rn(0.f);
+      reinterpret_cast<__nv_bfloat16 *>(rawv)[idx2] = __float2bfloat16_rn(0.f);
+    }
+    __syncthreads();
+    float g = 0.f, gC = 0.f;
+#pragma unroll
+    for (int j = 0; j < Q4; ++j) {
+      const float p = part[j * D + c];
+      gC += p;
+      if (j < qtr) g += p;
+    }
+    const float egC = __expf(gC);
+    {
+      float kbT[8], kbarT[8], vbT[8];
+#pragma unroll
+      for (int i = 0; i < R; ++i) {
+        const int r = r0 + i;
+        const float kv = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(rawk)[r * D + c]);
+        const float qv = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(rawq)[r * D + c]);
+        const float vv = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(rawv)[r * D + c]);
+        g += ld[i];
+        const float eg = __expf(g), eng = __expf(-g);
+        const float kb = bt[i] * kv * eg;
+        st_bf16(X1, umma::sw128_off(r, c, 128), kb);               // K_beta
+        st_bf16(X1, umma::sw128_off(kC + r, c, 128), qv * eg);     // Q * gamma
+        st_bf16(KH, umma::sw128_off(r, c, kC), kv * eng);          // K / gamma
+        kbT[i & 7] = kb;
+        kbarT[i & 7] = kv * eng * egC;
+        vbT[i & 7] = bt[i] * vv;
+        if ((i & 7) == 7) {
+          const int c8 = (r0 + i) >> 3;
+          st_chunk(X2, c, c8, 2 * D, kbT);                          // K_beta^T
+          st_chunk(X2, D + c, c8, 2 * D, vbT);                      // (beta V)^T
+          st_chunk(blob + B::KBT, c, c8, D, kbarT);                 // Kbar^T (output)
         }
-      } else {
-        const int r = lane_row - kC;
-        float mrow[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) mrow[j] = (cb + j <= r) ? x[j] : 0.f;
-        st_chunk(blob + B::MM, r, cb >> 3, kC, mrow);
-        st_chunk(blob + B::MM, r, (cb >> 3) + 1, kC, mrow + 8);
       }
+      if (qtr == 0) reinterpret_cast<float *>(blob + B::GC)[c] = egC;
     }
-  }
-  __syncthreads();
+    ptx::fence_proxy_async_smem();
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (tid == 0 && idx + (int)gridDim.x < total) issue_raw(idx + gridDim.x);  // prefetch
 
-  // ---- (4) T = (I + A)^-1 by forward substitution, one column per thread
-  if (tid < kC) {
-    const int j = tid;
-    float t[kC];
+    // ---- (2) [A_full; M_full] = [K_beta; Q*gamma] (K/gamma)^T  -> TMEM cols [0, 64)
+    if (tid == 0) {
 #pragma unroll
-    for (int i = 0; i < kC; ++i) {
-      float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-      for (int b = 0; b < (i + 3) / 4; ++b) {
-        const float4 a = reinterpret_cast<const float4 *>(AS)[i * 16 + (b ^ (i & 15))];
-        if (4 * b + 0 < i) acc0 += a.x * t[4 * b + 0];
-        if (4 * b + 1 < i) acc1 += a.y * t[4 * b + 1];
-        if (4 * b + 2 < i) acc0 += a.z * t[4 * b + 2];
-        if (4 * b + 3 < i) acc1 += a.w * t[4 * b + 3];
-      }
-      t[i] = (i == j) ? 1.f : -(acc0 + acc1);
-    }
-#pragma unroll
-    for (int i = 0; i < kC; ++i) st_bf16(TT, umma::sw128_off(i, j, kC), t[i]);
-  }
-  ptx::fence_proxy_async_smem();
-  ptx::tc_fence_before();
-  __syncthreads();
-  ptx::tc_fence_after();
-
-  // ---- (5) [W^T; U^T] = [K_beta^T; (beta V)^T] T^T  -> TMEM cols [64, 192) or [64, 128)
-  if (tid == 0) {
-#pragma unroll
-    for (int h = 0; h < 2 * D / 128; ++h)
-#pragma unroll
-      for (int ks = 0; ks < kC / 16; ++ks)
-        ptx::mma_bf16_ss(tmem + 64 + 64 * h, umma::sdesc_k(sX2 + h * 128 * 128, 2 * D, ks),
-                         umma::sdesc_k(sTT, kC, ks), umma::idesc_bf16(128, kC), ks > 0);
-    ptx::mma_commit(bar);
-  }
-  if (ok && !ptx::mbar_wait(bar, 1, kWaitLimit)) {
-    ok = false;
-    report_error(hdr, KDA_ERR_TIMEOUT, 0x102u);
-  }
-  ptx::tc_fence_after();
-
-  // ---- (6) W^T -> operand tile, U^T -> record
-  if (warp < 4) {
-    const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16);
-#pragma unroll
-    for (int h = 0; h < 2 * D / 128; ++h) {
-#pragma unroll
-      for (int cb = 0; cb < kC; cb += 16) {
-        float x[16];
-        ptx::tmem_ld16(ta + 64 + 64 * h + cb, x);
-        ptx::tmem_ld_wait();
-        // D = 128: h = 0 holds W^T rows (= lane), h = 1 U^T rows.
-        // D = 64:  lanes 0..63 W^T rows, lanes 64..127 U^T rows.
-        const int lane_row = tid;
-        const bool isW = (D == 128) ? (h == 0) : (lane_row < D);
-        const int row = (D == 128) ? lane_row : (lane_row % D);
-        uint8_t *dst = isW ? WT : blob + B::UT;
-        st_chunk(dst, row, cb >> 3, D, x);
-        st_chunk(dst, row, (cb >> 3) + 1, D, x + 8);
-      }
-    }
-  }
-  ptx::fence_proxy_async_smem();
-  ptx::tc_fence_before();
-  __syncthreads();
-  ptx::tc_fence_after();
-
-  // ---- (7) Kbar^T W  (and M W)  -> TMEM
-  if (tid == 0) {
-    if (D == 128) {
-      // cols [0, 128): Kbar^T W  (M = 128, N = 128)
-#pragma unroll
-      for (int ks = 0; ks < kC / 16; ++ks)
-        ptx::mma_bf16_ss(tmem, umma::sdesc_k(sKBT, D, ks), umma::sdesc_k(sWT, D, ks),
-                         umma::idesc_bf16(128, D), ks > 0);
-      // cols [128, 192): (M W)^T = W^T M^T  (M = 128, N = 64)
-#pragma unroll
-      for (int ks = 0; ks < kC / 16; ++ks)
-        ptx::mma_bf16_ss(tmem + 128, umma::sdesc_k(sWT, D, ks), umma::sdesc_k(sMM, kC, ks),
+      for (int ks = 0; ks < D / 16; ++ks)
+        ptx::mma_bf16_ss(tmem, umma::sdesc_k(sX1, 128, ks), umma::sdesc_k(sKH, kC, ks),
                          umma::idesc_bf16(128, kC), ks > 0);
-    } else {
-      // cols [0, 64): [Kbar^T; M] W  (Kbar^T and M are adjacent in the record)
-#pragma unroll
-      for (int ks = 0; ks < kC / 16; ++ks)
-        ptx::mma_bf16_ss(tmem, umma::sdesc_k(sKBT, 128, ks), umma::sdesc_k(sWT, D, ks),
-                         umma::idesc_bf16(128, D), ks > 0);
+      ptx::mma_commit(bar);
     }
-    ptx::mma_commit(bar);
-  }
-  if (ok && !ptx::mbar_wait(bar, 0, kWaitLimit)) {
-    ok = false;
-    report_error(hdr, KDA_ERR_TIMEOUT, 0x103u);
-  }
-  ptx::tc_fence_after();
+    if (ok && !ptx::mbar_wait(bar, mma_phase & 1, kWaitLimit)) {
+      ok = false;
+      report_error(hdr, KDA_ERR_TIMEOUT, 0x101u);
+    }
+    ++mma_phase;
+    ptx::tc_fence_after();
 
-  // ---- (8) Ap = -Kbar^T W;  Qp = Q*gamma - M W
-  if (warp < 4) {
-    const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16);
-    const int lane_row = tid;
-    if (D == 128) {
-#pragma unroll
-      for (int cb = 0; cb < D; cb += 16) {
-        float x[16];
-        ptx::tmem_ld16(ta + cb, x);
-        ptx::tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) x[j] = -x[j];
-        st_chunk(blob + B::AP, lane_row, cb >> 3, D, x);
-        st_chunk(blob + B::AP, lane_row, (cb >> 3) + 1, D, x + 8);
-      }
-      // (M W)^T: lane = key channel cc, column = token r
-      const int cc = lane_row;
+    // ---- (3) rows 0..63: A (strict lower) as float; rows 64..127: M (and [I | -M])
+    if (warp < 4) {
+      const int lane_row = tid;
+      const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16);
 #pragma unroll
       for (int cb = 0; cb < kC; cb += 16) {
         float x[16];
-        ptx::tmem_ld16(ta + 128 + cb, x);
-        ptx::tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int r = cb + j;
-          const float qg = ld_bf16(X1, umma::sw128_off(kC + r, cc, 128));
-          st_bf16(blob + B::QP, umma::sw128_off(r, cc, kC), qg - x[j]);
-        }
-      }
-    } else {
-#pragma unroll
-      for (int cb = 0; cb < D; cb += 16) {
-        float x[16];
         ptx::tmem_ld16(ta + cb, x);
         ptx::tmem_ld_wait();
-        if (lane_row < D) {
+        if (lane_row < kC) {
+          const int r = lane_row;
+#pragma unroll
+          for (int j4 = 0; j4 < 4; ++j4) {
+            const int m0 = cb + 4 * j4;
+            float4 a;
+            a.x = (m0 + 0 < r) ? x[4 * j4 + 0] : 0.f;
+            a.y = (m0 + 1 < r) ? x[4 * j4 + 1] : 0.f;
+            a.z = (m0 + 2 < r) ? x[4 * j4 + 2] : 0.f;
+            a.w = (m0 + 3 < r) ? x[4 * j4 + 3] : 0.f;
+            *reinterpret_cast<float4 *>(AS + as_idx(r, m0)) = a;
+          }
+        } else {
+          const int r = lane_row - kC;
+          float mrow[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) mrow[j] = (cb + j <= r) ? x[j] : 0.f;
+          st_chunk(blob + B::MM, r, cb >> 3, kC, mrow);
+          st_chunk(blob + B::MM, r, (cb >> 3) + 1, kC, mrow + 8);
+          if (D == 128) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) mrow[j] = -mrow[j];
+            st_chunk(IM, r, 8 + (cb >> 3), kC, mrow);               // K atom 1: -M
+            st_chunk(IM, r, 8 + (cb >> 3) + 1, kC, mrow + 8);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) mrow[j] = (cb + j == r) ? 1.f : 0.f;
+            st_chunk(IM, r, cb >> 3, kC, mrow);                     // K atom 0: I
+            st_chunk(IM, r, (cb >> 3) + 1, kC, mrow + 8);
+          }
+        }
+      }
+    }
+    __syncthreads();
+
+    // ---- (4) T = (I + A)^-1 (blocked forward substitution)
+    blocked_unit_lower_inverse(AS, TF, TT, tid);
+    ptx::fence_proxy_async_smem();
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+
+    // ---- (5) [W^T; U^T] = [K_beta^T; (beta V)^T] T^T  -> TMEM cols [64, 192) or [64, 128)
+    if (tid == 0) {
+#pragma unroll
+      for (int h = 0; h < 2 * D / 128; ++h)
+#pragma unroll
+        for (int ks = 0; ks < kC / 16; ++ks)
+          ptx::mma_bf16_ss(tmem + 64 + 64 * h, umma::sdesc_k(sX2 + h * 128 * 128, 2 * D, ks),
+                           umma::sdesc_k(sTT, kC, ks), umma::idesc_bf16(128, kC), ks > 0);
+      ptx::mma_commit(bar);
+    }
+    if (ok && !ptx::mbar_wait(bar, mma_phase & 1, kWaitLimit)) {
+      ok = false;
+      report_error(hdr, KDA_ERR_TIMEOUT, 0x102u);
+    }
+    ++mma_phase;
+    ptx::tc_fence_after();
+
+    // ---- (6) W^T -> operand tile, U^T -> record
+    if (warp < 4) {
+      const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16);
+#pragma unroll
+      for (int h = 0; h < 2 * D / 128; ++h) {
+#pragma unroll
+        for (int cb = 0; cb < kC; cb += 16) {
+          float x[16];
+          ptx::tmem_ld16(ta + 64 + 64 * h + cb, x);
+          ptx::tmem_ld_wait();
+          // D = 128: h = 0 holds W^T rows (= lane), h = 1 U^T rows.
+          // D = 64:  lanes 0..63 W^T rows, lanes 64..127 U^T rows.
+          const int lane_row = tid;
+          const bool isW = (D == 128) ? (h == 0) : (lane_row < D);
+          const int row = (D == 128) ? lane_row : (lane_row % D);
+          uint8_t *dst = isW ? WT : blob + B::UT;
+          st_chunk(dst, row, cb >> 3, D, x);
+          st_chunk(dst, row, (cb >> 3) + 1, D, x + 8);
+        }
+      }
+    }
+    ptx::fence_proxy_async_smem();
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+
+    // ---- (7) Kbar^T W, and Qp (D = 128: Qp^T directly; D = 64: M W)
+    if (tid == 0) {
+      if (D == 128) {
+        // cols [0, 128): Kbar^T W  (M = 128, N = 128)
+#pragma unroll
+        for (int ks = 0; ks < kC / 16; ++ks)
+          ptx::mma_bf16_ss(tmem, umma::sdesc_k(sKBT, D, ks), umma::sdesc_k(sWT, D, ks),
+                           umma::idesc_bf16(128, D), ks > 0);
+        // cols [128, 192): Qp^T = (Q*gamma)^T I - W^T M^T: A = [(Q*gamma)^T | W^T]
+        // (the first half read MN-major from the Q*gamma rows of X1), B^T = [I | -M]
+#pragma unroll
+        for (int ks = 0; ks < kC / 16; ++ks)
+          ptx::mma_bf16_ss(tmem + 128, umma::sdesc_mn(sX1 + 8192, 128, ks),
+                           umma::sdesc_k(sIM, kC, ks), umma::idesc_bf16_amn(128, kC), ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < kC / 16; ++ks)
+          ptx::mma_bf16_ss(tmem + 128, umma::sdesc_k(sWT, D, ks),
+                           umma::sdesc_k(sIM, kC, 4 + ks), umma::idesc_bf16(128, kC), 1);
+      } else {
+        // cols [0, 64): [Kbar^T; M] W  (Kbar^T and M are adjacent in the record)
+#pragma unroll
+        for (int ks = 0; ks < kC / 16; ++ks)
+          ptx::mma_bf16_ss(tmem, umma::sdesc_k(sKBT, 128, ks), umma::sdesc_k(sWT, D, ks),
+                           umma::idesc_bf16(128, D), ks > 0);
+      }
+      ptx::mma_commit(bar);
+    }
+    if (ok && !ptx::mbar_wait(bar, mma_phase & 1, kWaitLimit)) {
+      ok = false;
+      report_error(hdr, KDA_ERR_TIMEOUT, 0x103u);
+    }
+    ++mma_phase;
+    ptx::tc_fence_after();
+
+    // ---- (8) Ap = -Kbar^T W;  Qp
+    if (warp < 4) {
+      const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16);
+      const int lane_row = tid;
+      if (D == 128) {
+#pragma unroll
+        for (int cb = 0; cb < D; cb += 16) {
+          float x[16];
+          ptx::tmem_ld16(ta + cb, x);
+          ptx::tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 16; ++j) x[j] = -x[j];
           st_chunk(blob + B::AP, lane_row, cb >> 3, D, x);
           st_chunk(blob + B::AP, lane_row, (cb >> 3) + 1, D, x + 8);
-        } else {
-          const int r = lane_row - D;
-          float qg[16];
-          ld_chunk(X1, kC + r, cb >> 3, 128, qg);
-          ld_chunk(X1, kC + r, (cb >> 3) + 1, 128, qg + 8);
+        }
+        // Qp^T: lane = key channel, column = token
 #pragma unroll
-          for (int j = 0; j < 16; ++j) qg[j] -= x[j];
-          st_chunk(blob + B::QP, r, cb >> 3, kC, qg);
-          st_chunk(blob + B::QP, r, (cb >> 3) + 1, kC, qg + 8);
+        for (int cb = 0; cb < kC; cb += 16) {
+          float x[16];
+          ptx::tmem_ld16(ta + 128 + cb, x);
+          ptx::tmem_ld_wait();
+          st_chunk(blob + B::QP, lane_row, cb >> 3, D, x);
+          st_chunk(blob + B::QP, lane_row, (cb >> 3) + 1, D, x + 8);
+        }
+      } else {
+#pragma unroll
+        for (int cb = 0; cb < D; cb += 16) {
+          float x[16];
+          ptx::tmem_ld16(ta + cb, x);
+          ptx::tmem_ld_wait();
+          if (lane_row < D) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) x[j] = -x[j];
+            st_chunk(blob + B::AP, lane_row, cb >> 3, D, x);
+            st_chunk(blob + B::AP, lane_row, (cb >> 3) + 1, D, x + 8);
+          } else {
+            const int r = lane_row - D;
+            float qg[16];
+            ld_chunk(X1, kC + r, cb >> 3, 128, qg);
+            ld_chunk(X1, kC + r, (cb >> 3) + 1, 128, qg + 8);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) qg[j] -= x[j];
+            st_chunk(blob + B::QP, r, cb >> 3, kC, qg);
+            st_chunk(blob + B::QP, r, (cb >> 3) + 1, kC, qg + 8);
+          }
         }
       }
     }
+    ptx::fence_proxy_async_smem();
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+
+    // ---- (9) record -> workspace (one bulk copy; its read is awaited before
+    // the record region is written again)
+    if (tid == 0) {
+      uint8_t *dst = ws + sizeof(WorkspaceHeader) + (size_t)idx * B::BYTES;
+      ptx::bulk_s2g(dst, blob, B::BYTES);
+      ptx::bulk_commit();
+    }
   }
-  ptx::fence_proxy_async_smem();
+  if (tid == 0) ptx::bulk_wait_all();
   ptx::tc_fence_before();
   __syncthreads();
-
-  // ---- (9) record -> workspace (one bulk copy), release TMEM
-  if (tid == 0) {
-    uint8_t *dst = ws + sizeof(WorkspaceHeader) + ((size_t)bh * NC + n) * B::BYTES;
-    ptx::bulk_s2g(dst, blob, B::BYTES);
-    ptx::bulk_commit();
-    ptx::bulk_wait_read_all();  // shared memory may be released once read
-  }
   if (warp == 0) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, L::TMEM_COLS);
@@ -626,9 +702,9 @@ kda_scan_kernel(const float *__restrict__ h0, __nv_bfloat16 *__restrict__ o,
           ptx::mma_bf16_ss(tmem, umma::sdesc_k(sKB, D, ks), umma::sdesc_k(sUT, NB, ks),
                            umma::idesc_bf16(128, NB), 1);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          ptx::mma_bf16_ss(tmem + NB, umma::sdesc_k(sQP, kC, ks), umma::sdesc_k(sSB, NB, ks),
-                           umma::idesc_bf16(64, NB), ks > 0);
+        for (int ks = 0; ks < D / 16; ++ks)  // Qp is stored transposed: MN-major A
+          ptx::mma_bf16_ss(tmem + NB, umma::sdesc_mn(sQP, D, ks), umma::sdesc_k(sSB, NB, ks),
+                           umma::idesc_bf16_amn(64, NB), ks > 0);
 #pragma unroll
         for (int ks = 0; ks < kC / 16; ++ks)
           ptx::mma_bf16_ss(tmem + NB, umma::sdesc_k(sMM, kC, ks), umma::sdesc_k(sUT, NB, ks),
@@ -699,10 +775,17 @@ kda_status launch_d(const void *q, const void *k, const void *v, const float *be
                            (int)scan_smem) != cudaSuccess)
     return KDA_ERR_CUDA;
   if (NC > 0) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return KDA_ERR_CUDA;
+    const long long total = (long long)BH * NC;
+    if (total > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
+    const int grid = (int)(total < sms ? total : sms);  // persistent: one CTA per SM
     timer.mark();
-    kda_prep_kernel<D><<<dim3(NC, BH), 256, prep_smem, st>>>(
+    kda_prep_kernel<D><<<grid, 256, prep_smem, st>>>(
         static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
-        static_cast<const __nv_bfloat16 *>(v), beta, log_alpha, (int)am, T, NC, ws);
+        static_cast<const __nv_bfloat16 *>(v), beta, log_alpha, (int)am, T, NC, (int)total, ws);
   }
   timer.mark();
   kda_scan_kernel<D, NB><<<dim3(D / NB, BH), 128, scan_smem, st>>>(

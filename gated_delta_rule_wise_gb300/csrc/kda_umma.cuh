@@ -48,11 +48,28 @@ __device__ __forceinline__ uint64_t sdesc_k(uint32_t tile, int rows, int ks) {
   return sdesc(tile + (uint32_t)(ks >> 2) * rows * 128u + (uint32_t)(ks & 3) * 32u);
 }
 
+// Descriptor of the K-slice [16*ks, 16*ks + 16) of an MN-major operand stored
+// as a K-major SW128 tile whose ROWS run along K (the operand's K index) and
+// whose columns run along MN: the same bytes as the tile of the transposed
+// matrix.  `tile_rows` is the row count of the containing tile (its 64-column
+// blocks are tile_rows * 128 B apart); `tile` may point at a row that is a
+// multiple of 8 inside it.
+__device__ __forceinline__ uint64_t sdesc_mn(uint32_t tile, int tile_rows, int ks) {
+  uint64_t d = (uint64_t)(((tile + (uint32_t)ks * 2048u) & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(((uint32_t)tile_rows * 128u) >> 4) << 16;  // between 64-wide MN blocks
+  d |= (uint64_t)(1024u >> 4) << 32;                         // between 8-row K groups
+  d |= (uint64_t)1u << 46;
+  d |= (uint64_t)2u << 61;
+  return d;
+}
+
 // Instruction descriptor: D f32, A and B bf16, both K-major, shape M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
          ((uint32_t)(M >> 4) << 24);
 }
+// Same with the A operand MN-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_amn(int M, int N) { return idesc_bf16(M, N) | (1u << 15); }
 
 }  // namespace umma
 }  // namespace kda

@@ -1,8 +1,9 @@
 """White-box checks of the tensor-core prefill path.
 
 The prep kernel leaves one record per (head, chunk) in the workspace:
-Ap = -Kbar^T W, Qp = Q*gamma - M W, Kbar^T, M, U^T (bf16 tiles in the 128-byte
-swizzled K-major operand layout) and gamma_C (float).  These tests decode the
+Ap = -Kbar^T W, Qp = Q*gamma - M W (stored transposed when D = 128), Kbar^T,
+M, U^T (bf16 tiles in the 128-byte swizzled K-major operand layout) and
+gamma_C (float).  These tests decode the
 records and compare each matrix with a float64 numpy evaluation of its
 definition (the chunk-wise form with cumulative decay), then check that the
 tensor path and the CUDA-core path agree on o and hT.  End-to-end parity with
@@ -92,7 +93,9 @@ def test_prep_records_match_definitions(D, alpha):
                                   pad(x["k"][0, h, sl].astype(np.float64)),
                                   pad(x["v"][0, h, sl].astype(np.float64)),
                                   pad(x["beta"][0, h, sl].astype(np.float64)), la)
-            got = dict(AP=untile(rec[L["AP"]:L["QP"]], D, D), QP=untile(rec[L["QP"]:L["KBT"]], C, D),
+            qp = (untile(rec[L["QP"]:L["KBT"]], D, C).T if D == 128
+                  else untile(rec[L["QP"]:L["KBT"]], C, D))
+            got = dict(AP=untile(rec[L["AP"]:L["QP"]], D, D), QP=qp,
                        KBT=untile(rec[L["KBT"]:L["MM"]], D, C), MM=untile(rec[L["MM"]:L["UT"]], C, C),
                        UT=untile(rec[L["UT"]:L["GC"]], D, C),
                        GC=np.frombuffer(rec[L["GC"]:L["BYTES"]], dtype=np.float32).astype(np.float64))
