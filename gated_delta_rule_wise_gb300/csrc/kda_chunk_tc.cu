@@ -119,67 +119,79 @@ struct PrepSmem {
   static_assert(BYTES + 1024 <= 232448, "prep shared memory");
 };
 
-// A float [C][C]: row r, 4-float chunk (c / 4) stored at chunk (c / 4) ^ (r % 16).
-__device__ __forceinline__ int as_idx(int r, int c) {
-  return r * kC + ((((c >> 2) ^ (r & 15)) << 2) | (c & 3));
+// Float [C][C] matrices (A, T) in shared memory: row r, 4-float chunk j of
+// the row stored at chunk j ^ (r % 8), so column reads across 8 rows and
+// 16-byte row writes are both free of bank conflicts.
+__device__ __forceinline__ int sw8(int r, int c) {
+  return r * kC + ((((c >> 2) ^ (r & 7)) << 2) | (c & 3));
+}
+__device__ __forceinline__ float4 &at4(float *M, int r, int c0) {
+  return *reinterpret_cast<float4 *>(M + r * kC + (((c0 >> 2) ^ (r & 7)) << 2));
+}
+__device__ __forceinline__ void fma4(float4 &acc, float a, const float4 &b) {
+  acc.x += a * b.x; acc.y += a * b.y; acc.z += a * b.z; acc.w += a * b.w;
 }
 
 // T = (I + A)^-1 for the strictly lower A in AS (float), by blocks of 16:
 // the four diagonal blocks by forward substitution (one column per thread),
-// then T_ij = -T_ii sum_{m=j}^{i-1} A_im T_mj along the sub-diagonals.
-// Leaves T (float, row-major, lower blocks only) in TF and T (bf16, zeros
-// above the diagonal) as a K-major [C][C] tile in TT.  Called by all 256
-// threads; XS (3 x 256 floats) is scratch inside TT.
-__device__ __forceinline__ void blocked_unit_lower_inverse(const float *AS, float *TF, uint8_t *TT,
+// then T_ij = -T_ii sum_{m=j}^{i-1} A_im T_mj along the sub-diagonals, each
+// block product by 64 threads holding 1 x 4 strips.  Leaves T (float, lower
+// blocks only) in TF and T (bf16, zeros above the diagonal) as a K-major
+// [C][C] tile in TT.  Called by all 256 threads; XS (3 x 256 floats) is
+// scratch inside TT.
+__device__ __forceinline__ void blocked_unit_lower_inverse(float *AS, float *TF, uint8_t *TT,
                                                            int tid) {
   float *XS = reinterpret_cast<float *>(TT);
   if (tid < kC) {
     const int b = tid >> 4, j = tid & 15, o = b * 16;
     float t[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) t[i] = 0.f;
-#pragma unroll
     for (int i = 0; i < 16; ++i) {
       float acc = 0.f;
 #pragma unroll
-      for (int m = 0; m < i; ++m) acc += AS[as_idx(o + i, o + m)] * t[m];
-      t[i] = (i == j) ? 1.f : -acc;
+      for (int m = 0; m < i; ++m) acc += AS[sw8(o + i, o + m)] * t[m];
+      t[i] = (i == j) ? 1.f : ((i < j) ? 0.f : -acc);
     }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) TF[(o + i) * kC + o + j] = t[i];
+    for (int i = 0; i < 16; ++i) TF[sw8(o + i, o + j)] = t[i];
   }
   __syncthreads();
 #pragma unroll
   for (int d = 1; d < 4; ++d) {
     const int np = 4 - d;
-    for (int w = tid; w < np * 256; w += 256) {  // X_p = sum_m A_{p+d, m} T_{m, p}
-      const int pp = w >> 8, e = w & 255, r = e >> 4, c = e & 15;
-      const int bi = pp + d, bj = pp;
-      float acc = 0.f;
-      for (int bm = bj; bm < bi; ++bm)
+    const int pp = tid >> 6, e = tid & 63, r = e >> 2, c0 = (e & 3) * 4;
+    const int bi = pp + d, bj = pp;
+    if (tid < np * 64) {  // X_p = sum_m A_{p+d, m} T_{m, p}
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int bm = bj; bm < bi; ++bm) {
 #pragma unroll
         for (int s2 = 0; s2 < 16; ++s2)
-          acc += AS[as_idx(bi * 16 + r, bm * 16 + s2)] * TF[(bm * 16 + s2) * kC + bj * 16 + c];
-      XS[w] = acc;
+          fma4(acc, AS[sw8(bi * 16 + r, bm * 16 + s2)], at4(TF, bm * 16 + s2, bj * 16 + c0));
+      }
+      *reinterpret_cast<float4 *>(XS + pp * 256 + r * 16 + c0) = acc;
     }
     __syncthreads();
-    for (int w = tid; w < np * 256; w += 256) {  // T_{p+d, p} = -T_{p+d, p+d} X_p
-      const int pp = w >> 8, e = w & 255, r = e >> 4, c = e & 15;
-      const int bi = pp + d, bj = pp;
-      float acc = 0.f;
+    if (tid < np * 64) {  // T_{p+d, p} = -T_{p+d, p+d} X_p
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int s2 = 0; s2 < 16; ++s2)
-        acc += TF[(bi * 16 + r) * kC + bi * 16 + s2] * XS[pp * 256 + s2 * 16 + c];
-      TF[(bi * 16 + r) * kC + bj * 16 + c] = -acc;
+        fma4(acc, TF[sw8(bi * 16 + r, bi * 16 + s2)],
+             *reinterpret_cast<const float4 *>(XS + pp * 256 + s2 * 16 + c0));
+      at4(TF, bi * 16 + r, bj * 16 + c0) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
     }
     __syncthreads();
   }
   for (int u = tid; u < kC * 8; u += 256) {  // bf16 operand tile, zeros above the diagonal blocks
     const int row = u >> 3, c8 = u & 7;
     float x[8];
-    const bool lower = (row >> 4) >= (c8 >> 1);
+    if ((row >> 4) >= (c8 >> 1)) {
+      const float4 a = at4(TF, row, c8 * 8), b = at4(TF, row, c8 * 8 + 4);
+      x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+      x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    } else {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] = lower ? TF[row * kC + c8 * 8 + e] : 0.f;
+      for (int e2 = 0; e2 < 8; ++e2) x[e2] = 0.f;
+    }
     st_chunk(TT, row, c8, kC, x);
   }
 }
@@ -247,32 +259,39 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
   if (tid == 0 && (int)blockIdx.x < total) issue_raw(blockIdx.x);
   uint32_t mma_phase = 0;
 
+  // Decay inputs (log_alpha, beta) of one chunk for this thread's rows; loaded
+  // one chunk ahead, unconditionally (clamped rows), so the loads overlap.
+  float la_n[R], bt_n[R];
+  auto load_decay = [&](int idx) {
+    const int t0n = (idx % NC) * kC;
+    const int validn = min(kC, T - t0n);
+    const size_t row0n = (size_t)(idx / NC) * T + t0n;
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      const int rr = min(r0 + i, validn - 1);
+      bt_n[i] = beta[row0n + rr];
+      la_n[i] = 0.f;
+      if (alpha_mode == KDA_ALPHA_CHANNEL)
+        la_n[i] = log_alpha[(row0n + rr) * D + c];
+      else if (alpha_mode == KDA_ALPHA_SCALAR)
+        la_n[i] = log_alpha[row0n + rr];
+    }
+  };
+  if ((int)blockIdx.x < total) load_decay(blockIdx.x);
+
   for (int idx = blockIdx.x, it = 0; idx < total; idx += gridDim.x, ++it) {
     const int bh = idx / NC, n = idx % NC;
     const int t0 = n * kC;
     const int valid = min(kC, T - t0);
     const size_t row0 = (size_t)bh * T + t0;
 
-    // ---- (1) decay inputs (all in flight at once), then the raw rows
+    // ---- (1) decay inputs (loaded during the previous chunk), then the raw rows
     float ld[R], bt[R];
-    {
-      float la[R];
 #pragma unroll
-      for (int i = 0; i < R; ++i) {
-        const int rr = min(r0 + i, valid - 1);
-        bt[i] = beta[row0 + rr];
-        la[i] = 0.f;
-        if (alpha_mode == KDA_ALPHA_CHANNEL)
-          la[i] = log_alpha[(row0 + rr) * D + c];
-        else if (alpha_mode == KDA_ALPHA_SCALAR)
-          la[i] = log_alpha[row0 + rr];
-      }
-#pragma unroll
-      for (int i = 0; i < R; ++i) {
-        const bool live = r0 + i < valid;
-        ld[i] = (live && alpha_mode != KDA_ALPHA_NONE) ? -__expf(la[i]) : 0.f;
-        bt[i] = live ? bt[i] : 0.f;
-      }
+    for (int i = 0; i < R; ++i) {
+      const bool live = r0 + i < valid;
+      ld[i] = (live && alpha_mode != KDA_ALPHA_NONE) ? -__expf(la_n[i]) : 0.f;
+      bt[i] = live ? bt_n[i] : 0.f;
     }
     float psum = 0.f;
 #pragma unroll
@@ -327,7 +346,10 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    if (tid == 0 && idx + (int)gridDim.x < total) issue_raw(idx + gridDim.x);  // prefetch
+    if (idx + (int)gridDim.x < total) {  // prefetch the next chunk
+      if (tid == 0) issue_raw(idx + gridDim.x);
+      load_decay(idx + gridDim.x);
+    }
 
     // ---- (2) [A_full; M_full] = [K_beta; Q*gamma] (K/gamma)^T  -> TMEM cols [0, 64)
     if (tid == 0) {
@@ -363,7 +385,7 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
             a.y = (m0 + 1 < r) ? x[4 * j4 + 1] : 0.f;
             a.z = (m0 + 2 < r) ? x[4 * j4 + 2] : 0.f;
             a.w = (m0 + 3 < r) ? x[4 * j4 + 3] : 0.f;
-            *reinterpret_cast<float4 *>(AS + as_idx(r, m0)) = a;
+            at4(AS, r, m0) = a;
           }
         } else {
           const int r = lane_row - kC;
