@@ -34,6 +34,8 @@
 //    the serial path.
 // A partial last chunk is padded with k = q = v = 0, beta = 0, a = 1, which
 // adds nothing; padded rows of o are not stored.
+#include <type_traits>
+
 #include "kda_launch.cuh"
 #include "kda_ptx.cuh"
 #include "kda_umma.cuh"
@@ -58,6 +60,7 @@ struct Blob {
 };
 
 __host__ __device__ constexpr uint32_t align1k(uint32_t x) { return (x + 1023u) & ~1023u; }
+constexpr int kLD = kC + 4;  // row stride (floats) of the float A and T tiles of the solve
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
@@ -97,95 +100,129 @@ struct PrepSmem {
   static constexpr uint32_t BLOB = 0;
   static constexpr uint32_t X1 = align1k(B::BYTES);        // [K_beta; Q*gamma] [128 rows][D]
   static constexpr uint32_t TT = X1 + 128 * D * 2;         // T bf16 [C rows][C]; solve scratch before
-  static constexpr uint32_t WT = TT + kC * kC * 2;         // W^T [D rows][C]
-  static constexpr uint32_t AS = WT + D * kC * 2;          // A float [C][C], chunk-swizzled rows
+  static constexpr uint32_t TF = TT + kC * kC * 2;         // T float [C][kLD] during the solve
+  static constexpr uint32_t WT = TF;                       // W^T [D rows][C] afterwards
+  static constexpr uint32_t AS = align1k(TF + kC * kLD * 4);  // A float [C][kLD]
   // D = 128 reuses the Ap and Qp slots of the record for X2 and Khat (both dead
   // before Ap and Qp are written); D = 64 gives them their own space.
-  static constexpr uint32_t X2 = (D == 128) ? B::AP : AS + kC * kC * 4;     // [K_beta^T; (beta V)^T] [2D rows][C]
+  static constexpr uint32_t X2 = (D == 128) ? B::AP : AS + kC * kLD * 4;    // [K_beta^T; (beta V)^T] [2D rows][C]
   static constexpr uint32_t KH = (D == 128) ? B::QP : X2 + 2 * D * kC * 2;  // K/gamma  [C rows][D]
   // D = 128: [I | -M], the B operand of Qp^T = [(Q*gamma)^T | W^T] [I | -M]^T, in the
   // Qp slot between Khat's last use and Qp^T's write.
   static constexpr uint32_t IM = B::QP;
-  // T as float during the blocked solve: in the W^T tile (D = 128) or its own space.
-  static constexpr uint32_t TF = (D == 128) ? WT : KH + kC * D * 2;
-  static constexpr uint32_t RAW = (D == 128) ? AS + kC * kC * 4 : TF + kC * kC * 4;  // q | k | v [C][D] bf16
-  static constexpr uint32_t PART = RAW + 3 * kC * D * 2;   // float [4][D] partial decay sums
+  static constexpr uint32_t RAW = (D == 128) ? AS + kC * kLD * 4 : KH + kC * D * 2;  // q | k | v [C][D] bf16
+  static constexpr uint32_t BETA = RAW + 3 * kC * D * 2;   // float [C]
+  static constexpr uint32_t PART = BETA + kC * 4;          // float [4][D] partial decay sums
   static constexpr uint32_t BAR = PART + 4 * D * 4;        // mbarrier (MMA commits)
   static constexpr uint32_t LBAR = BAR + 8;                // mbarrier (raw loads)
   static constexpr uint32_t TMEMP = LBAR + 8;              // TMEM base address
   static constexpr uint32_t BYTES = TMEMP + 8;
   static constexpr uint32_t TMEM_COLS = (D == 128) ? 256 : 128;
-  static_assert(D != 128 || D * kC * 2 >= kC * kC * 4, "T float must fit the W^T tile");
+  static_assert(kC * kLD * 4 >= D * kC * 2, "W^T must fit the float T region");
+  static_assert((X2 & 1023u) == 0 && (KH & 1023u) == 0 && (AS & 1023u) == 0 && (TF & 1023u) == 0,
+                "operand tiles need 1024-byte alignment");
   static_assert(BYTES + 1024 <= 232448, "prep shared memory");
 };
 
-// Float [C][C] matrices (A, T) in shared memory: row r, 4-float chunk j of
-// the row stored at chunk j ^ (r % 8), so column reads across 8 rows and
-// 16-byte row writes are both free of bank conflicts.
-__device__ __forceinline__ int sw8(int r, int c) {
-  return r * kC + ((((c >> 2) ^ (r & 7)) << 2) | (c & 3));
-}
-__device__ __forceinline__ float4 &at4(float *M, int r, int c0) {
-  return *reinterpret_cast<float4 *>(M + r * kC + (((c0 >> 2) ^ (r & 7)) << 2));
-}
 __device__ __forceinline__ void fma4(float4 &acc, float a, const float4 &b) {
   acc.x += a * b.x; acc.y += a * b.y; acc.z += a * b.z; acc.w += a * b.w;
 }
 
-// T = (I + A)^-1 for the strictly lower A in AS (float), by blocks of 16:
-// the four diagonal blocks by forward substitution (one column per thread),
-// then T_ij = -T_ii sum_{m=j}^{i-1} A_im T_mj along the sub-diagonals, each
-// block product by 64 threads holding 1 x 4 strips.  Leaves T (float, lower
-// blocks only) in TF and T (bf16, zeros above the diagonal) as a K-major
-// [C][C] tile in TT.  Called by all 256 threads; XS (3 x 256 floats) is
-// scratch inside TT.
-__device__ __forceinline__ void blocked_unit_lower_inverse(float *AS, float *TF, uint8_t *TT,
+// T = (I + A)^-1 for the strictly lower A (float, row stride kLD), in blocks
+// of 16.  The diagonal blocks by right-looking forward substitution (one
+// column per thread, partial sums in registers); then, right-looking over the
+// block columns, S_ij accumulates A_im T_mj as soon as T_mj exists and
+// T_ij = -T_ii S_ij, every block product done by 64 threads on 1 x 4 strips.
+// The float row stride kLD = C + 4 keeps column reads across rows and 16-byte
+// row accesses free of bank conflicts, and lets every inner-loop address be an
+// immediate offset.  Leaves T (float, lower blocks) in TF and the bf16 K-major
+// [C][C] tile of T (zeros above the diagonal) in TT.  All 256 threads call
+// it; XS (6 x 256 floats) is scratch inside TT.
+__device__ __forceinline__ void blocked_unit_lower_inverse(const float *AF, float *TF, uint8_t *TT,
                                                            int tid) {
   float *XS = reinterpret_cast<float *>(TT);
   if (tid < kC) {
     const int b = tid >> 4, j = tid & 15, o = b * 16;
-    float t[16];
+    const float *Ab = AF + o * kLD + o;
+    float t[16], p[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float acc = 0.f;
+    for (int i = 0; i < 16; ++i) p[i] = 0.f;
 #pragma unroll
-      for (int m = 0; m < i; ++m) acc += AS[sw8(o + i, o + m)] * t[m];
-      t[i] = (i == j) ? 1.f : ((i < j) ? 0.f : -acc);
+    for (int kk = 0; kk < 16; ++kk) {
+      t[kk] = (kk == j) ? 1.f : ((kk < j) ? 0.f : -p[kk]);
+#pragma unroll
+      for (int i = kk + 1; i < 16; ++i) p[i] += Ab[i * kLD + kk] * t[kk];
     }
+    float *Tb = TF + o * kLD + o + j;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) TF[sw8(o + i, o + j)] = t[i];
+    for (int i = 0; i < 16; ++i) Tb[i * kLD] = t[i];
   }
   __syncthreads();
+  const int r = (tid & 63) >> 2, c0 = (tid & 3) * 4, g = tid >> 6;
+  // out (+)= L (16 x 16, rows li.., cols lj..) * R (16 x 16 at rows ri.., cols rj..)
+  auto strip = [&](const float *Lm, int li, int lj, const float *Rm, int ri, int rj) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float *lrow = Lm + (li + r) * kLD + lj;
+    const float *rcol = Rm + ri * kLD + rj + c0;
 #pragma unroll
-  for (int d = 1; d < 4; ++d) {
-    const int np = 4 - d;
-    const int pp = tid >> 6, e = tid & 63, r = e >> 2, c0 = (e & 3) * 4;
-    const int bi = pp + d, bj = pp;
-    if (tid < np * 64) {  // X_p = sum_m A_{p+d, m} T_{m, p}
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int bm = bj; bm < bi; ++bm) {
+    for (int s2 = 0; s2 < 16; ++s2)
+      fma4(acc, lrow[s2], *reinterpret_cast<const float4 *>(rcol + s2 * kLD));
+    return acc;
+  };
+  auto xs = [&](int slot) -> float4 & { return *reinterpret_cast<float4 *>(XS + slot * 256 + r * 16 + c0); };
+  auto tf = [&](int bi, int bj) -> float4 & {
+    return *reinterpret_cast<float4 *>(TF + (bi * 16 + r) * kLD + bj * 16 + c0);
+  };
+  auto neg_tii_x = [&](int bi, int bj, int slot) {  // T_ij = -T_ii S_ij
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float *trow = TF + (bi * 16 + r) * kLD + bi * 16;
+    const float *xcol = XS + slot * 256 + c0;
 #pragma unroll
-        for (int s2 = 0; s2 < 16; ++s2)
-          fma4(acc, AS[sw8(bi * 16 + r, bm * 16 + s2)], at4(TF, bm * 16 + s2, bj * 16 + c0));
-      }
-      *reinterpret_cast<float4 *>(XS + pp * 256 + r * 16 + c0) = acc;
-    }
-    __syncthreads();
-    if (tid < np * 64) {  // T_{p+d, p} = -T_{p+d, p+d} X_p
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s2 = 0; s2 < 16; ++s2) fma4(acc, trow[s2], *reinterpret_cast<const float4 *>(xcol + s2 * 16));
+    tf(bi, bj) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+  };
+  // S_ij = A_ij T_jj for the six blocks below the diagonal (slots 0..5:
+  // (1,0) (2,1) (3,2) (2,0) (3,1) (3,0))
+  for (int w = tid; w < 6 * 64; w += 256) {
+    const int sl = w >> 6;
+    const int bi = sl < 3 ? sl + 1 : (sl == 5 ? 3 : sl - 1);
+    const int bj = sl < 3 ? sl : (sl == 5 ? 0 : sl - 3);
+    const int rr = (w & 63) >> 2, cc = (w & 3) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float *lrow = AF + (bi * 16 + rr) * kLD + bj * 16;
+    const float *rcol = TF + (bj * 16) * kLD + bj * 16 + cc;
 #pragma unroll
-      for (int s2 = 0; s2 < 16; ++s2)
-        fma4(acc, TF[sw8(bi * 16 + r, bi * 16 + s2)],
-             *reinterpret_cast<const float4 *>(XS + pp * 256 + s2 * 16 + c0));
-      at4(TF, bi * 16 + r, bj * 16 + c0) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-    }
-    __syncthreads();
+    for (int s2 = 0; s2 < 16; ++s2)
+      fma4(acc, lrow[s2], *reinterpret_cast<const float4 *>(rcol + s2 * kLD));
+    *reinterpret_cast<float4 *>(XS + sl * 256 + rr * 16 + cc) = acc;
   }
+  __syncthreads();
+  if (g < 3) neg_tii_x(g + 1, g, g);                 // T_10, T_21, T_32
+  __syncthreads();
+  if (g < 3) {                                        // S_20 += A_21 T_10; S_31 += A_32 T_21; S_30 += A_31 T_10
+    const int sl = 3 + g;
+    const int bi = g == 0 ? 2 : 3, bm = g == 0 ? 1 : (g == 1 ? 2 : 1), bj = g == 1 ? 1 : 0;
+    const float4 a = strip(AF, bi * 16, bm * 16, TF, bm * 16, bj * 16);
+    float4 &x = xs(sl);
+    x.x += a.x; x.y += a.y; x.z += a.z; x.w += a.w;
+  }
+  __syncthreads();
+  if (g < 2) neg_tii_x(g + 2, g, 3 + g);             // T_20, T_31
+  __syncthreads();
+  if (g == 0) {                                       // S_30 += A_32 T_20
+    const float4 a = strip(AF, 48, 32, TF, 32, 0);
+    float4 &x = xs(5);
+    x.x += a.x; x.y += a.y; x.z += a.z; x.w += a.w;
+  }
+  __syncthreads();
+  if (g == 0) neg_tii_x(3, 0, 5);                    // T_30
+  __syncthreads();
   for (int u = tid; u < kC * 8; u += 256) {  // bf16 operand tile, zeros above the diagonal blocks
     const int row = u >> 3, c8 = u & 7;
     float x[8];
     if ((row >> 4) >= (c8 >> 1)) {
-      const float4 a = at4(TF, row, c8 * 8), b = at4(TF, row, c8 * 8 + 4);
+      const float4 a = *reinterpret_cast<const float4 *>(TF + row * kLD + c8 * 8);
+      const float4 b = *reinterpret_cast<const float4 *>(TF + row * kLD + c8 * 8 + 4);
       x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
       x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
     } else {
@@ -259,25 +296,32 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
   if (tid == 0 && (int)blockIdx.x < total) issue_raw(blockIdx.x);
   uint32_t mma_phase = 0;
 
-  // Decay inputs (log_alpha, beta) of one chunk for this thread's rows; loaded
-  // one chunk ahead, unconditionally (clamped rows), so the loads overlap.
-  float la_n[R], bt_n[R];
-  auto load_decay = [&](int idx) {
-    const int t0n = (idx % NC) * kC;
+  // Decay inputs of the next chunk, prefetched in three batches hidden under the
+  // three MMA waits of the current chunk (few loads in flight at a time):
+  // log_alpha for this thread's key channel and rows, beta of row `tid`.
+  float la_n[R], b_n = 0.f;
+  auto load_la = [&](int idxn, auto I0, auto I1) {
+    constexpr int i0 = decltype(I0)::value, i1 = decltype(I1)::value;
+    const int t0n = (idxn % NC) * kC;
     const int validn = min(kC, T - t0n);
-    const size_t row0n = (size_t)(idx / NC) * T + t0n;
+    const size_t row0n = (size_t)(idxn / NC) * T + t0n;
 #pragma unroll
-    for (int i = 0; i < R; ++i) {
+    for (int i = i0; i < i1; ++i) {
       const int rr = min(r0 + i, validn - 1);
-      bt_n[i] = beta[row0n + rr];
       la_n[i] = 0.f;
       if (alpha_mode == KDA_ALPHA_CHANNEL)
         la_n[i] = log_alpha[(row0n + rr) * D + c];
       else if (alpha_mode == KDA_ALPHA_SCALAR)
         la_n[i] = log_alpha[row0n + rr];
     }
+    if (i0 == 0 && tid < kC) b_n = beta[row0n + min(tid, validn - 1)];
   };
-  if ((int)blockIdx.x < total) load_decay(blockIdx.x);
+  using I_0 = std::integral_constant<int, 0>;
+  using I_1 = std::integral_constant<int, R / 3>;
+  using I_2 = std::integral_constant<int, 2 * R / 3>;
+  using I_3 = std::integral_constant<int, R>;
+  if ((int)blockIdx.x < total) load_la(blockIdx.x, I_0{}, I_3{});
+  float *betas = reinterpret_cast<float *>(sm + L::BETA);
 
   for (int idx = blockIdx.x, it = 0; idx < total; idx += gridDim.x, ++it) {
     const int bh = idx / NC, n = idx % NC;
@@ -286,13 +330,11 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
     const size_t row0 = (size_t)bh * T + t0;
 
     // ---- (1) decay inputs (loaded during the previous chunk), then the raw rows
-    float ld[R], bt[R];
+    float ld[R];
 #pragma unroll
-    for (int i = 0; i < R; ++i) {
-      const bool live = r0 + i < valid;
-      ld[i] = (live && alpha_mode != KDA_ALPHA_NONE) ? -__expf(la_n[i]) : 0.f;
-      bt[i] = live ? bt_n[i] : 0.f;
-    }
+    for (int i = 0; i < R; ++i)
+      ld[i] = (r0 + i < valid && alpha_mode != KDA_ALPHA_NONE) ? -__expf(la_n[i]) : 0.f;
+    if (tid < kC) betas[tid] = (tid < valid) ? b_n : 0.f;
     float psum = 0.f;
 #pragma unroll
     for (int i = 0; i < R; ++i) psum += ld[i];
@@ -326,13 +368,14 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
         const float vv = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(rawv)[r * D + c]);
         g += ld[i];
         const float eg = __expf(g), eng = __expf(-g);
-        const float kb = bt[i] * kv * eg;
+        const float bti = betas[r];
+        const float kb = bti * kv * eg;
         st_bf16(X1, umma::sw128_off(r, c, 128), kb);               // K_beta
         st_bf16(X1, umma::sw128_off(kC + r, c, 128), qv * eg);     // Q * gamma
         st_bf16(KH, umma::sw128_off(r, c, kC), kv * eng);          // K / gamma
         kbT[i & 7] = kb;
         kbarT[i & 7] = kv * eng * egC;
-        vbT[i & 7] = bt[i] * vv;
+        vbT[i & 7] = bti * vv;
         if ((i & 7) == 7) {
           const int c8 = (r0 + i) >> 3;
           st_chunk(X2, c, c8, 2 * D, kbT);                          // K_beta^T
@@ -346,10 +389,9 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    if (idx + (int)gridDim.x < total) {  // prefetch the next chunk
-      if (tid == 0) issue_raw(idx + gridDim.x);
-      load_decay(idx + gridDim.x);
-    }
+    const int idx_next = idx + (int)gridDim.x;
+    const bool has_next = idx_next < total;
+    if (has_next && tid == 0) issue_raw(idx_next);  // prefetch the next chunk's q, k, v rows
 
     // ---- (2) [A_full; M_full] = [K_beta; Q*gamma] (K/gamma)^T  -> TMEM cols [0, 64)
     if (tid == 0) {
@@ -359,6 +401,7 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
                          umma::idesc_bf16(128, kC), ks > 0);
       ptx::mma_commit(bar);
     }
+    if (has_next) load_la(idx_next, I_0{}, I_1{});
     if (ok && !ptx::mbar_wait(bar, mma_phase & 1, kWaitLimit)) {
       ok = false;
       report_error(hdr, KDA_ERR_TIMEOUT, 0x101u);
@@ -385,7 +428,7 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
             a.y = (m0 + 1 < r) ? x[4 * j4 + 1] : 0.f;
             a.z = (m0 + 2 < r) ? x[4 * j4 + 2] : 0.f;
             a.w = (m0 + 3 < r) ? x[4 * j4 + 3] : 0.f;
-            at4(AS, r, m0) = a;
+            *reinterpret_cast<float4 *>(AS + r * kLD + m0) = a;
           }
         } else {
           const int r = lane_row - kC;
@@ -426,6 +469,7 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
                            umma::sdesc_k(sTT, kC, ks), umma::idesc_bf16(128, kC), ks > 0);
       ptx::mma_commit(bar);
     }
+    if (has_next) load_la(idx_next, I_1{}, I_2{});
     if (ok && !ptx::mbar_wait(bar, mma_phase & 1, kWaitLimit)) {
       ok = false;
       report_error(hdr, KDA_ERR_TIMEOUT, 0x102u);
@@ -486,6 +530,7 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
       }
       ptx::mma_commit(bar);
     }
+    if (has_next) load_la(idx_next, I_2{}, I_3{});
     if (ok && !ptx::mbar_wait(bar, mma_phase & 1, kWaitLimit)) {
       ok = false;
       report_error(hdr, KDA_ERR_TIMEOUT, 0x103u);
