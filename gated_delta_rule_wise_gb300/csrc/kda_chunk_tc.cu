@@ -46,17 +46,38 @@ namespace {
 constexpr int kC = 64;                 // chunk length on this path
 constexpr uint32_t kWaitLimit = 1u << 24;  // polls before a wait gives up (~1 s)
 
-// Per-chunk intermediate record in the workspace (and its shared-memory image).
+// Per-chunk intermediate record in the workspace, one per (head, chunk).
 template <int D>
-struct Blob {
-  static constexpr uint32_t AP = 0;                     // Ap    [D rows][D]    K-major SW128
-  static constexpr uint32_t QP = AP + D * D * 2;        // Qp^T [D rows][C] (D = 128), Qp [C rows][D] (D = 64)
-  static constexpr uint32_t KBT = QP + kC * D * 2;      // Kbar^T[D rows][C]
-  static constexpr uint32_t MM = KBT + D * kC * 2;      // M     [C rows][C]
-  static constexpr uint32_t UT = MM + kC * kC * 2;      // U^T   [D rows][C]
-  static constexpr uint32_t GC = UT + D * kC * 2;       // gamma_C [D] float
-  static constexpr uint32_t BYTES = GC + D * 4;
-  static constexpr uint32_t PRE = UT;                   // Ap | Qp | Kbar^T | M
+struct Rec;
+// D = 64: every operand the scan multiplies, as swizzled K-major bf16 tiles
+// (Ap and Qp, and Kbar^T and M, are adjacent 64-row tiles: one 128-row
+// operand each), then gamma_C.
+template <>
+struct Rec<64> {
+  static constexpr uint32_t AP = 0;        // Ap     [64 rows][64]
+  static constexpr uint32_t QP = 8192;     // Qp     [C rows][64]
+  static constexpr uint32_t KBT = 16384;   // Kbar^T [64 rows][C]
+  static constexpr uint32_t MM = 24576;    // M      [C rows][C]
+  static constexpr uint32_t UT = 32768;    // U^T    [64 rows][C]
+  static constexpr uint32_t GC = 40960;    // gamma_C [64] float
+  static constexpr uint32_t BYTES = 41216;
+  static constexpr uint32_t PRE = UT;      // Ap | Qp | Kbar^T | M
+};
+// D = 128: the two operands of the state products as swizzled tiles (Ap
+// K-major, Qp^T read MN-major), then the chunk's additive terms already
+// multiplied out: B = Kbar^T U [128 keys][128 values] and O = M U
+// [C tokens][128 values], plain row-major bf16 stored as four 32-column
+// blocks each (a scan CTA owns one block), then gamma_C.
+template <>
+struct Rec<128> {
+  static constexpr uint32_t AP = 0;        // Ap    [128 rows][128]
+  static constexpr uint32_t QP = 32768;    // Qp^T  [128 rows][C]
+  static constexpr uint32_t BI = 49152;    // B     [4][128][32] bf16
+  static constexpr uint32_t OI = 81920;    // O     [4][C][32] bf16
+  static constexpr uint32_t GC = 98304;    // gamma_C [128] float
+  static constexpr uint32_t BYTES = 98816;
+  static constexpr uint32_t PRE = BI;      // Ap | Qp^T
+  static constexpr int BLK = 32;           // value columns per block of B and O
 };
 
 __host__ __device__ constexpr uint32_t align1k(uint32_t x) { return (x + 1023u) & ~1023u; }
@@ -68,9 +89,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 __device__ __forceinline__ void st_bf16(uint8_t *base, uint32_t off, float x) {
   *reinterpret_cast<__nv_bfloat16 *>(base + off) = __float2bfloat16_rn(x);
-}
-__device__ __forceinline__ float ld_bf16(const uint8_t *base, uint32_t off) {
-  return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(base + off));
 }
 // 8 consecutive K values of one row -> one 16-byte chunk.
 __device__ __forceinline__ void st_chunk(uint8_t *tile, int row, int c8, int rows, const float *v) {
@@ -96,20 +114,29 @@ __device__ __forceinline__ void ld_chunk(const uint8_t *tile, int row, int c8, i
 
 template <int D>
 struct PrepSmem {
-  using B = Blob<D>;
-  static constexpr uint32_t BLOB = 0;
-  static constexpr uint32_t X1 = align1k(B::BYTES);        // [K_beta; Q*gamma] [128 rows][D]
+  using R = Rec<D>;
+  // Staging of the stored record (D = 64: the whole record; D = 128: Ap | Qp^T
+  // | gamma_C), and the operand tiles Kbar^T, M, U^T (inside the record for
+  // D = 64, separate for D = 128).
+  static constexpr uint32_t AP_S = 0;
+  static constexpr uint32_t QP_S = R::QP;
+  static constexpr uint32_t GC_S = (D == 128) ? R::PRE : R::GC;
+  static constexpr uint32_t KBT_S = (D == 128) ? align1k(R::PRE + D * 4) : Rec<64>::KBT;
+  static constexpr uint32_t MM_S = (D == 128) ? KBT_S + D * kC * 2 : Rec<64>::MM;
+  static constexpr uint32_t UT_S = (D == 128) ? MM_S + kC * kC * 2 : Rec<64>::UT;
+  static constexpr uint32_t STG_END = (D == 128) ? UT_S + D * kC * 2 : Rec<64>::BYTES;
+  static constexpr uint32_t X1 = align1k(STG_END);         // [K_beta; Q*gamma] [128 rows][D]
   static constexpr uint32_t TT = X1 + 128 * D * 2;         // T bf16 [C rows][C]; solve scratch before
   static constexpr uint32_t TF = TT + kC * kC * 2;         // T float [C][kLD] during the solve
   static constexpr uint32_t WT = TF;                       // W^T [D rows][C] afterwards
   static constexpr uint32_t AS = align1k(TF + kC * kLD * 4);  // A float [C][kLD]
-  // D = 128 reuses the Ap and Qp slots of the record for X2 and Khat (both dead
-  // before Ap and Qp are written); D = 64 gives them their own space.
-  static constexpr uint32_t X2 = (D == 128) ? B::AP : AS + kC * kLD * 4;    // [K_beta^T; (beta V)^T] [2D rows][C]
-  static constexpr uint32_t KH = (D == 128) ? B::QP : X2 + 2 * D * kC * 2;  // K/gamma  [C rows][D]
+  // D = 128 keeps X2 and Khat in the Ap and Qp staging slots (both dead before
+  // Ap and Qp^T are written); D = 64 gives them their own space.
+  static constexpr uint32_t X2 = (D == 128) ? AP_S : AS + kC * kLD * 4;    // [K_beta^T; (beta V)^T] [2D rows][C]
+  static constexpr uint32_t KH = (D == 128) ? QP_S : X2 + 2 * D * kC * 2;  // K/gamma  [C rows][D]
   // D = 128: [I | -M], the B operand of Qp^T = [(Q*gamma)^T | W^T] [I | -M]^T, in the
   // Qp slot between Khat's last use and Qp^T's write.
-  static constexpr uint32_t IM = B::QP;
+  static constexpr uint32_t IM = QP_S;
   static constexpr uint32_t RAW = (D == 128) ? AS + kC * kLD * 4 : KH + kC * D * 2;  // q | k | v [C][D] bf16
   static constexpr uint32_t BETA = RAW + 3 * kC * D * 2;   // float [C]
   static constexpr uint32_t PART = BETA + kC * 4;          // float [4][D] partial decay sums
@@ -117,9 +144,10 @@ struct PrepSmem {
   static constexpr uint32_t LBAR = BAR + 8;                // mbarrier (raw loads)
   static constexpr uint32_t TMEMP = LBAR + 8;              // TMEM base address
   static constexpr uint32_t BYTES = TMEMP + 8;
-  static constexpr uint32_t TMEM_COLS = (D == 128) ? 256 : 128;
+  static constexpr uint32_t TMEM_COLS = (D == 128) ? 512 : 128;
   static_assert(kC * kLD * 4 >= D * kC * 2, "W^T must fit the float T region");
-  static_assert((X2 & 1023u) == 0 && (KH & 1023u) == 0 && (AS & 1023u) == 0 && (TF & 1023u) == 0,
+  static_assert((X2 & 1023u) == 0 && (KH & 1023u) == 0 && (AS & 1023u) == 0 && (TF & 1023u) == 0 &&
+                    (KBT_S & 1023u) == 0 && (MM_S & 1023u) == 0 && (UT_S & 1023u) == 0,
                 "operand tiles need 1024-byte alignment");
   static_assert(BYTES + 1024 <= 232448, "prep shared memory");
 };
@@ -239,14 +267,14 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
                 const __nv_bfloat16 *__restrict__ v, const float *__restrict__ beta,
                 const float *__restrict__ log_alpha, int alpha_mode, int T, int NC, int total,
                 uint8_t *__restrict__ ws) {
-  using B = Blob<D>;
+  using Rr = Rec<D>;
   using L = PrepSmem<D>;
   constexpr int Q4 = 256 / D;          // threads per key channel
   constexpr int R = kC / Q4;           // rows per thread in the elementwise phase
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));
-  uint8_t *blob = sm + L::BLOB;
+  uint8_t *stg = sm;  // staging of the stored record
   uint8_t *X1 = sm + L::X1;
   uint8_t *TT = sm + L::TT;
   uint8_t *WT = sm + L::WT;
@@ -292,7 +320,8 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
   const uint32_t tmem = *tmem_ptr;
   const uint32_t sX1 = ptx::smem_u32(X1), sKH = ptx::smem_u32(KH), sX2 = ptx::smem_u32(X2);
   const uint32_t sTT = ptx::smem_u32(TT), sWT = ptx::smem_u32(WT), sIM = ptx::smem_u32(IM);
-  const uint32_t sKBT = ptx::smem_u32(blob + B::KBT);
+  const uint32_t sKBT = ptx::smem_u32(sm + L::KBT_S);
+  const uint32_t sMMs = ptx::smem_u32(sm + L::MM_S), sUTs = ptx::smem_u32(sm + L::UT_S);
   if (tid == 0 && (int)blockIdx.x < total) issue_raw(blockIdx.x);
   uint32_t mma_phase = 0;
 
@@ -380,10 +409,10 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
           const int c8 = (r0 + i) >> 3;
           st_chunk(X2, c, c8, 2 * D, kbT);                          // K_beta^T
           st_chunk(X2, D + c, c8, 2 * D, vbT);                      // (beta V)^T
-          st_chunk(blob + B::KBT, c, c8, D, kbarT);                 // Kbar^T (output)
+          st_chunk(sm + L::KBT_S, c, c8, D, kbarT);                 // Kbar^T (output)
         }
       }
-      if (qtr == 0) reinterpret_cast<float *>(blob + B::GC)[c] = egC;
+      if (qtr == 0) reinterpret_cast<float *>(stg + L::GC_S)[c] = egC;
     }
     ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
@@ -435,8 +464,8 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
           float mrow[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) mrow[j] = (cb + j <= r) ? x[j] : 0.f;
-          st_chunk(blob + B::MM, r, cb >> 3, kC, mrow);
-          st_chunk(blob + B::MM, r, (cb >> 3) + 1, kC, mrow + 8);
+          st_chunk(sm + L::MM_S, r, cb >> 3, kC, mrow);
+          st_chunk(sm + L::MM_S, r, (cb >> 3) + 1, kC, mrow + 8);
           if (D == 128) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) mrow[j] = -mrow[j];
@@ -492,7 +521,7 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
           const int lane_row = tid;
           const bool isW = (D == 128) ? (h == 0) : (lane_row < D);
           const int row = (D == 128) ? lane_row : (lane_row % D);
-          uint8_t *dst = isW ? WT : blob + B::UT;
+          uint8_t *dst = isW ? WT : sm + L::UT_S;
           st_chunk(dst, row, cb >> 3, D, x);
           st_chunk(dst, row, (cb >> 3) + 1, D, x + 8);
         }
@@ -521,6 +550,15 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
         for (int ks = 0; ks < kC / 16; ++ks)
           ptx::mma_bf16_ss(tmem + 128, umma::sdesc_k(sWT, D, ks),
                            umma::sdesc_k(sIM, kC, 4 + ks), umma::idesc_bf16(128, kC), 1);
+        // cols [256, 384): B = Kbar^T U;  cols [384, 512): O = M U (M = 64 layout)
+#pragma unroll
+        for (int ks = 0; ks < kC / 16; ++ks)
+          ptx::mma_bf16_ss(tmem + 256, umma::sdesc_k(sKBT, D, ks), umma::sdesc_k(sUTs, D, ks),
+                           umma::idesc_bf16(128, D), ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < kC / 16; ++ks)
+          ptx::mma_bf16_ss(tmem + 384, umma::sdesc_k(sMMs, kC, ks), umma::sdesc_k(sUTs, D, ks),
+                           umma::idesc_bf16(64, D), ks > 0);
       } else {
         // cols [0, 64): [Kbar^T; M] W  (Kbar^T and M are adjacent in the record)
 #pragma unroll
@@ -550,8 +588,8 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
           ptx::tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 16; ++j) x[j] = -x[j];
-          st_chunk(blob + B::AP, lane_row, cb >> 3, D, x);
-          st_chunk(blob + B::AP, lane_row, (cb >> 3) + 1, D, x + 8);
+          st_chunk(stg + L::AP_S, lane_row, cb >> 3, D, x);
+          st_chunk(stg + L::AP_S, lane_row, (cb >> 3) + 1, D, x + 8);
         }
         // Qp^T: lane = key channel, column = token
 #pragma unroll
@@ -559,8 +597,34 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
           float x[16];
           ptx::tmem_ld16(ta + 128 + cb, x);
           ptx::tmem_ld_wait();
-          st_chunk(blob + B::QP, lane_row, cb >> 3, D, x);
-          st_chunk(blob + B::QP, lane_row, (cb >> 3) + 1, D, x + 8);
+          st_chunk(stg + L::QP_S, lane_row, cb >> 3, D, x);
+          st_chunk(stg + L::QP_S, lane_row, (cb >> 3) + 1, D, x + 8);
+        }
+        // B and O straight to the record (plain row-major, 32-column blocks)
+        uint8_t *recg = ws + sizeof(WorkspaceHeader) + (size_t)idx * Rr::BYTES;
+        const int lane = tid & 31;
+        const int orow = warp * 16 + lane;  // M = 64 layout: lanes 32w + (0..15)
+#pragma unroll
+        for (int cb = 0; cb < D; cb += 16) {
+          float x[16], y[16];
+          ptx::tmem_ld16(ta + 256 + cb, x);
+          ptx::tmem_ld16(ta + 384 + cb, y);
+          ptx::tmem_ld_wait();
+          const uint32_t blk = (uint32_t)(cb >> 5), cin = (uint32_t)(cb & 31);
+          uint4 *db = reinterpret_cast<uint4 *>(recg + Rec<128>::BI + blk * (128u * 64u) +
+                                                (uint32_t)lane_row * 64u + cin * 2u);
+          db[0] = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]),
+                             pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
+          db[1] = make_uint4(pack_bf16x2(x[8], x[9]), pack_bf16x2(x[10], x[11]),
+                             pack_bf16x2(x[12], x[13]), pack_bf16x2(x[14], x[15]));
+          if (lane < 16) {
+            uint4 *dq = reinterpret_cast<uint4 *>(recg + Rec<128>::OI + blk * (uint32_t)(kC * 64) +
+                                                  (uint32_t)orow * 64u + cin * 2u);
+            dq[0] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
+                               pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
+            dq[1] = make_uint4(pack_bf16x2(y[8], y[9]), pack_bf16x2(y[10], y[11]),
+                               pack_bf16x2(y[12], y[13]), pack_bf16x2(y[14], y[15]));
+          }
         }
       } else {
 #pragma unroll
@@ -571,8 +635,8 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
           if (lane_row < D) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) x[j] = -x[j];
-            st_chunk(blob + B::AP, lane_row, cb >> 3, D, x);
-            st_chunk(blob + B::AP, lane_row, (cb >> 3) + 1, D, x + 8);
+            st_chunk(stg + L::AP_S, lane_row, cb >> 3, D, x);
+            st_chunk(stg + L::AP_S, lane_row, (cb >> 3) + 1, D, x + 8);
           } else {
             const int r = lane_row - D;
             float qg[16];
@@ -580,8 +644,8 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
             ld_chunk(X1, kC + r, (cb >> 3) + 1, 128, qg + 8);
 #pragma unroll
             for (int j = 0; j < 16; ++j) qg[j] -= x[j];
-            st_chunk(blob + B::QP, r, cb >> 3, kC, qg);
-            st_chunk(blob + B::QP, r, (cb >> 3) + 1, kC, qg + 8);
+            st_chunk(stg + L::QP_S, r, cb >> 3, kC, qg);
+            st_chunk(stg + L::QP_S, r, (cb >> 3) + 1, kC, qg + 8);
           }
         }
       }
@@ -594,8 +658,13 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
     // ---- (9) record -> workspace (one bulk copy; its read is awaited before
     // the record region is written again)
     if (tid == 0) {
-      uint8_t *dst = ws + sizeof(WorkspaceHeader) + (size_t)idx * B::BYTES;
-      ptx::bulk_s2g(dst, blob, B::BYTES);
+      uint8_t *dst = ws + sizeof(WorkspaceHeader) + (size_t)idx * Rr::BYTES;
+      if (D == 128) {
+        ptx::bulk_s2g(dst, stg, Rr::PRE);                           // Ap | Qp^T
+        ptx::bulk_s2g(dst + Rr::GC, stg + L::GC_S, D * 4);          // gamma_C
+      } else {
+        ptx::bulk_s2g(dst, stg, Rr::BYTES);
+      }
       ptx::bulk_commit();
     }
   }
@@ -610,27 +679,245 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
 
 // ============================================================== scan kernel
 
-template <int D, int NB>
-struct ScanSmem {
-  using B = Blob<D>;
+// D = 64: double-buffered records, one commit per chunk, merged accumulator
+// (lanes 0..63 state, lanes 64..127 output).
+template <int NB>
+struct ScanSmem64 {
+  using B = Rec<64>;
+  static constexpr int D = 64;
   static constexpr uint32_t STAGE_BYTES = B::PRE + NB * 128 + D * 4;  // Ap|Qp|Kbar^T|M, U^T block, gamma_C
   static constexpr uint32_t STAGE = align1k(STAGE_BYTES);
   static constexpr uint32_t SB = 2 * STAGE;                 // bf16 state operand [NB rows][D]
   static constexpr uint32_t BAR = SB + NB * D * 2;          // full[2], mma
   static constexpr uint32_t TMEMP = BAR + 3 * 8;
   static constexpr uint32_t BYTES = TMEMP + 8;
-  static constexpr uint32_t TMEM_COLS = (D == 128) ? ((2 * NB <= 32) ? 32 : (2 * NB <= 64 ? 64 : 128)) : (NB <= 32 ? 32 : 64);
+  static constexpr uint32_t TMEM_COLS = NB <= 32 ? 32 : 64;
 };
 
-template <int D, int NB>
-__global__ void __launch_bounds__(128, 1)
-kda_scan_kernel(const float *__restrict__ h0, __nv_bfloat16 *__restrict__ o,
-                float *__restrict__ hT, int T, int NC, uint8_t *__restrict__ ws) {
-  using B = Blob<D>;
-  using L = ScanSmem<D, NB>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                            ~static_cast<uintptr_t>(1023));
+// D = 128: a producer warp streams records through a ring of kStages stages;
+// four consumer warps (TMEM lane = key channel) own the state.  Per chunk the
+// serial path is: wait for the previous state products, read S, write its
+// bf16 copy (row-major, read MN-major by the MMA), write
+// gamma_C * S + Kbar^T U back to TMEM, then one thread issues S += Ap S (8
+// MMAs, committed on their own) and o = Qp S (8 MMAs into one of two output
+// accumulators, committed separately and read one chunk later with M U added).
+constexpr int kStages = 3;
+template <int NB>
+struct ScanSmem128 {
+  using R = Rec<128>;
+  static_assert(NB == R::BLK, "a scan CTA owns one 32-column block");
+  static constexpr uint32_t BI_S = R::PRE;                   // B block [128][NB]
+  static constexpr uint32_t OI_S = BI_S + 128 * NB * 2;      // O block [C][NB]
+  static constexpr uint32_t GC_S = OI_S + kC * NB * 2;       // gamma_C [128]
+  static constexpr uint32_t STAGE_BYTES = GC_S + 128 * 4;
+  static constexpr uint32_t STAGE = align1k(STAGE_BYTES);
+  static constexpr uint32_t SB = kStages * STAGE;            // 2 x bf16 S [128 rows][64 cols]
+  static constexpr uint32_t BAR = SB + 2 * 128 * 64 * 2;     // full[3], empty[3], mS, mO
+  static constexpr uint32_t TMEMP = BAR + (2 * kStages + 2) * 8;
+  static constexpr uint32_t BYTES = TMEMP + 8;
+  static constexpr uint32_t TMEM_COLS = 128;                 // S | o[0] | o[1]
+  static_assert(BYTES + 1024 <= 232448, "scan shared memory");
+};
+
+template <int NB>
+__device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfloat16 *__restrict__ o,
+                                          float *__restrict__ hT, int T, int NC,
+                                          uint8_t *__restrict__ ws, uint8_t *sm) {
+  constexpr int D = 128;
+  using R = Rec<128>;
+  using L = ScanSmem128<NB>;
+  uint64_t *full = reinterpret_cast<uint64_t *>(sm + L::BAR);
+  uint64_t *empty = full + kStages;
+  uint64_t *mS = empty + kStages;
+  uint64_t *mO = mS + 1;
+  uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(sm + L::TMEMP);
+  WorkspaceHeader *hdr = reinterpret_cast<WorkspaceHeader *>(ws);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.y, blk = blockIdx.x, j0 = blk * NB;
+  const uint8_t *rec0 = ws + sizeof(WorkspaceHeader) + (size_t)bh * NC * R::BYTES;
+  bool ok = true;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    ptx::mbar_init(mS, 1);
+    ptx::mbar_init(mO, 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc(tmem_ptr, L::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_ptr;
+
+  if (warp == 4) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      for (int j = 0; j < NC; ++j) {
+        const int s = j % kStages;
+        if (j >= kStages && ok && !ptx::mbar_wait(&empty[s], ((j / kStages) - 1) & 1, kWaitLimit)) {
+          ok = false;
+          report_error(hdr, KDA_ERR_TIMEOUT, 0x210u);
+        }
+        uint8_t *st = sm + s * L::STAGE;
+        const uint8_t *rec = rec0 + (size_t)j * R::BYTES;
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive_expect_tx(&full[s], L::STAGE_BYTES);
+        ptx::bulk_g2s(st, rec, R::PRE, &full[s]);
+        ptx::bulk_g2s(st + L::BI_S, rec + R::BI + (size_t)blk * (128 * NB * 2), 128 * NB * 2, &full[s]);
+        ptx::bulk_g2s(st + L::OI_S, rec + R::OI + (size_t)blk * (kC * NB * 2), kC * NB * 2, &full[s]);
+        ptx::bulk_g2s(st + L::GC_S, rec + R::GC, 128 * 4, &full[s]);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- consumers
+    const int r = tid;                                         // key channel = TMEM lane
+    const uint32_t tS = tmem + ((uint32_t)(warp * 32) << 16);  // state columns [0, NB)
+    const int orow = warp * 16 + lane;                         // output row (M = 64 layout)
+    {
+      const size_t s0 = (size_t)bh * D * D;
+#pragma unroll
+      for (int cb = 0; cb < NB; cb += 16) {
+        float x[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) x[j] = h0 ? h0[s0 + (size_t)r * D + j0 + cb + j] : 0.f;
+        ptx::tmem_st16(tS + cb, x);
+      }
+      ptx::tmem_st_wait();
+    }
+    auto store_o = [&](int chunk) {  // o rows of `chunk`: accumulator + M U
+      const uint32_t tO = tS + NB * (1 + (chunk & 1));
+      const uint8_t *oi = sm + (chunk % kStages) * L::STAGE + L::OI_S + (size_t)orow * NB * 2;
+      const int t = chunk * kC + orow;
+#pragma unroll
+      for (int cb = 0; cb < NB; cb += 16) {
+        float x[16];
+        ptx::tmem_ld16(tO + cb, x);
+        ptx::tmem_ld_wait();
+        if (lane < 16 && t < T) {
+          const uint4 a = *reinterpret_cast<const uint4 *>(oi + cb * 2);
+          const uint4 b = *reinterpret_cast<const uint4 *>(oi + cb * 2 + 16);
+          const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+          uint32_t pk[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const __nv_bfloat162 p2 = *reinterpret_cast<const __nv_bfloat162 *>(&w[e]);
+            pk[e] = pack_bf16x2(x[2 * e] + __low2float(p2), x[2 * e + 1] + __high2float(p2));
+          }
+          uint4 *dst = reinterpret_cast<uint4 *>(o + ((size_t)bh * T + t) * D + j0 + cb);
+          dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+      }
+    };
+    for (int i = 0; i < NC; ++i) {
+      const int s = i % kStages;
+      uint8_t *st = sm + s * L::STAGE;
+      uint8_t *sb = sm + L::SB + (i & 1) * (128 * 64 * 2);
+      if (i > 0 && ok && !ptx::mbar_wait(mS, (i - 1) & 1, kWaitLimit)) {
+        ok = false;
+        report_error(hdr, KDA_ERR_TIMEOUT, 0x201u);
+      }
+      ptx::tc_fence_after();
+      if (ok && !ptx::mbar_wait(&full[s], (i / kStages) & 1, kWaitLimit)) {
+        ok = false;
+        report_error(hdr, KDA_ERR_TIMEOUT, 0x202u);
+      }
+      {  // S -> bf16 operand; S <- gamma_C * S + B
+        const float gam = reinterpret_cast<const float *>(st + L::GC_S)[r];
+        const uint8_t *brow = st + L::BI_S + (size_t)r * NB * 2;
+#pragma unroll
+        for (int cb = 0; cb < NB; cb += 16) {
+          float x[16];
+          ptx::tmem_ld16(tS + cb, x);
+          ptx::tmem_ld_wait();
+          st_chunk(sb, r, cb >> 3, 128, x);
+          st_chunk(sb, r, (cb >> 3) + 1, 128, x + 8);
+          const uint4 a = *reinterpret_cast<const uint4 *>(brow + cb * 2);
+          const uint4 b = *reinterpret_cast<const uint4 *>(brow + cb * 2 + 16);
+          const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const __nv_bfloat162 p2 = *reinterpret_cast<const __nv_bfloat162 *>(&w[e]);
+            x[2 * e] = gam * x[2 * e] + __low2float(p2);
+            x[2 * e + 1] = gam * x[2 * e + 1] + __high2float(p2);
+          }
+          ptx::tmem_st16(tS + cb, x);
+        }
+      }
+      if (i > 0) {  // output of the previous chunk
+        if (ok && !ptx::mbar_wait(mO, (i - 1) & 1, kWaitLimit)) {
+          ok = false;
+          report_error(hdr, KDA_ERR_TIMEOUT, 0x203u);
+        }
+        ptx::tc_fence_after();
+        store_o(i - 1);
+      }
+      ptx::tmem_st_wait();
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      ptx::named_barrier(1, 128);
+      if (tid == 0) {
+        ptx::tc_fence_after();
+        const uint32_t sAP = ptx::smem_u32(st + R::AP), sQP = ptx::smem_u32(st + R::QP);
+        const uint32_t sSB = ptx::smem_u32(sb);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)  // S += Ap S   (S read MN-major)
+          ptx::mma_bf16_ss(tmem, umma::sdesc_k(sAP, D, ks), umma::sdesc_mn(sSB, 128, ks),
+                           umma::idesc_bf16_bmn(128, NB), 1);
+        ptx::mma_commit(mS);
+        const uint32_t tOc = tmem + NB * (1 + (i & 1));
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)  // o = Qp S   (Qp^T and S read MN-major)
+          ptx::mma_bf16_ss(tOc, umma::sdesc_mn(sQP, D, ks), umma::sdesc_mn(sSB, 128, ks),
+                           umma::idesc_bf16_abmn(64, NB), ks > 0);
+        ptx::mma_commit(mO);
+        if (i > 0) ptx::mbar_arrive(&empty[(i - 1) % kStages]);  // chunk i-1 fully consumed
+      }
+    }
+    if (NC > 0) {
+      if (ok && !ptx::mbar_wait(mO, (NC - 1) & 1, kWaitLimit)) {  // covers the state products too
+        ok = false;
+        report_error(hdr, KDA_ERR_TIMEOUT, 0x204u);
+      }
+      ptx::tc_fence_after();
+      store_o(NC - 1);
+    }
+    if (hT) {
+      const size_t s0 = (size_t)bh * D * D;
+#pragma unroll
+      for (int cb = 0; cb < NB; cb += 16) {
+        float x[16];
+        ptx::tmem_ld16(tS + cb, x);
+        ptx::tmem_ld_wait();
+        float4 *dst = reinterpret_cast<float4 *>(hT + s0 + (size_t)r * D + j0 + cb);
+#pragma unroll
+        for (int j4 = 0; j4 < 4; ++j4)
+          dst[j4] = make_float4(x[4 * j4], x[4 * j4 + 1], x[4 * j4 + 2], x[4 * j4 + 3]);
+      }
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, L::TMEM_COLS);
+  }
+}
+
+template <int NB>
+__device__ __forceinline__ void scan_d64(const float *__restrict__ h0, __nv_bfloat16 *__restrict__ o,
+                                         float *__restrict__ hT, int T, int NC,
+                                         uint8_t *__restrict__ ws, uint8_t *sm) {
+  constexpr int D = 64;
+  using B = Rec<64>;
+  using L = ScanSmem64<NB>;
   uint8_t *SB = sm + L::SB;
   uint64_t *full = reinterpret_cast<uint64_t *>(sm + L::BAR);
   uint64_t *mbar = full + 2;
@@ -638,6 +925,7 @@ kda_scan_kernel(const float *__restrict__ h0, __nv_bfloat16 *__restrict__ o,
   WorkspaceHeader *hdr = reinterpret_cast<WorkspaceHeader *>(ws);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (warp >= 4) return;  // 128 threads on this path
   const int bh = blockIdx.y, j0 = blockIdx.x * NB;
   const int dv = D;
   const uint8_t *rec0 = ws + sizeof(WorkspaceHeader) + (size_t)bh * NC * B::BYTES;
@@ -654,7 +942,7 @@ kda_scan_kernel(const float *__restrict__ h0, __nv_bfloat16 *__restrict__ o,
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  ptx::named_barrier(1, 128);
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_ptr;
   const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
@@ -688,7 +976,7 @@ kda_scan_kernel(const float *__restrict__ h0, __nv_bfloat16 *__restrict__ o,
   }
   if (tid == 0 && NC > 0) issue_loads(0, 0);
   ptx::tc_fence_before();
-  __syncthreads();
+  ptx::named_barrier(1, 128);
 
   auto store_o_rows = [&](int chunk) {
     // D = 128: output rows sit in lanes 32w + (0..15) (M = 64 layout); D = 64: lanes 64..127.
@@ -753,7 +1041,7 @@ kda_scan_kernel(const float *__restrict__ h0, __nv_bfloat16 *__restrict__ o,
     ptx::tmem_st_wait();
     ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
-    __syncthreads();
+    ptx::named_barrier(1, 128);
     if (tid == 0) {
       ptx::tc_fence_after();
       const uint32_t sAP = ptx::smem_u32(st + B::AP), sQP = ptx::smem_u32(st + B::QP);
@@ -816,11 +1104,25 @@ kda_scan_kernel(const float *__restrict__ h0, __nv_bfloat16 *__restrict__ o,
     }
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  ptx::named_barrier(1, 128);
   if (warp == 0) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, L::TMEM_COLS);
   }
+}
+
+
+template <int D, int NB>
+__global__ void __launch_bounds__(160, 1)
+kda_scan_kernel(const float *__restrict__ h0, __nv_bfloat16 *__restrict__ o,
+                float *__restrict__ hT, int T, int NC, uint8_t *__restrict__ ws) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                            ~static_cast<uintptr_t>(1023));
+  if constexpr (D == 128)
+    scan_d128<NB>(h0, o, hT, T, NC, ws, sm);
+  else
+    scan_d64<NB>(h0, o, hT, T, NC, ws, sm);
 }
 
 // ============================================================== launch
@@ -835,7 +1137,8 @@ kda_status launch_d(const void *q, const void *k, const void *v, const float *be
   constexpr int NB = scan_nb<D>();
   const int NC = (T + kC - 1) / kC;
   const uint32_t prep_smem = PrepSmem<D>::BYTES + 1024;
-  const uint32_t scan_smem = ScanSmem<D, NB>::BYTES + 1024;
+  const uint32_t scan_smem =
+      (D == 128 ? ScanSmem128<NB>::BYTES : ScanSmem64<NB>::BYTES) + 1024;
   if (cudaFuncSetAttribute(kda_prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)prep_smem) != cudaSuccess ||
       cudaFuncSetAttribute(kda_scan_kernel<D, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -855,7 +1158,7 @@ kda_status launch_d(const void *q, const void *k, const void *v, const float *be
         static_cast<const __nv_bfloat16 *>(v), beta, log_alpha, (int)am, T, NC, (int)total, ws);
   }
   timer.mark();
-  kda_scan_kernel<D, NB><<<dim3(D / NB, BH), 128, scan_smem, st>>>(
+  kda_scan_kernel<D, NB><<<dim3(D / NB, BH), D == 128 ? 160 : 128, scan_smem, st>>>(
       h0, static_cast<__nv_bfloat16 *>(o), hT, T, NC, ws);
   timer.mark();
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
@@ -870,7 +1173,7 @@ bool chunk_tc_supported(int dk, int dv, int C, kda_dtype dt) {
 size_t chunk_tc_workspace_bytes(int B, int H, int T, int dk, int dv, int C) {
   if (dk != dv || C != kC) return 0;
   const size_t NC = (size_t)(T + kC - 1) / kC;
-  const size_t rec = dk == 128 ? Blob<128>::BYTES : Blob<64>::BYTES;
+  const size_t rec = dk == 128 ? Rec<128>::BYTES : Rec<64>::BYTES;
   return (size_t)B * H * NC * rec;
 }
 

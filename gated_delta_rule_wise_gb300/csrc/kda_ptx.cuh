@@ -53,6 +53,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
   return false;
 }
 
+// Barrier among `count` threads (a multiple of 32) under id `id` (1..15).
+__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ---------------------------------------------------------------- TMA (bulk)
 // 1-D bulk copy global -> shared, completing on an mbarrier (tx bytes).
 // Both addresses 16-byte aligned, size a multiple of 16.

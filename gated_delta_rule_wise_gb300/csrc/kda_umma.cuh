@@ -68,8 +68,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
          ((uint32_t)(M >> 4) << 24);
 }
-// Same with the A operand MN-major.
+// Same with the A operand MN-major, the B operand MN-major, or both.
 __host__ __device__ constexpr uint32_t idesc_bf16_amn(int M, int N) { return idesc_bf16(M, N) | (1u << 15); }
+__host__ __device__ constexpr uint32_t idesc_bf16_bmn(int M, int N) { return idesc_bf16(M, N) | (1u << 16); }
+__host__ __device__ constexpr uint32_t idesc_bf16_abmn(int M, int N) {
+  return idesc_bf16(M, N) | (1u << 15) | (1u << 16);
+}
 
 }  // namespace umma
 }  // namespace kda

@@ -149,7 +149,7 @@ def test_tensor_path_is_what_auto_picks_for_bf16_c64(lib):
     assert kda.kda_chunk_fwd_kernel_names(1, 1, 0, 128, 128, 64, kda.KDA_BF16, 2) == ["kda_scan_kernel"]
     assert kda.kda_chunk_fwd_kernel_names(1, 1, 64, 16, 16, 16, kda.KDA_F32, 2) == ["chunk_ffma_kernel"]
     big = kda.kda_chunk_fwd_workspace_size(1, 32, 131072, 128, 128, 64, kda.KDA_BF16, 2)
-    assert big == 256 + 32 * 2048 * 90624     # one 90624-byte record per (head, chunk)
+    assert big == 256 + 32 * 2048 * 98816     # one 98816-byte record per (head, chunk)
 
 
 def test_status_and_selftest_validation(lib):

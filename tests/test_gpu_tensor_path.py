@@ -1,9 +1,10 @@
 """White-box checks of the tensor-core prefill path.
 
-The prep kernel leaves one record per (head, chunk) in the workspace:
-Ap = -Kbar^T W, Qp = Q*gamma - M W (stored transposed when D = 128), Kbar^T,
-M, U^T (bf16 tiles in the 128-byte swizzled K-major operand layout) and
-gamma_C (float).  These tests decode the
+The prep kernel leaves one record per (head, chunk) in the workspace.
+D = 64: Ap = -Kbar^T W, Qp = Q*gamma - M W, Kbar^T, M, U^T (bf16 tiles in the
+128-byte swizzled K-major operand layout) and gamma_C (float).
+D = 128: Ap, Qp^T (swizzled tiles), B = Kbar^T U and O = M U (plain bf16 in
+32-column blocks) and gamma_C.  These tests decode the
 records and compare each matrix with a float64 numpy evaluation of its
 definition (the chunk-wise form with cumulative decay), then check that the
 tensor path and the CUDA-core path agree on o and hT.  End-to-end parity with
@@ -35,7 +36,16 @@ def untile(buf, rows, K):
     return (u16[off].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
+def bf16_blocks(buf, rows):
+    """[4][rows][32] bf16 blocks -> float64 [rows, 128]."""
+    u16 = np.frombuffer(buf, dtype=np.uint16).reshape(4, rows, 32)
+    f = (u16.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return np.concatenate([f[b] for b in range(4)], axis=1)
+
+
 def record_layout(D):
+    if D == 128:
+        return dict(AP=0, QP=32768, BI=49152, OI=81920, GC=98304, BYTES=98816)
     AP = 0
     QP = AP + D * D * 2
     KBT = QP + C * D * 2
@@ -59,7 +69,8 @@ def chunk_reference(q, k, v, beta, la):
     Wm = Tm @ Kb
     U = Tm @ (beta[:, None] * v)
     M = np.tril(Qg @ Kh.T)
-    return dict(AP=-Kbar.T @ Wm, QP=Qg - M @ Wm, KBT=Kbar.T, MM=M, UT=U.T, GC=gam[-1])
+    return dict(AP=-Kbar.T @ Wm, QP=Qg - M @ Wm, KBT=Kbar.T, MM=M, UT=U.T, GC=gam[-1],
+                BI=Kbar.T @ U, OI=M @ U)
 
 
 @pytest.mark.parametrize("D,alpha", [(128, "channel"), (128, "scalar"), (64, "none"), (64, "channel")])
@@ -93,13 +104,17 @@ def test_prep_records_match_definitions(D, alpha):
                                   pad(x["k"][0, h, sl].astype(np.float64)),
                                   pad(x["v"][0, h, sl].astype(np.float64)),
                                   pad(x["beta"][0, h, sl].astype(np.float64)), la)
-            qp = (untile(rec[L["QP"]:L["KBT"]], D, C).T if D == 128
-                  else untile(rec[L["QP"]:L["KBT"]], C, D))
-            got = dict(AP=untile(rec[L["AP"]:L["QP"]], D, D), QP=qp,
-                       KBT=untile(rec[L["KBT"]:L["MM"]], D, C), MM=untile(rec[L["MM"]:L["UT"]], C, C),
-                       UT=untile(rec[L["UT"]:L["GC"]], D, C),
-                       GC=np.frombuffer(rec[L["GC"]:L["BYTES"]], dtype=np.float32).astype(np.float64))
-            for key in ("GC", "KBT", "MM", "UT", "AP", "QP"):
+            gc = np.frombuffer(rec[L["GC"]:L["BYTES"]], dtype=np.float32).astype(np.float64)
+            if D == 128:
+                got = dict(AP=untile(rec[L["AP"]:L["QP"]], D, D),
+                           QP=untile(rec[L["QP"]:L["BI"]], D, C).T,
+                           BI=bf16_blocks(rec[L["BI"]:L["OI"]], D),
+                           OI=bf16_blocks(rec[L["OI"]:L["GC"]], C), GC=gc)
+            else:
+                got = dict(AP=untile(rec[L["AP"]:L["QP"]], D, D), QP=untile(rec[L["QP"]:L["KBT"]], C, D),
+                           KBT=untile(rec[L["KBT"]:L["MM"]], D, C), MM=untile(rec[L["MM"]:L["UT"]], C, C),
+                           UT=untile(rec[L["UT"]:L["GC"]], D, C), GC=gc)
+            for key in got:
                 e = rel_err(got[key], ref[key])
                 assert e <= 2e-2, f"D={D} {alpha} head {h} chunk {n}: {key} rel err {e:.3e}"
 
