@@ -694,14 +694,17 @@ struct ScanSmem64 {
   static constexpr uint32_t TMEM_COLS = NB <= 32 ? 32 : 64;
 };
 
-// D = 128: a producer warp streams records through a ring of kStages stages;
-// four consumer warps (TMEM lane = key channel) own the state.  Per chunk the
-// serial path is: wait for the previous state products, read S, write its
-// bf16 copy (row-major, read MN-major by the MMA), write
-// gamma_C * S + Kbar^T U back to TMEM, then one thread issues S += Ap S (8
-// MMAs, committed on their own) and o = Qp S (8 MMAs into one of two output
-// accumulators, committed separately and read one chunk later with M U added).
+// D = 128: three warp groups.  A producer warp streams records through a ring
+// of kStages stages.  Four state warps (TMEM lane = key channel) own S: per
+// chunk they wait for the previous state products, read S, write its bf16
+// copy (row-major, read MN-major by the MMA) and gamma_C * S + Kbar^T U back
+// to TMEM; then one of them issues S += Ap S (8 MMAs).  Four output warps
+// (same TMEM lane quarters) issue o = Qp S into one of two output
+// accumulators as soon as the bf16 copy exists, wait for it, add M U and store
+// o.  Only the state products and the state conversion are on the serial
+// path.
 constexpr int kStages = 3;
+constexpr int kScan128Threads = 288;  // 4 state warps, 4 output warps, 1 producer warp
 template <int NB>
 struct ScanSmem128 {
   using R = Rec<128>;
@@ -712,8 +715,9 @@ struct ScanSmem128 {
   static constexpr uint32_t STAGE_BYTES = GC_S + 128 * 4;
   static constexpr uint32_t STAGE = align1k(STAGE_BYTES);
   static constexpr uint32_t SB = kStages * STAGE;            // 2 x bf16 S [128 rows][64 cols]
-  static constexpr uint32_t BAR = SB + 2 * 128 * 64 * 2;     // full[3], empty[3], mS, mO
-  static constexpr uint32_t TMEMP = BAR + (2 * kStages + 2) * 8;
+  // full[3], empty[3], mS, sbready[2], mO[2]
+  static constexpr uint32_t BAR = SB + 2 * 128 * 64 * 2;
+  static constexpr uint32_t TMEMP = BAR + (2 * kStages + 5) * 8;
   static constexpr uint32_t BYTES = TMEMP + 8;
   static constexpr uint32_t TMEM_COLS = 128;                 // S | o[0] | o[1]
   static_assert(BYTES + 1024 <= 232448, "scan shared memory");
@@ -729,7 +733,8 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
   uint64_t *full = reinterpret_cast<uint64_t *>(sm + L::BAR);
   uint64_t *empty = full + kStages;
   uint64_t *mS = empty + kStages;
-  uint64_t *mO = mS + 1;
+  uint64_t *sbready = mS + 1;
+  uint64_t *mO = sbready + 2;
   uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(sm + L::TMEMP);
   WorkspaceHeader *hdr = reinterpret_cast<WorkspaceHeader *>(ws);
 
@@ -741,10 +746,13 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&full[s], 1);
-      ptx::mbar_init(&empty[s], 1);
+      ptx::mbar_init(&empty[s], 2);  // released by the state warps and by the output warps
     }
     ptx::mbar_init(mS, 1);
-    ptx::mbar_init(mO, 1);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&sbready[b], 1);
+      ptx::mbar_init(&mO[b], 1);
+    }
     ptx::fence_mbar_init();
   }
   if (warp == 0) {
@@ -755,8 +763,10 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_ptr;
+  const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+  auto sb_of = [&](int chunk) { return sm + L::SB + (chunk & 1) * (128 * 64 * 2); };
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ---------------------------------------------------------- producer
     if (lane == 0) {
       for (int j = 0; j < NC; ++j) {
@@ -775,26 +785,34 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
         ptx::bulk_g2s(st + L::GC_S, rec + R::GC, 128 * 4, &full[s]);
       }
     }
-  } else {
-    // ---------------------------------------------------------- consumers
-    const int r = tid;                                         // key channel = TMEM lane
-    const uint32_t tS = tmem + ((uint32_t)(warp * 32) << 16);  // state columns [0, NB)
-    const int orow = warp * 16 + lane;                         // output row (M = 64 layout)
-    {
-      const size_t s0 = (size_t)bh * D * D;
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------- output warps
+    const int orow = (warp - 4) * 16 + lane;  // output row (M = 64 layout: lanes 32w + 0..15)
+    for (int j = 0; j < NC; ++j) {
+      const int b = j & 1;
+      if (tid == 128) {  // issue o = Qp S for chunk j once its bf16 S exists
+        if (ok && !ptx::mbar_wait(&sbready[b], (j >> 1) & 1, kWaitLimit)) {
+          ok = false;
+          report_error(hdr, KDA_ERR_TIMEOUT, 0x220u);
+        }
+        ptx::tc_fence_after();
+        const uint8_t *st = sm + (j % kStages) * L::STAGE;
+        const uint32_t sQP = ptx::smem_u32(st + R::QP), sSB = ptx::smem_u32(sb_of(j));
+        const uint32_t tOc = tmem + NB * (1 + b);
 #pragma unroll
-      for (int cb = 0; cb < NB; cb += 16) {
-        float x[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) x[j] = h0 ? h0[s0 + (size_t)r * D + j0 + cb + j] : 0.f;
-        ptx::tmem_st16(tS + cb, x);
+        for (int ks = 0; ks < D / 16; ++ks)  // Qp^T and S read MN-major
+          ptx::mma_bf16_ss(tOc, umma::sdesc_mn(sQP, D, ks), umma::sdesc_mn(sSB, 128, ks),
+                           umma::idesc_bf16_abmn(64, NB), ks > 0);
+        ptx::mma_commit(&mO[b]);
       }
-      ptx::tmem_st_wait();
-    }
-    auto store_o = [&](int chunk) {  // o rows of `chunk`: accumulator + M U
-      const uint32_t tO = tS + NB * (1 + (chunk & 1));
-      const uint8_t *oi = sm + (chunk % kStages) * L::STAGE + L::OI_S + (size_t)orow * NB * 2;
-      const int t = chunk * kC + orow;
+      if (ok && !ptx::mbar_wait(&mO[b], (j >> 1) & 1, kWaitLimit)) {
+        ok = false;
+        report_error(hdr, KDA_ERR_TIMEOUT, 0x221u);
+      }
+      ptx::tc_fence_after();
+      const uint32_t tO = t_lane + NB * (1 + b);
+      const uint8_t *oi = sm + (j % kStages) * L::STAGE + L::OI_S + (size_t)orow * NB * 2;
+      const int t = j * kC + orow;
 #pragma unroll
       for (int cb = 0; cb < NB; cb += 16) {
         float x[16];
@@ -802,8 +820,8 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
         ptx::tmem_ld_wait();
         if (lane < 16 && t < T) {
           const uint4 a = *reinterpret_cast<const uint4 *>(oi + cb * 2);
-          const uint4 b = *reinterpret_cast<const uint4 *>(oi + cb * 2 + 16);
-          const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+          const uint4 c2 = *reinterpret_cast<const uint4 *>(oi + cb * 2 + 16);
+          const uint32_t w[8] = {a.x, a.y, a.z, a.w, c2.x, c2.y, c2.z, c2.w};
           uint32_t pk[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
@@ -815,14 +833,36 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
           dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
         }
       }
-    };
+      ptx::tc_fence_before();
+      ptx::named_barrier(2, 128);  // all output rows of chunk j read before the buffer is reused
+      if (tid == 128) ptx::mbar_arrive(&empty[j % kStages]);
+    }
+  } else {
+    // ---------------------------------------------------------- state warps
+    const int r = tid;  // key channel = TMEM lane
+    const uint32_t tS = t_lane;
+    {
+      const size_t s0 = (size_t)bh * D * D;
+#pragma unroll
+      for (int cb = 0; cb < NB; cb += 16) {
+        float x[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) x[j] = h0 ? h0[s0 + (size_t)r * D + j0 + cb + j] : 0.f;
+        ptx::tmem_st16(tS + cb, x);
+      }
+      ptx::tmem_st_wait();
+    }
     for (int i = 0; i < NC; ++i) {
       const int s = i % kStages;
       uint8_t *st = sm + s * L::STAGE;
-      uint8_t *sb = sm + L::SB + (i & 1) * (128 * 64 * 2);
+      uint8_t *sb = sb_of(i);
       if (i > 0 && ok && !ptx::mbar_wait(mS, (i - 1) & 1, kWaitLimit)) {
         ok = false;
         report_error(hdr, KDA_ERR_TIMEOUT, 0x201u);
+      }
+      if (i > 1 && ok && !ptx::mbar_wait(&mO[i & 1], ((i - 2) >> 1) & 1, kWaitLimit)) {
+        ok = false;  // the bf16 copy of chunk i-2 has been read by its output products
+        report_error(hdr, KDA_ERR_TIMEOUT, 0x203u);
       }
       ptx::tc_fence_after();
       if (ok && !ptx::mbar_wait(&full[s], (i / kStages) & 1, kWaitLimit)) {
@@ -840,8 +880,8 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
           st_chunk(sb, r, cb >> 3, 128, x);
           st_chunk(sb, r, (cb >> 3) + 1, 128, x + 8);
           const uint4 a = *reinterpret_cast<const uint4 *>(brow + cb * 2);
-          const uint4 b = *reinterpret_cast<const uint4 *>(brow + cb * 2 + 16);
-          const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+          const uint4 c2 = *reinterpret_cast<const uint4 *>(brow + cb * 2 + 16);
+          const uint32_t w[8] = {a.x, a.y, a.z, a.w, c2.x, c2.y, c2.z, c2.w};
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const __nv_bfloat162 p2 = *reinterpret_cast<const __nv_bfloat162 *>(&w[e]);
@@ -851,44 +891,27 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
           ptx::tmem_st16(tS + cb, x);
         }
       }
-      if (i > 0) {  // output of the previous chunk
-        if (ok && !ptx::mbar_wait(mO, (i - 1) & 1, kWaitLimit)) {
-          ok = false;
-          report_error(hdr, KDA_ERR_TIMEOUT, 0x203u);
-        }
-        ptx::tc_fence_after();
-        store_o(i - 1);
-      }
       ptx::tmem_st_wait();
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       ptx::named_barrier(1, 128);
       if (tid == 0) {
         ptx::tc_fence_after();
-        const uint32_t sAP = ptx::smem_u32(st + R::AP), sQP = ptx::smem_u32(st + R::QP);
-        const uint32_t sSB = ptx::smem_u32(sb);
+        const uint32_t sAP = ptx::smem_u32(st + R::AP), sSB = ptx::smem_u32(sb);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)  // S += Ap S   (S read MN-major)
           ptx::mma_bf16_ss(tmem, umma::sdesc_k(sAP, D, ks), umma::sdesc_mn(sSB, 128, ks),
                            umma::idesc_bf16_bmn(128, NB), 1);
         ptx::mma_commit(mS);
-        const uint32_t tOc = tmem + NB * (1 + (i & 1));
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)  // o = Qp S   (Qp^T and S read MN-major)
-          ptx::mma_bf16_ss(tOc, umma::sdesc_mn(sQP, D, ks), umma::sdesc_mn(sSB, 128, ks),
-                           umma::idesc_bf16_abmn(64, NB), ks > 0);
-        ptx::mma_commit(mO);
-        if (i > 0) ptx::mbar_arrive(&empty[(i - 1) % kStages]);  // chunk i-1 fully consumed
+        ptx::mbar_arrive(&sbready[i & 1]);
+        if (i > 0) ptx::mbar_arrive(&empty[(i - 1) % kStages]);  // state side done with chunk i-1
       }
     }
-    if (NC > 0) {
-      if (ok && !ptx::mbar_wait(mO, (NC - 1) & 1, kWaitLimit)) {  // covers the state products too
-        ok = false;
-        report_error(hdr, KDA_ERR_TIMEOUT, 0x204u);
-      }
-      ptx::tc_fence_after();
-      store_o(NC - 1);
+    if (NC > 0 && ok && !ptx::mbar_wait(mS, (NC - 1) & 1, kWaitLimit)) {
+      ok = false;
+      report_error(hdr, KDA_ERR_TIMEOUT, 0x204u);
     }
+    ptx::tc_fence_after();
     if (hT) {
       const size_t s0 = (size_t)bh * D * D;
 #pragma unroll
@@ -1113,7 +1136,7 @@ __device__ __forceinline__ void scan_d64(const float *__restrict__ h0, __nv_bflo
 
 
 template <int D, int NB>
-__global__ void __launch_bounds__(160, 1)
+__global__ void __launch_bounds__(kScan128Threads, 1)
 kda_scan_kernel(const float *__restrict__ h0, __nv_bfloat16 *__restrict__ o,
                 float *__restrict__ hT, int T, int NC, uint8_t *__restrict__ ws) {
   extern __shared__ uint8_t smem_raw[];
@@ -1158,7 +1181,7 @@ kda_status launch_d(const void *q, const void *k, const void *v, const float *be
         static_cast<const __nv_bfloat16 *>(v), beta, log_alpha, (int)am, T, NC, (int)total, ws);
   }
   timer.mark();
-  kda_scan_kernel<D, NB><<<dim3(D / NB, BH), D == 128 ? 160 : 128, scan_smem, st>>>(
+  kda_scan_kernel<D, NB><<<dim3(D / NB, BH), D == 128 ? kScan128Threads : 128, scan_smem, st>>>(
       h0, static_cast<__nv_bfloat16 *>(o), hT, T, NC, ws);
   timer.mark();
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
