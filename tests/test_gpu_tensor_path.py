@@ -3,7 +3,7 @@
 The prep kernel leaves one record per (head, chunk) in the workspace.
 D = 64: Ap = -Kbar^T W, Qp = Q*gamma - M W, Kbar^T, M, U^T (bf16 tiles in the
 128-byte swizzled K-major operand layout) and gamma_C (float).
-D = 128: Ap, Qp^T (swizzled tiles), B = Kbar^T U and O = M U (plain bf16 in
+D = 128: Ap, Qp (swizzled tiles), B = Kbar^T U and O = M U (plain bf16 in
 32-column blocks) and gamma_C.  These tests decode the
 records and compare each matrix with a float64 numpy evaluation of its
 definition (the chunk-wise form with cumulative decay), then check that the
@@ -107,7 +107,7 @@ def test_prep_records_match_definitions(D, alpha):
             gc = np.frombuffer(rec[L["GC"]:L["BYTES"]], dtype=np.float32).astype(np.float64)
             if D == 128:
                 got = dict(AP=untile(rec[L["AP"]:L["QP"]], D, D),
-                           QP=untile(rec[L["QP"]:L["BI"]], D, C).T,
+                           QP=untile(rec[L["QP"]:L["BI"]], C, D),
                            BI=bf16_blocks(rec[L["BI"]:L["OI"]], D),
                            OI=bf16_blocks(rec[L["OI"]:L["GC"]], C), GC=gc)
             else:
