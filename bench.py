@@ -301,6 +301,8 @@ def run_ours(args, rank, world, local, dist):
     stream = torch.cuda.current_stream(dev)
     peaks, peak_src = load_peaks()
     w = W.KDA_PREFILL_BF16
+    if args.seq_len:  # shorter sequences for profiler captures; not the headline
+        w = w.with_(T=args.seq_len)
     wd = W.KDA_DECODE_BF16
 
     # ---- inputs
@@ -478,6 +480,10 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=16384,
                     help="tokens per head in each reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seq-len", type=int, default=0,
+                    help="prefill T other than the workload's 131072 (profiler captures "
+                         "of a smaller case; the line then names that T and is not the "
+                         "headline)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -166,8 +166,14 @@ __device__ __forceinline__ void fma4(float4 &acc, float a, const float4 &b) {
 // immediate offset.  Leaves T (float, lower blocks) in TF and the bf16 K-major
 // [C][C] tile of T (zeros above the diagonal) in TT.  All 256 threads call
 // it; XS (6 x 256 floats) is scratch inside TT.
+// `late` runs on threads 64..255 while threads 0..63 form the last block of
+// T, after the last read of AF: the caller may reuse AF's space there.
+struct NoLateWork {
+  __device__ void operator()() const {}
+};
+template <class Late = NoLateWork>
 __device__ __forceinline__ void blocked_unit_lower_inverse(const float *AF, float *TF, uint8_t *TT,
-                                                           int tid) {
+                                                           int tid, const Late &late = Late()) {
   float *XS = reinterpret_cast<float *>(TT);
   if (tid < kC) {
     const int b = tid >> 4, j = tid & 15, o = b * 16;
@@ -243,7 +249,10 @@ __device__ __forceinline__ void blocked_unit_lower_inverse(const float *AF, floa
     x.x += a.x; x.y += a.y; x.z += a.z; x.w += a.w;
   }
   __syncthreads();
-  if (g == 0) neg_tii_x(3, 0, 5);                    // T_30
+  if (g == 0)
+    neg_tii_x(3, 0, 5);                               // T_30
+  else
+    late();
   __syncthreads();
   for (int u = tid; u < kC * 8; u += 256) {  // bf16 operand tile, zeros above the diagonal blocks
     const int row = u >> 3, c8 = u & 7;
@@ -676,50 +685,52 @@ __device__ __forceinline__ void prep_d64(const __nv_bfloat16 *__restrict__ q,
   }
 }
 
-// D = 128 prep.  Per chunk (one CTA per SM, chunks taken in turn):
+// D = 128 prep.  Two CTAs share an SM (about 109 KB of shared memory, 256 TMEM
+// columns and at most 128 registers per thread each), so one CTA's MMA waits,
+// barriers and loads overlap the other's work.  Per chunk:
 //  (0) decay, one thread per key channel and half of the rows: g = running sum
-//      of -exp(log_alpha), gamma = exp(g) to a float tile;
-//  (1) one thread per (row, 8 channels): K_beta = beta K gamma, Q*gamma,
-//      beta V, K/gamma and Kbar = K gamma_C / gamma, all written as natural
-//      (row = token) swizzled tiles;
+//      of -exp(log_alpha) read straight from global memory, gamma = exp(g) to
+//      a float tile; gamma_C to the record;
+//  (1) the chunk's q, k, v rows (bulk copies into the operand area) to
+//      registers, then one thread per (row, 8 channels) writes K_beta = beta K
+//      gamma, Q*gamma, beta V and K/gamma as natural (row = token) swizzled
+//      tiles over them;
 //  (2) [A; M] = [K_beta; Q*gamma] (K/gamma)^T        8 MMAs (M = 128, N = 64)
-//  (3) A to float, M to a bf16 tile;  (4) T = (I + A)^-1 (blocked)
+//  (3) A to float;  (4) T = (I + A)^-1 (blocked), M to a bf16 tile in A's
+//      space while the last block of T is formed
 //  (5) [W | U] = T [K_beta | beta V]                   4 MMAs (M = 64, N = 256),
 //      the right factor read MN-major from the natural tiles
-//  (6) [W | U] to a natural tile
-//  (7) Kbar^T [W | U] and M [W | U]                    8 MMAs (N = 256),
-//      Kbar^T and [W | U] read MN-major
-//  (8) Ap = -Kbar^T W and Qp = Q*gamma - M W to the record tiles, B = Kbar^T U
-//      and O = M U straight to the record.
-// The next chunk's q, k, v rows (bulk copies) and decay inputs (registers,
-// three batches under the three MMA waits) are fetched during this one.
+//  (6) [W | U] to a natural tile over K_beta and beta V
+//  (7) (K/gamma)^T [W | U]                              4 MMAs (M = 128, N = 256)
+//  (8) Ap = -gamma_C (K/gamma)^T W and B = gamma_C (K/gamma)^T U to the record
+//  (9) M [W | U]                                        4 MMAs (M = 64, N = 256)
+// (10) Qp = Q*gamma - M W and O = M U to the record.
+// Record tiles go to global memory straight from registers, already swizzled.
 struct PrepSmem128 {
   using R = Rec<128>;
   static constexpr int D = 128;
-  // R_A: gamma as float [C][D] (phases 0-1) | A, T float (3-4) | Ap tile (8-9)
-  static constexpr uint32_t RA = 0;
-  static constexpr uint32_t EG = RA, AF = RA, TF = RA + kC * kLD * 4, AP_S = RA;
-  // R_B: T bf16 tile and M tile (3-7) | Qp tile (8-9)
-  static constexpr uint32_t RB = align1k(RA + 2 * kC * kLD * 4);
-  static constexpr uint32_t TT = RB, MM = RB + kC * kC * 2, QP_S = RB;
-  // X1: blocks 0-1 = [K_beta; Q*gamma] (128 rows x 128), blocks 2-3 = [beta V; K/gamma];
-  // blocks 2-3 hold [W | U] (64 rows x 256, 8 KB column blocks) from phase 6 on.
-  static constexpr uint32_t X1 = RB + 16384;
-  static constexpr uint32_t WU = X1 + 32768;
-  static constexpr uint32_t KB = X1 + 65536;                 // Kbar [C rows][D]
-  static constexpr uint32_t RAW = KB + kC * D * 2;           // q | k | v [C][D] bf16
-  static constexpr uint32_t GC_S = RAW + 3 * kC * D * 2;     // gamma_C (record copy)
-  static constexpr uint32_t EGC = GC_S + D * 4;              // gamma_C (float, for phase 1)
-  static constexpr uint32_t BETA = EGC + D * 4;
-  static constexpr uint32_t PART = BETA + kC * 4;            // float [2][D]
+  // X1: blocks 0-1 = [K_beta; Q*gamma] (128 rows x 128), blocks 2-3 = [beta V;
+  // K/gamma]; rows 0-63 of the four blocks hold [W | U] (64 rows x 256) from
+  // phase 6 on.  Before phase 1 its first 48 KB receive the raw q | k | v rows.
+  static constexpr uint32_t X1 = 0;
+  static constexpr uint32_t RAW = X1;
+  // R_A: gamma as float [C][D] (phases 0-1) | A, T float (3-4) | M tile (4-9)
+  static constexpr uint32_t RA = X1 + 65536;
+  static constexpr uint32_t EG = RA, AF = RA, TF = RA + kC * kLD * 4, MM = RA;
+  static constexpr uint32_t TT = align1k(RA + 2 * kC * kLD * 4);  // T bf16; solve scratch before
+  static constexpr uint32_t GCS = TT + kC * kC * 2;  // gamma_C float [D]
+  static constexpr uint32_t BETA = GCS + D * 4;      // float [C]
+  static constexpr uint32_t PART = BETA + kC * 4;    // float [2][D]
   static constexpr uint32_t BAR = PART + 2 * D * 4;
   static constexpr uint32_t LBAR = BAR + 8;
   static constexpr uint32_t TMEMP = LBAR + 8;
   static constexpr uint32_t BYTES = TMEMP + 8;
-  static constexpr uint32_t TMEM_COLS = 512;
-  static_assert(2 * kC * kLD * 4 >= 32768 && kC * D * 4 <= 2 * kC * kLD * 4, "R_A sizes");
-  static_assert((RB & 1023u) == 0 && (X1 & 1023u) == 0 && (KB & 1023u) == 0, "tile alignment");
-  static_assert(BYTES + 1024 <= 232448, "prep shared memory");
+  static constexpr uint32_t TMEM_COLS = 256;
+  static_assert(kC * D * 4 <= 2 * kC * kLD * 4, "gamma tile fits R_A");
+  static_assert(kC * kC * 2 <= kC * kLD * 4, "M tile fits A's space");
+  static_assert((RA & 1023u) == 0 && (TT & 1023u) == 0, "tile alignment");
+  // two CTAs per SM: 228 KB per SM, 1 KB reserved per CTA, 1 KB alignment slack
+  static_assert(2 * (BYTES + 1024 + 1024) <= 233472, "prep shared memory");
 };
 
 __device__ __forceinline__ void unpack8(const uint4 &u, float *f) {
@@ -730,6 +741,10 @@ __device__ __forceinline__ void unpack8(const uint4 &u, float *f) {
     f[2 * i] = __low2float(p);
     f[2 * i + 1] = __high2float(p);
   }
+}
+__device__ __forceinline__ uint4 pack8(const float *x) {
+  return make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                    pack_bf16x2(x[6], x[7]));
 }
 
 __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
@@ -746,11 +761,9 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
   float *EG = reinterpret_cast<float *>(sm + L::EG);
   float *AF = reinterpret_cast<float *>(sm + L::AF);
   float *TF = reinterpret_cast<float *>(sm + L::TF);
-  uint8_t *TT = sm + L::TT, *MM = sm + L::MM;
-  uint8_t *X1 = sm + L::X1, *WU = sm + L::WU, *KB = sm + L::KB;
+  uint8_t *TT = sm + L::TT, *MM = sm + L::MM, *X1 = sm + L::X1;
   uint8_t *rawq = sm + L::RAW, *rawk = rawq + kC * D * 2, *rawv = rawk + kC * D * 2;
-  float *gcs = reinterpret_cast<float *>(sm + L::GC_S);
-  float *egc = reinterpret_cast<float *>(sm + L::EGC);
+  float *gcs = reinterpret_cast<float *>(sm + L::GCS);
   float *betas = reinterpret_cast<float *>(sm + L::BETA);
   float *part = reinterpret_cast<float *>(sm + L::PART);
   uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::BAR);
@@ -759,13 +772,14 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
   WorkspaceHeader *hdr = reinterpret_cast<WorkspaceHeader *>(ws);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3, colhalf = warp >> 2;  // TMEM lane quarter, column half
   const int c = tid & (D - 1), half = tid >> 7, r0 = half * R;   // decay phase mapping
   bool ok = true;
 
   auto issue_raw = [&](int idx) {
-    const int bh = idx / NC, t0 = (idx % NC) * kC;
+    const int t0 = (idx % NC) * kC;
     const int valid = min(kC, T - t0);
-    const size_t row0 = (size_t)bh * T + t0;
+    const size_t row0 = (size_t)(idx / NC) * T + t0;
     const uint32_t bytes = (uint32_t)valid * D * 2;
     ptx::mbar_arrive_expect_tx(lbar, 3 * bytes);
     ptx::bulk_g2s(rawq, q + row0 * D, bytes, lbar);
@@ -786,34 +800,12 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_ptr;
-  const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-  const uint32_t sX1 = ptx::smem_u32(X1), sWU = ptx::smem_u32(WU), sKB = ptx::smem_u32(KB);
-  const uint32_t sTT = ptx::smem_u32(TT), sMM = ptx::smem_u32(MM);
+  const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+  const uint32_t sX1 = ptx::smem_u32(X1), sTT = ptx::smem_u32(TT), sMM = ptx::smem_u32(MM);
+  const uint32_t sWU = sX1;                          // [W | U]: rows 0-63 of the four blocks
+  const uint32_t sKH = sX1 + 32768 + kC * 128;       // K/gamma: rows 64-127 of blocks 2-3
   if (tid == 0 && (int)blockIdx.x < total) issue_raw(blockIdx.x);
   uint32_t mma_phase = 0;
-
-  float la_n[R], b_n = 0.f;
-  auto load_la = [&](int idxn, auto I0, auto I1) {
-    constexpr int i0 = decltype(I0)::value, i1 = decltype(I1)::value;
-    const int t0n = (idxn % NC) * kC;
-    const int validn = min(kC, T - t0n);
-    const size_t row0n = (size_t)(idxn / NC) * T + t0n;
-#pragma unroll
-    for (int i = i0; i < i1; ++i) {
-      const int rr = min(r0 + i, validn - 1);
-      la_n[i] = 0.f;
-      if (alpha_mode == KDA_ALPHA_CHANNEL)
-        la_n[i] = log_alpha[(row0n + rr) * D + c];
-      else if (alpha_mode == KDA_ALPHA_SCALAR)
-        la_n[i] = log_alpha[row0n + rr];
-    }
-    if (i0 == 0 && tid < kC) b_n = beta[row0n + min(tid, validn - 1)];
-  };
-  using I_0 = std::integral_constant<int, 0>;
-  using I_1 = std::integral_constant<int, 11>;
-  using I_2 = std::integral_constant<int, 22>;
-  using I_3 = std::integral_constant<int, R>;
-  if ((int)blockIdx.x < total) load_la(blockIdx.x, I_0{}, I_3{});
 
   auto wait_mma = [&](unsigned code) {
     if (ok && !ptx::mbar_wait(bar, mma_phase & 1, kWaitLimit)) {
@@ -831,230 +823,260 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
   };
 
   for (int idx = blockIdx.x, it = 0; idx < total; idx += gridDim.x, ++it) {
-    const int bh = idx / NC, n = idx % NC;
+    const int n = idx % NC;
     const int t0 = n * kC;
     const int valid = min(kC, T - t0);
-    const int idx_next = idx + (int)gridDim.x;
-    const bool has_next = idx_next < total;
+    const size_t row0 = (size_t)(idx / NC) * T + t0;
+    uint8_t *recg = ws + sizeof(WorkspaceHeader) + (size_t)idx * Rr::BYTES;
 
     // ---- (0) decay
     float ld[R];
 #pragma unroll
-    for (int i = 0; i < R; ++i)
-      ld[i] = (r0 + i < valid && alpha_mode != KDA_ALPHA_NONE) ? -__expf(la_n[i]) : 0.f;
+    for (int i = 0; i < R; ++i) {
+      const int rr = min(r0 + i, valid - 1);
+      ld[i] = 0.f;
+      if (alpha_mode == KDA_ALPHA_CHANNEL)
+        ld[i] = log_alpha[(row0 + rr) * D + c];
+      else if (alpha_mode == KDA_ALPHA_SCALAR)
+        ld[i] = log_alpha[row0 + rr];
+    }
+    if (tid < kC) betas[tid] = (tid < valid) ? beta[row0 + tid] : 0.f;
     float psum = 0.f;
 #pragma unroll
-    for (int i = 0; i < R; ++i) psum += ld[i];
+    for (int i = 0; i < R; ++i) {
+      ld[i] = (r0 + i < valid && alpha_mode != KDA_ALPHA_NONE) ? -__expf(ld[i]) : 0.f;
+      psum += ld[i];
+    }
     part[half * D + c] = psum;
-    if (tid < kC) betas[tid] = (tid < valid) ? b_n : 0.f;
-    if (tid == 0) ptx::bulk_wait_read_all();  // the previous record has left R_A, R_B, GC_S
     __syncthreads();
     {
       const float p0 = part[c], p1 = part[D + c];
       float g = half ? p0 : 0.f;
-      const float gC = p0 + p1;
 #pragma unroll
       for (int i = 0; i < R; ++i) {
         g += ld[i];
         EG[(r0 + i) * D + c] = __expf(g);
       }
       if (half == 0) {
-        const float e = __expf(gC);
-        egc[c] = e;
+        const float e = __expf(p0 + p1);
         gcs[c] = e;
+        reinterpret_cast<float *>(recg + Rr::GC)[c] = e;
       }
     }
     if (ok && !ptx::mbar_wait(lbar, it & 1, kWaitLimit)) {
       ok = false;
       report_error(hdr, KDA_ERR_TIMEOUT, 0x100u);
     }
-    for (int i2 = valid * D / 8 + tid; i2 < kC * D / 8; i2 += 256) {  // zero padded raw rows
-      reinterpret_cast<uint4 *>(rawq)[i2] = make_uint4(0u, 0u, 0u, 0u);
-      reinterpret_cast<uint4 *>(rawk)[i2] = make_uint4(0u, 0u, 0u, 0u);
-      reinterpret_cast<uint4 *>(rawv)[i2] = make_uint4(0u, 0u, 0u, 0u);
-    }
     __syncthreads();
 
-    // ---- (1) decayed tiles, one thread per (row, 8 channels)
+    // ---- (1) decayed tiles, one thread per (row, 8 channels): raw rows to
+    // registers first (the tiles overwrite them), rows past the end as zeros
+    uint4 rq[4], rk[4], rv[4];
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const int u = tid + 256 * m;
       const int r = u >> 4, c8 = u & 15;
-      float kf[8], qf[8], vf[8], eg[8], ec[8];
-      unpack8(*reinterpret_cast<const uint4 *>(rawk + r * (D * 2) + c8 * 16), kf);
-      unpack8(*reinterpret_cast<const uint4 *>(rawq + r * (D * 2) + c8 * 16), qf);
-      unpack8(*reinterpret_cast<const uint4 *>(rawv + r * (D * 2) + c8 * 16), vf);
+      const uint32_t off = (uint32_t)r * (D * 2) + (uint32_t)c8 * 16u;
+      const bool in = r < valid;
+      rq[m] = in ? *reinterpret_cast<const uint4 *>(rawq + off) : make_uint4(0u, 0u, 0u, 0u);
+      rk[m] = in ? *reinterpret_cast<const uint4 *>(rawk + off) : make_uint4(0u, 0u, 0u, 0u);
+      rv[m] = in ? *reinterpret_cast<const uint4 *>(rawv + off) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int u = tid + 256 * m;
+      const int r = u >> 4, c8 = u & 15;
+      float kf[8], qf[8], vf[8], eg[8];
+      unpack8(rk[m], kf);
+      unpack8(rq[m], qf);
+      unpack8(rv[m], vf);
       const float4 e0 = *reinterpret_cast<const float4 *>(EG + r * D + c8 * 8);
       const float4 e1 = *reinterpret_cast<const float4 *>(EG + r * D + c8 * 8 + 4);
-      const float4 f0 = *reinterpret_cast<const float4 *>(egc + c8 * 8);
-      const float4 f1 = *reinterpret_cast<const float4 *>(egc + c8 * 8 + 4);
       eg[0] = e0.x; eg[1] = e0.y; eg[2] = e0.z; eg[3] = e0.w;
       eg[4] = e1.x; eg[5] = e1.y; eg[6] = e1.z; eg[7] = e1.w;
-      ec[0] = f0.x; ec[1] = f0.y; ec[2] = f0.z; ec[3] = f0.w;
-      ec[4] = f1.x; ec[5] = f1.y; ec[6] = f1.z; ec[7] = f1.w;
       const float bt = betas[r];
-      float kb[8], qg[8], vb[8], kh[8], kbar[8];
+      float kb[8], qg[8], vb[8], kh[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const float inv = __fdividef(1.f, eg[e]);
         kb[e] = bt * kf[e] * eg[e];
         qg[e] = qf[e] * eg[e];
         vb[e] = bt * vf[e];
-        kh[e] = kf[e] * inv;
-        kbar[e] = kh[e] * ec[e];
+        kh[e] = kf[e] * __fdividef(1.f, eg[e]);
       }
       st_chunk(X1, r, c8, 128, kb);                 // K_beta          (blocks 0-1, rows 0-63)
       st_chunk(X1, kC + r, c8, 128, qg);            // Q * gamma       (blocks 0-1, rows 64-127)
       st_chunk(X1 + 32768, r, c8, 128, vb);         // beta V          (blocks 2-3, rows 0-63)
       st_chunk(X1 + 32768, kC + r, c8, 128, kh);    // K / gamma       (blocks 2-3, rows 64-127)
-      st_chunk(KB, r, c8, kC, kbar);                // Kbar
     }
     sync_for_mma();
-    if (has_next && tid == 0) issue_raw(idx_next);
 
     // ---- (2) [A; M] = [K_beta; Q*gamma] (K/gamma)^T   -> TMEM cols [0, 64)
     if (tid == 0) {
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks)
-        ptx::mma_bf16_ss(tmem, umma::sdesc_k(sX1, 128, ks),
-                         umma::sdesc_k(sX1 + 32768 + 8192, 128, ks),  // K/gamma rows of blocks 2-3
+        ptx::mma_bf16_ss(tmem, umma::sdesc_k(sX1, 128, ks), umma::sdesc_k(sKH, 128, ks),
                          umma::idesc_bf16(128, kC), ks > 0);
       ptx::mma_commit(bar);
     }
-    if (has_next) load_la(idx_next, I_0{}, I_1{});
     wait_mma(0x101u);
 
-    // ---- (3) rows 0..63: A (strict lower) as float; rows 64..127: M
-    if (warp < 4) {
+    // ---- (3) lanes 0..63: A (strict lower) as float, 32 columns per warp
+    if (quarter < 2) {
+      const int r = quarter * 32 + lane;
 #pragma unroll
-      for (int cb = 0; cb < kC; cb += 16) {
+      for (int h = 0; h < 2; ++h) {
+        const int cb = colhalf * 32 + h * 16;
         float x[16];
         ptx::tmem_ld16(t_lane + cb, x);
         ptx::tmem_ld_wait();
-        if (tid < kC) {
-          const int r = tid;
 #pragma unroll
-          for (int j4 = 0; j4 < 4; ++j4) {
-            const int m0 = cb + 4 * j4;
-            float4 a;
-            a.x = (m0 + 0 < r) ? x[4 * j4 + 0] : 0.f;
-            a.y = (m0 + 1 < r) ? x[4 * j4 + 1] : 0.f;
-            a.z = (m0 + 2 < r) ? x[4 * j4 + 2] : 0.f;
-            a.w = (m0 + 3 < r) ? x[4 * j4 + 3] : 0.f;
-            *reinterpret_cast<float4 *>(AF + r * kLD + m0) = a;
-          }
-        } else {
-          const int r = tid - kC;
+        for (int j4 = 0; j4 < 4; ++j4) {
+          const int m0 = cb + 4 * j4;
+          float4 a;
+          a.x = (m0 + 0 < r) ? x[4 * j4 + 0] : 0.f;
+          a.y = (m0 + 1 < r) ? x[4 * j4 + 1] : 0.f;
+          a.z = (m0 + 2 < r) ? x[4 * j4 + 2] : 0.f;
+          a.w = (m0 + 3 < r) ? x[4 * j4 + 3] : 0.f;
+          *reinterpret_cast<float4 *>(AF + r * kLD + m0) = a;
+        }
+      }
+    }
+    __syncthreads();
+
+    // ---- (4) T = (I + A)^-1; lanes 64..127 (M, lower incl.) to a bf16 tile
+    // in A's space once A is no longer read
+    blocked_unit_lower_inverse(AF, TF, TT, tid, [&]() {
+      if (quarter >= 2) {
+        const int r = quarter * 32 + lane - kC;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int cb = colhalf * 32 + h * 16;
+          float x[16];
+          ptx::tmem_ld16(t_lane + cb, x);
+          ptx::tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 16; ++j) x[j] = (cb + j <= r) ? x[j] : 0.f;
           st_chunk(MM, r, cb >> 3, kC, x);
           st_chunk(MM, r, (cb >> 3) + 1, kC, x + 8);
         }
       }
-    }
-    __syncthreads();
-
-    // ---- (4) T = (I + A)^-1
-    blocked_unit_lower_inverse(AF, TF, TT, tid);
+    });
     sync_for_mma();
 
-    // ---- (5) [W | U] = T [K_beta | beta V]   -> TMEM cols [256, 512), M = 64 layout
+    // ---- (5) [W | U] = T [K_beta | beta V]   -> TMEM cols [0, 256), M = 64 layout
     if (tid == 0) {
 #pragma unroll
       for (int ks = 0; ks < kC / 16; ++ks)
-        ptx::mma_bf16_ss(tmem + 256, umma::sdesc_k(sTT, kC, ks), umma::sdesc_mn(sX1, 128, ks),
+        ptx::mma_bf16_ss(tmem, umma::sdesc_k(sTT, kC, ks), umma::sdesc_mn(sX1, 128, ks),
                          umma::idesc_bf16_bmn(64, 256), ks > 0);
       ptx::mma_commit(bar);
     }
-    if (has_next) load_la(idx_next, I_1{}, I_2{});
     wait_mma(0x102u);
 
-    // ---- (6) [W | U] rows -> natural tile (over beta V and K/gamma, both consumed)
-    if (warp < 4) {
-      const int rr = warp * 16 + lane;
+    // ---- (6) [W | U] rows -> natural tile over K_beta and beta V (both consumed)
+    {
+      const int rr = quarter * 16 + lane;  // token row (lanes < 16 of the M = 64 layout)
 #pragma unroll
-      for (int cb = 0; cb < 256; cb += 16) {
+      for (int h = 0; h < 8; ++h) {
+        const int cb = colhalf * 128 + h * 16;
         float x[16];
-        ptx::tmem_ld16(t_lane + 256 + cb, x);
+        ptx::tmem_ld16(t_lane + cb, x);
         ptx::tmem_ld_wait();
         if (lane < 16) {
-          st_chunk(WU, rr, cb >> 3, kC, x);
-          st_chunk(WU, rr, (cb >> 3) + 1, kC, x + 8);
+          st_chunk(X1, rr, cb >> 3, 128, x);
+          st_chunk(X1, rr, (cb >> 3) + 1, 128, x + 8);
         }
       }
     }
     sync_for_mma();
 
-    // ---- (7) Kbar^T [W | U] -> cols [0, 256);  M [W | U] -> cols [256, 512) (M = 64)
+    // ---- (7) (K/gamma)^T [W | U] -> cols [0, 256)
     if (tid == 0) {
 #pragma unroll
       for (int ks = 0; ks < kC / 16; ++ks)
-        ptx::mma_bf16_ss(tmem, umma::sdesc_mn(sKB, kC, ks), umma::sdesc_mn(sWU, kC, ks),
+        ptx::mma_bf16_ss(tmem, umma::sdesc_mn(sKH, 128, ks), umma::sdesc_mn(sWU, 128, ks),
                          umma::idesc_bf16_abmn(128, 256), ks > 0);
-#pragma unroll
-      for (int ks = 0; ks < kC / 16; ++ks)
-        ptx::mma_bf16_ss(tmem + 256, umma::sdesc_k(sMM, kC, ks), umma::sdesc_mn(sWU, kC, ks),
-                         umma::idesc_bf16_bmn(64, 256), ks > 0);
       ptx::mma_commit(bar);
     }
-    if (has_next) load_la(idx_next, I_2{}, I_3{});
     wait_mma(0x103u);
 
-    // ---- (8) Ap, Qp -> record tiles; B, O -> record directly
-    uint8_t *recg = ws + sizeof(WorkspaceHeader) + (size_t)idx * Rr::BYTES;
-    if (warp < 4) {
-      const int key = tid;                 // lanes of the M = 128 accumulator
-      const int rr = warp * 16 + lane;     // token rows of the M = 64 accumulator (lane < 16)
-#pragma unroll
-      for (int cb = 0; cb < D; cb += 16) {
-        float x[16], y[16], z[16], w[16];
-        ptx::tmem_ld16(t_lane + cb, x);          // Kbar^T W
-        ptx::tmem_ld16(t_lane + D + cb, y);      // Kbar^T U
-        ptx::tmem_ld16(t_lane + 256 + cb, z);    // M W
-        ptx::tmem_ld16(t_lane + 256 + D + cb, w);  // M U
+    // ---- (8) lane = key channel: Ap = -gamma_C (K/gamma)^T W (warps 0-3),
+    // B = gamma_C (K/gamma)^T U (warps 4-7), both straight to the record
+    {
+      const int key = quarter * 32 + lane;
+      const float gk = gcs[key];
+#pragma unroll 2
+      for (int h = 0; h < 8; ++h) {
+        const int cb = h * 16;
+        float x[16];
+        ptx::tmem_ld16(t_lane + colhalf * 128 + cb, x);
         ptx::tmem_ld_wait();
+        if (colhalf == 0) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) x[j] = -x[j];
-        st_chunk(sm + L::AP_S, key, cb >> 3, D, x);
-        st_chunk(sm + L::AP_S, key, (cb >> 3) + 1, D, x + 8);
-        const uint32_t blk = (uint32_t)(cb >> 5), cin = (uint32_t)(cb & 31);
-        uint4 *db = reinterpret_cast<uint4 *>(recg + Rr::BI + blk * (128u * 64u) + (uint32_t)key * 64u +
-                                              cin * 2u);
-        db[0] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
-                           pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
-        db[1] = make_uint4(pack_bf16x2(y[8], y[9]), pack_bf16x2(y[10], y[11]),
-                           pack_bf16x2(y[12], y[13]), pack_bf16x2(y[14], y[15]));
-        if (lane < 16) {
-          float qg[16];
-          ld_chunk(X1, kC + rr, cb >> 3, 128, qg);
-          ld_chunk(X1, kC + rr, (cb >> 3) + 1, 128, qg + 8);
+          for (int j = 0; j < 16; ++j) x[j] *= -gk;
+          *reinterpret_cast<uint4 *>(recg + Rr::AP + umma::sw128_chunk(key, cb >> 3, D)) = pack8(x);
+          *reinterpret_cast<uint4 *>(recg + Rr::AP + umma::sw128_chunk(key, (cb >> 3) + 1, D)) =
+              pack8(x + 8);
+        } else {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) qg[j] -= z[j];
-          st_chunk(sm + L::QP_S, rr, cb >> 3, kC, qg);
-          st_chunk(sm + L::QP_S, rr, (cb >> 3) + 1, kC, qg + 8);
-          uint4 *dq = reinterpret_cast<uint4 *>(recg + Rr::OI + blk * (uint32_t)(kC * 64) +
-                                                (uint32_t)rr * 64u + cin * 2u);
-          dq[0] = make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]),
-                             pack_bf16x2(w[4], w[5]), pack_bf16x2(w[6], w[7]));
-          dq[1] = make_uint4(pack_bf16x2(w[8], w[9]), pack_bf16x2(w[10], w[11]),
-                             pack_bf16x2(w[12], w[13]), pack_bf16x2(w[14], w[15]));
+          for (int j = 0; j < 16; ++j) x[j] *= gk;
+          uint4 *db = reinterpret_cast<uint4 *>(recg + Rr::BI + (uint32_t)(cb >> 5) * (128u * 64u) +
+                                                (uint32_t)key * 64u + (uint32_t)(cb & 31) * 2u);
+          db[0] = pack8(x);
+          db[1] = pack8(x + 8);
         }
       }
     }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+
+    // ---- (9) M [W | U] -> cols [0, 256), M = 64 layout
+    if (tid == 0) {
+#pragma unroll
+      for (int ks = 0; ks < kC / 16; ++ks)
+        ptx::mma_bf16_ss(tmem, umma::sdesc_k(sMM, kC, ks), umma::sdesc_mn(sWU, 128, ks),
+                         umma::idesc_bf16_bmn(64, 256), ks > 0);
+      ptx::mma_commit(bar);
+    }
+    wait_mma(0x104u);
+
+    // ---- (10) token rows: Qp = Q*gamma - M W (warps 0-3), O = M U (warps 4-7)
+    {
+      const int rr = quarter * 16 + lane;
+#pragma unroll 2
+      for (int h = 0; h < 8; ++h) {
+        const int cb = h * 16;
+        float x[16];
+        ptx::tmem_ld16(t_lane + colhalf * 128 + cb, x);
+        ptx::tmem_ld_wait();
+        if (lane < 16) {
+          if (colhalf == 0) {
+            float qg[16];
+            ld_chunk(X1, kC + rr, cb >> 3, 128, qg);
+            ld_chunk(X1, kC + rr, (cb >> 3) + 1, 128, qg + 8);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) qg[j] -= x[j];
+            *reinterpret_cast<uint4 *>(recg + Rr::QP + umma::sw128_chunk(rr, cb >> 3, kC)) = pack8(qg);
+            *reinterpret_cast<uint4 *>(recg + Rr::QP + umma::sw128_chunk(rr, (cb >> 3) + 1, kC)) =
+                pack8(qg + 8);
+          } else {
+            uint4 *dq = reinterpret_cast<uint4 *>(recg + Rr::OI + (uint32_t)(cb >> 5) * (uint32_t)(kC * 64) +
+                                                  (uint32_t)rr * 64u + (uint32_t)(cb & 31) * 2u);
+            dq[0] = pack8(x);
+            dq[1] = pack8(x + 8);
+          }
+        }
+      }
+    }
+    // X1 and the TMEM columns are free again: fetch the next chunk's rows
     ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
     __syncthreads();
-
-    // ---- (9) Ap, Qp, gamma_C -> record (bulk copies; read completion awaited
-    // before R_A, R_B and GC_S are written again)
-    if (tid == 0) {
-      ptx::bulk_s2g(recg + Rr::AP, sm + L::AP_S, 32768);
-      ptx::bulk_s2g(recg + Rr::QP, sm + L::QP_S, 16384);
-      ptx::bulk_s2g(recg + Rr::GC, sm + L::GC_S, D * 4);
-      ptx::bulk_commit();
-    }
+    ptx::tc_fence_after();
+    if (tid == 0 && idx + (int)gridDim.x < total) issue_raw(idx + (int)gridDim.x);
   }
-  if (tid == 0) ptx::bulk_wait_all();
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -1064,7 +1086,7 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
 }
 
 template <int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(256, D == 128 ? 2 : 1)
 kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                 const __nv_bfloat16 *__restrict__ v, const float *__restrict__ beta,
                 const float *__restrict__ log_alpha, int alpha_mode, int T, int NC, int total,
@@ -1575,7 +1597,8 @@ kda_status launch_d(const void *q, const void *k, const void *v, const float *be
       return KDA_ERR_CUDA;
     const long long total = (long long)BH * NC;
     if (total > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
-    const int grid = (int)(total < sms ? total : sms);  // persistent: one CTA per SM
+    const long long slots = (long long)sms * (D == 128 ? 2 : 1);  // persistent CTAs per SM
+    const int grid = (int)(total < slots ? total : slots);
     timer.mark();
     kda_prep_kernel<D><<<grid, 256, prep_smem, st>>>(
         static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
