@@ -689,12 +689,11 @@ __device__ __forceinline__ void prep_d64(const __nv_bfloat16 *__restrict__ q,
 // columns and at most 128 registers per thread each), so one CTA's MMA waits,
 // barriers and loads overlap the other's work.  Per chunk:
 //  (0) decay, one thread per key channel and half of the rows: g = running sum
-//      of -exp(log_alpha) read straight from global memory, gamma = exp(g) to
-//      a float tile; gamma_C to the record;
-//  (1) the chunk's q, k, v rows (bulk copies into the operand area) to
-//      registers, then one thread per (row, 8 channels) writes K_beta = beta K
-//      gamma, Q*gamma, beta V and K/gamma as natural (row = token) swizzled
-//      tiles over them;
+//      of -exp(log_alpha), gamma = exp(g) to a float tile over the
+//      log_alpha rows; gamma_C to the record;
+//  (1) the chunk's q, k, v rows to registers, then one thread per (row, 8
+//      channels) writes K_beta = beta K gamma, Q*gamma, beta V and K/gamma as
+//      natural (row = token) swizzled tiles over them;
 //  (2) [A; M] = [K_beta; Q*gamma] (K/gamma)^T        8 MMAs (M = 128, N = 64)
 //  (3) A to float;  (4) T = (I + A)^-1 (blocked), M to a bf16 tile in A's
 //      space while the last block of T is formed
@@ -706,15 +705,18 @@ __device__ __forceinline__ void prep_d64(const __nv_bfloat16 *__restrict__ q,
 //  (9) M [W | U]                                        4 MMAs (M = 64, N = 256)
 // (10) Qp = Q*gamma - M W and O = M U to the record.
 // Record tiles go to global memory straight from registers, already swizzled.
+// The next chunk's log_alpha, k and v rows are bulk-copied as soon as the last
+// product has read A's space and blocks 2-3 (after (9)), its q rows after (10).
 struct PrepSmem128 {
   using R = Rec<128>;
   static constexpr int D = 128;
   // X1: blocks 0-1 = [K_beta; Q*gamma] (128 rows x 128), blocks 2-3 = [beta V;
   // K/gamma]; rows 0-63 of the four blocks hold [W | U] (64 rows x 256) from
-  // phase 6 on.  Before phase 1 its first 48 KB receive the raw q | k | v rows.
+  // phase 6 on.  Before phase 1 blocks 0, 2 and 3 receive the raw q, k and v rows.
   static constexpr uint32_t X1 = 0;
-  static constexpr uint32_t RAW = X1;
-  // R_A: gamma as float [C][D] (phases 0-1) | A, T float (3-4) | M tile (4-9)
+  static constexpr uint32_t RAWQ = X1, RAWK = X1 + 32768, RAWV = X1 + 49152;
+  // R_A: log_alpha, then gamma, as float [C][D] (phases 0-1) | A, T float (3-4) |
+  // M tile (4-9)
   static constexpr uint32_t RA = X1 + 65536;
   static constexpr uint32_t EG = RA, AF = RA, TF = RA + kC * kLD * 4, MM = RA;
   static constexpr uint32_t TT = align1k(RA + 2 * kC * kLD * 4);  // T bf16; solve scratch before
@@ -722,8 +724,9 @@ struct PrepSmem128 {
   static constexpr uint32_t BETA = GCS + D * 4;      // float [C]
   static constexpr uint32_t PART = BETA + kC * 4;    // float [2][D]
   static constexpr uint32_t BAR = PART + 2 * D * 4;
-  static constexpr uint32_t LBAR = BAR + 8;
-  static constexpr uint32_t TMEMP = LBAR + 8;
+  static constexpr uint32_t LBAR = BAR + 8;   // log_alpha, k, v rows landed
+  static constexpr uint32_t QBAR = LBAR + 8;  // q rows landed
+  static constexpr uint32_t TMEMP = QBAR + 8;
   static constexpr uint32_t BYTES = TMEMP + 8;
   static constexpr uint32_t TMEM_COLS = 256;
   static_assert(kC * D * 4 <= 2 * kC * kLD * 4, "gamma tile fits R_A");
@@ -762,12 +765,13 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
   float *AF = reinterpret_cast<float *>(sm + L::AF);
   float *TF = reinterpret_cast<float *>(sm + L::TF);
   uint8_t *TT = sm + L::TT, *MM = sm + L::MM, *X1 = sm + L::X1;
-  uint8_t *rawq = sm + L::RAW, *rawk = rawq + kC * D * 2, *rawv = rawk + kC * D * 2;
+  const uint8_t *rawq = sm + L::RAWQ, *rawk = sm + L::RAWK, *rawv = sm + L::RAWV;
   float *gcs = reinterpret_cast<float *>(sm + L::GCS);
   float *betas = reinterpret_cast<float *>(sm + L::BETA);
   float *part = reinterpret_cast<float *>(sm + L::PART);
   uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::BAR);
   uint64_t *lbar = reinterpret_cast<uint64_t *>(sm + L::LBAR);
+  uint64_t *qbar = reinterpret_cast<uint64_t *>(sm + L::QBAR);
   uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(sm + L::TMEMP);
   WorkspaceHeader *hdr = reinterpret_cast<WorkspaceHeader *>(ws);
 
@@ -776,20 +780,35 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
   const int c = tid & (D - 1), half = tid >> 7, r0 = half * R;   // decay phase mapping
   bool ok = true;
 
-  auto issue_raw = [&](int idx) {
+  const bool la_bulk = alpha_mode == KDA_ALPHA_CHANNEL;  // per-channel rows: 512 B each
+  auto rows_of = [&](int idx, int &valid, size_t &row0) {
     const int t0 = (idx % NC) * kC;
-    const int valid = min(kC, T - t0);
-    const size_t row0 = (size_t)(idx / NC) * T + t0;
+    valid = min(kC, T - t0);
+    row0 = (size_t)(idx / NC) * T + t0;
+  };
+  auto issue_lkv = [&](int idx) {  // log_alpha -> R_A, k -> block 2, v -> block 3
+    int valid;
+    size_t row0;
+    rows_of(idx, valid, row0);
     const uint32_t bytes = (uint32_t)valid * D * 2;
-    ptx::mbar_arrive_expect_tx(lbar, 3 * bytes);
-    ptx::bulk_g2s(rawq, q + row0 * D, bytes, lbar);
-    ptx::bulk_g2s(rawk, k + row0 * D, bytes, lbar);
-    ptx::bulk_g2s(rawv, v + row0 * D, bytes, lbar);
+    ptx::mbar_arrive_expect_tx(lbar, 2 * bytes + (la_bulk ? 2 * bytes : 0u));
+    if (la_bulk) ptx::bulk_g2s(sm + L::EG, log_alpha + row0 * D, 2 * bytes, lbar);
+    ptx::bulk_g2s(sm + L::RAWK, k + row0 * D, bytes, lbar);
+    ptx::bulk_g2s(sm + L::RAWV, v + row0 * D, bytes, lbar);
+  };
+  auto issue_q = [&](int idx) {  // q -> block 0
+    int valid;
+    size_t row0;
+    rows_of(idx, valid, row0);
+    const uint32_t bytes = (uint32_t)valid * D * 2;
+    ptx::mbar_arrive_expect_tx(qbar, bytes);
+    ptx::bulk_g2s(sm + L::RAWQ, q + row0 * D, bytes, qbar);
   };
 
   if (tid == 0) {
     ptx::mbar_init(bar, 1);
     ptx::mbar_init(lbar, 1);
+    ptx::mbar_init(qbar, 1);
     ptx::fence_mbar_init();
   }
   if (warp == 0) {
@@ -804,7 +823,17 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
   const uint32_t sX1 = ptx::smem_u32(X1), sTT = ptx::smem_u32(TT), sMM = ptx::smem_u32(MM);
   const uint32_t sWU = sX1;                          // [W | U]: rows 0-63 of the four blocks
   const uint32_t sKH = sX1 + 32768 + kC * 128;       // K/gamma: rows 64-127 of blocks 2-3
-  if (tid == 0 && (int)blockIdx.x < total) issue_raw(blockIdx.x);
+  if (tid == 0 && (int)blockIdx.x < total) {
+    issue_lkv(blockIdx.x);
+    issue_q(blockIdx.x);
+  }
+  float b_next = 0.f;  // beta of the next chunk's row tid (tid < C)
+  if ((int)blockIdx.x < total && tid < kC) {
+    int valid;
+    size_t row0;
+    rows_of(blockIdx.x, valid, row0);
+    b_next = tid < valid ? beta[row0 + tid] : 0.f;
+  }
   uint32_t mma_phase = 0;
 
   auto wait_mma = [&](unsigned code) {
@@ -829,18 +858,25 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
     const size_t row0 = (size_t)(idx / NC) * T + t0;
     uint8_t *recg = ws + sizeof(WorkspaceHeader) + (size_t)idx * Rr::BYTES;
 
+    const int idx_next = idx + (int)gridDim.x;
+    const bool has_next = idx_next < total;
+
     // ---- (0) decay
+    if (tid < kC) betas[tid] = b_next;
+    if (ok && !ptx::mbar_wait(lbar, it & 1, kWaitLimit)) {
+      ok = false;
+      report_error(hdr, KDA_ERR_TIMEOUT, 0x100u);
+    }
     float ld[R];
 #pragma unroll
     for (int i = 0; i < R; ++i) {
       const int rr = min(r0 + i, valid - 1);
       ld[i] = 0.f;
-      if (alpha_mode == KDA_ALPHA_CHANNEL)
-        ld[i] = log_alpha[(row0 + rr) * D + c];
+      if (la_bulk)
+        ld[i] = EG[(r0 + i) * D + c];
       else if (alpha_mode == KDA_ALPHA_SCALAR)
         ld[i] = log_alpha[row0 + rr];
     }
-    if (tid < kC) betas[tid] = (tid < valid) ? beta[row0 + tid] : 0.f;
     float psum = 0.f;
 #pragma unroll
     for (int i = 0; i < R; ++i) {
@@ -863,9 +899,9 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
         reinterpret_cast<float *>(recg + Rr::GC)[c] = e;
       }
     }
-    if (ok && !ptx::mbar_wait(lbar, it & 1, kWaitLimit)) {
+    if (ok && !ptx::mbar_wait(qbar, it & 1, kWaitLimit)) {
       ok = false;
-      report_error(hdr, KDA_ERR_TIMEOUT, 0x100u);
+      report_error(hdr, KDA_ERR_TIMEOUT, 0x105u);
     }
     __syncthreads();
 
@@ -924,22 +960,19 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
     // ---- (3) lanes 0..63: A (strict lower) as float, 32 columns per warp
     if (quarter < 2) {
       const int r = quarter * 32 + lane;
+      const int cb = colhalf * 32;
+      float x[32];
+      ptx::tmem_ld32(t_lane + cb, x);
+      ptx::tmem_ld_wait();
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int cb = colhalf * 32 + h * 16;
-        float x[16];
-        ptx::tmem_ld16(t_lane + cb, x);
-        ptx::tmem_ld_wait();
-#pragma unroll
-        for (int j4 = 0; j4 < 4; ++j4) {
-          const int m0 = cb + 4 * j4;
-          float4 a;
-          a.x = (m0 + 0 < r) ? x[4 * j4 + 0] : 0.f;
-          a.y = (m0 + 1 < r) ? x[4 * j4 + 1] : 0.f;
-          a.z = (m0 + 2 < r) ? x[4 * j4 + 2] : 0.f;
-          a.w = (m0 + 3 < r) ? x[4 * j4 + 3] : 0.f;
-          *reinterpret_cast<float4 *>(AF + r * kLD + m0) = a;
-        }
+      for (int j4 = 0; j4 < 8; ++j4) {
+        const int m0 = cb + 4 * j4;
+        float4 a;
+        a.x = (m0 + 0 < r) ? x[4 * j4 + 0] : 0.f;
+        a.y = (m0 + 1 < r) ? x[4 * j4 + 1] : 0.f;
+        a.z = (m0 + 2 < r) ? x[4 * j4 + 2] : 0.f;
+        a.w = (m0 + 3 < r) ? x[4 * j4 + 3] : 0.f;
+        *reinterpret_cast<float4 *>(AF + r * kLD + m0) = a;
       }
     }
     __syncthreads();
@@ -949,17 +982,14 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
     blocked_unit_lower_inverse(AF, TF, TT, tid, [&]() {
       if (quarter >= 2) {
         const int r = quarter * 32 + lane - kC;
+        const int cb = colhalf * 32;
+        float x[32];
+        ptx::tmem_ld32(t_lane + cb, x);
+        ptx::tmem_ld_wait();
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int cb = colhalf * 32 + h * 16;
-          float x[16];
-          ptx::tmem_ld16(t_lane + cb, x);
-          ptx::tmem_ld_wait();
+        for (int j = 0; j < 32; ++j) x[j] = (cb + j <= r) ? x[j] : 0.f;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) x[j] = (cb + j <= r) ? x[j] : 0.f;
-          st_chunk(MM, r, cb >> 3, kC, x);
-          st_chunk(MM, r, (cb >> 3) + 1, kC, x + 8);
-        }
+        for (int j8 = 0; j8 < 4; ++j8) st_chunk(MM, r, (cb >> 3) + j8, kC, x + 8 * j8);
       }
     });
     sync_for_mma();
@@ -978,14 +1008,14 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
     {
       const int rr = quarter * 16 + lane;  // token row (lanes < 16 of the M = 64 layout)
 #pragma unroll
-      for (int h = 0; h < 8; ++h) {
-        const int cb = colhalf * 128 + h * 16;
-        float x[16];
-        ptx::tmem_ld16(t_lane + cb, x);
+      for (int h = 0; h < 4; ++h) {
+        const int cb = colhalf * 128 + h * 32;
+        float x[32];
+        ptx::tmem_ld32(t_lane + cb, x);
         ptx::tmem_ld_wait();
         if (lane < 16) {
-          st_chunk(X1, rr, cb >> 3, 128, x);
-          st_chunk(X1, rr, (cb >> 3) + 1, 128, x + 8);
+#pragma unroll
+          for (int j8 = 0; j8 < 4; ++j8) st_chunk(X1, rr, (cb >> 3) + j8, 128, x + 8 * j8);
         }
       }
     }
@@ -1005,26 +1035,25 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
     // B = gamma_C (K/gamma)^T U (warps 4-7), both straight to the record
     {
       const int key = quarter * 32 + lane;
-      const float gk = gcs[key];
-#pragma unroll 2
-      for (int h = 0; h < 8; ++h) {
-        const int cb = h * 16;
-        float x[16];
-        ptx::tmem_ld16(t_lane + colhalf * 128 + cb, x);
+      const float gk = colhalf == 0 ? -gcs[key] : gcs[key];
+#pragma unroll 1
+      for (int h = 0; h < 4; ++h) {
+        const int cb = h * 32;
+        float x[32];
+        ptx::tmem_ld32(t_lane + colhalf * 128 + cb, x);
         ptx::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] *= gk;
         if (colhalf == 0) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) x[j] *= -gk;
-          *reinterpret_cast<uint4 *>(recg + Rr::AP + umma::sw128_chunk(key, cb >> 3, D)) = pack8(x);
-          *reinterpret_cast<uint4 *>(recg + Rr::AP + umma::sw128_chunk(key, (cb >> 3) + 1, D)) =
-              pack8(x + 8);
+          for (int j8 = 0; j8 < 4; ++j8)
+            *reinterpret_cast<uint4 *>(recg + Rr::AP + umma::sw128_chunk(key, (cb >> 3) + j8, D)) =
+                pack8(x + 8 * j8);
         } else {
+          uint4 *db = reinterpret_cast<uint4 *>(recg + Rr::BI + (uint32_t)h * (128u * 64u) +
+                                                (uint32_t)key * 64u);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) x[j] *= gk;
-          uint4 *db = reinterpret_cast<uint4 *>(recg + Rr::BI + (uint32_t)(cb >> 5) * (128u * 64u) +
-                                                (uint32_t)key * 64u + (uint32_t)(cb & 31) * 2u);
-          db[0] = pack8(x);
-          db[1] = pack8(x + 8);
+          for (int j8 = 0; j8 < 4; ++j8) db[j8] = pack8(x + 8 * j8);
         }
       }
     }
@@ -1041,41 +1070,52 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
       ptx::mma_commit(bar);
     }
     wait_mma(0x104u);
+    // A's space and blocks 2-3 are free: fetch the next chunk's log_alpha, k, v
+    if (has_next) {
+      if (tid == 0) issue_lkv(idx_next);
+      if (tid < kC) {
+        int vn;
+        size_t rn;
+        rows_of(idx_next, vn, rn);
+        b_next = tid < vn ? beta[rn + tid] : 0.f;
+      }
+    }
 
     // ---- (10) token rows: Qp = Q*gamma - M W (warps 0-3), O = M U (warps 4-7)
     {
       const int rr = quarter * 16 + lane;
-#pragma unroll 2
-      for (int h = 0; h < 8; ++h) {
-        const int cb = h * 16;
-        float x[16];
-        ptx::tmem_ld16(t_lane + colhalf * 128 + cb, x);
+#pragma unroll 1
+      for (int h = 0; h < 4; ++h) {
+        const int cb = h * 32;
+        float x[32];
+        ptx::tmem_ld32(t_lane + colhalf * 128 + cb, x);
         ptx::tmem_ld_wait();
         if (lane < 16) {
           if (colhalf == 0) {
-            float qg[16];
-            ld_chunk(X1, kC + rr, cb >> 3, 128, qg);
-            ld_chunk(X1, kC + rr, (cb >> 3) + 1, 128, qg + 8);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) qg[j] -= x[j];
-            *reinterpret_cast<uint4 *>(recg + Rr::QP + umma::sw128_chunk(rr, cb >> 3, kC)) = pack8(qg);
-            *reinterpret_cast<uint4 *>(recg + Rr::QP + umma::sw128_chunk(rr, (cb >> 3) + 1, kC)) =
-                pack8(qg + 8);
+            for (int j8 = 0; j8 < 4; ++j8) {
+              float qg[8];
+              ld_chunk(X1, kC + rr, (cb >> 3) + j8, 128, qg);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) qg[j] -= x[8 * j8 + j];
+              *reinterpret_cast<uint4 *>(recg + Rr::QP + umma::sw128_chunk(rr, (cb >> 3) + j8, kC)) =
+                  pack8(qg);
+            }
           } else {
-            uint4 *dq = reinterpret_cast<uint4 *>(recg + Rr::OI + (uint32_t)(cb >> 5) * (uint32_t)(kC * 64) +
-                                                  (uint32_t)rr * 64u + (uint32_t)(cb & 31) * 2u);
-            dq[0] = pack8(x);
-            dq[1] = pack8(x + 8);
+            uint4 *dq = reinterpret_cast<uint4 *>(recg + Rr::OI + (uint32_t)h * (uint32_t)(kC * 64) +
+                                                  (uint32_t)rr * 64u);
+#pragma unroll
+            for (int j8 = 0; j8 < 4; ++j8) dq[j8] = pack8(x + 8 * j8);
           }
         }
       }
     }
-    // X1 and the TMEM columns are free again: fetch the next chunk's rows
+    // block 0 and the TMEM columns are free again: fetch the next chunk's q rows
     ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    if (tid == 0 && idx + (int)gridDim.x < total) issue_raw(idx + (int)gridDim.x);
+    if (tid == 0 && has_next) issue_q(idx_next);
   }
   ptx::tc_fence_before();
   __syncthreads();
