@@ -1032,31 +1032,63 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
     wait_mma(0x103u);
 
     // ---- (8) lane = key channel: Ap = -gamma_C (K/gamma)^T W (warps 0-3),
-    // B = gamma_C (K/gamma)^T U (warps 4-7), both straight to the record
+    // B = gamma_C (K/gamma)^T U (warps 4-7).  A warp's rows form contiguous
+    // pieces of the record (4 KB of Ap per K atom, 2 KB of B per 32-column
+    // block): each piece is assembled in a per-warp staging slot (the consumed
+    // K/gamma rows, the T tile) and leaves with 512-byte coalesced stores.
     {
       const int key = quarter * 32 + lane;
       const float gk = colhalf == 0 ? -gcs[key] : gcs[key];
+      if (colhalf == 0) {
+        uint8_t *stg = X1 + 32768 + (quarter >> 1) * 16384 + kC * 128 + (quarter & 1) * 4096;
 #pragma unroll 1
-      for (int h = 0; h < 4; ++h) {
-        const int cb = h * 32;
-        float x[32];
-        ptx::tmem_ld32(t_lane + colhalf * 128 + cb, x);
-        ptx::tmem_ld_wait();
+        for (int a = 0; a < 2; ++a) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] *= gk;
-        if (colhalf == 0) {
+          for (int hh = 0; hh < 2; ++hh) {
+            float x[32];
+            ptx::tmem_ld32(t_lane + a * 64 + hh * 32, x);
+            ptx::tmem_ld_wait();
 #pragma unroll
-          for (int j8 = 0; j8 < 4; ++j8)
-            *reinterpret_cast<uint4 *>(recg + Rr::AP + umma::sw128_chunk(key, (cb >> 3) + j8, D)) =
+            for (int j = 0; j < 32; ++j) x[j] *= gk;
+#pragma unroll
+            for (int j8 = 0; j8 < 4; ++j8)  // same swizzle as the record tile (rows 32q + lane)
+              *reinterpret_cast<uint4 *>(stg + lane * 128 + (((hh * 4 + j8) ^ (lane & 7)) << 4)) =
+                  pack8(x + 8 * j8);
+          }
+          __syncwarp();
+          uint8_t *dst = recg + Rr::AP + a * (D * 128) + quarter * 4096;
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            *reinterpret_cast<uint4 *>(dst + i * 512 + lane * 16) =
+                *reinterpret_cast<const uint4 *>(stg + i * 512 + lane * 16);
+          __syncwarp();
+        }
+      } else {
+        uint8_t *stg = TT + quarter * 2048;
+#pragma unroll 1
+        for (int h = 0; h < 4; ++h) {
+          float x[32];
+          ptx::tmem_ld32(t_lane + 128 + h * 32, x);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) x[j] *= gk;
+#pragma unroll
+          for (int j8 = 0; j8 < 4; ++j8)  // 64-byte rows, chunks rotated for conflict-free writes
+            *reinterpret_cast<uint4 *>(stg + lane * 64 + ((j8 ^ ((lane >> 1) & 3)) << 4)) =
                 pack8(x + 8 * j8);
-        } else {
-          uint4 *db = reinterpret_cast<uint4 *>(recg + Rr::BI + (uint32_t)h * (128u * 64u) +
-                                                (uint32_t)key * 64u);
+          __syncwarp();
+          uint8_t *dst = recg + Rr::BI + h * (128 * 64) + quarter * 2048;
 #pragma unroll
-          for (int j8 = 0; j8 < 4; ++j8) db[j8] = pack8(x + 8 * j8);
+          for (int i = 0; i < 4; ++i) {
+            const int p = i * 512 + lane * 16, R = p >> 6, j = ((p >> 4) & 3) ^ ((R >> 1) & 3);
+            *reinterpret_cast<uint4 *>(dst + R * 64 + j * 16) =
+                *reinterpret_cast<const uint4 *>(stg + p);
+          }
+          __syncwarp();
         }
       }
     }
+    ptx::fence_proxy_async_smem();  // staging slots are bulk-copy targets later
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -1081,32 +1113,62 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
       }
     }
 
-    // ---- (10) token rows: Qp = Q*gamma - M W (warps 0-3), O = M U (warps 4-7)
+    // ---- (10) token rows (lanes < 16): Qp = Q*gamma - M W (warps 0-3), O = M U
+    // (warps 4-7); staged per warp (the consumed W rows, the T tile) as in (8):
+    // 2 KB of Qp per K atom, 1 KB of O per 32-column block
     {
       const int rr = quarter * 16 + lane;
+      if (colhalf == 0) {
+        uint8_t *stg = X1 + quarter * 2048;
 #pragma unroll 1
-      for (int h = 0; h < 4; ++h) {
-        const int cb = h * 32;
-        float x[32];
-        ptx::tmem_ld32(t_lane + colhalf * 128 + cb, x);
-        ptx::tmem_ld_wait();
-        if (lane < 16) {
-          if (colhalf == 0) {
+        for (int a = 0; a < 2; ++a) {
 #pragma unroll
-            for (int j8 = 0; j8 < 4; ++j8) {
-              float qg[8];
-              ld_chunk(X1, kC + rr, (cb >> 3) + j8, 128, qg);
+          for (int hh = 0; hh < 2; ++hh) {
+            float x[32];
+            ptx::tmem_ld32(t_lane + a * 64 + hh * 32, x);
+            ptx::tmem_ld_wait();
+            if (lane < 16) {
 #pragma unroll
-              for (int j = 0; j < 8; ++j) qg[j] -= x[8 * j8 + j];
-              *reinterpret_cast<uint4 *>(recg + Rr::QP + umma::sw128_chunk(rr, (cb >> 3) + j8, kC)) =
-                  pack8(qg);
+              for (int j8 = 0; j8 < 4; ++j8) {
+                const int cc = hh * 4 + j8;
+                float qg[8];
+                ld_chunk(X1, kC + rr, a * 8 + cc, 128, qg);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) qg[j] -= x[8 * j8 + j];
+                *reinterpret_cast<uint4 *>(stg + lane * 128 + ((cc ^ (lane & 7)) << 4)) = pack8(qg);
+              }
             }
-          } else {
-            uint4 *dq = reinterpret_cast<uint4 *>(recg + Rr::OI + (uint32_t)h * (uint32_t)(kC * 64) +
-                                                  (uint32_t)rr * 64u);
-#pragma unroll
-            for (int j8 = 0; j8 < 4; ++j8) dq[j8] = pack8(x + 8 * j8);
           }
+          __syncwarp();
+          uint8_t *dst = recg + Rr::QP + a * (kC * 128) + quarter * 2048;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<uint4 *>(dst + i * 512 + lane * 16) =
+                *reinterpret_cast<const uint4 *>(stg + i * 512 + lane * 16);
+          __syncwarp();
+        }
+      } else {
+        uint8_t *stg = TT + quarter * 1024;
+#pragma unroll 1
+        for (int h = 0; h < 4; ++h) {
+          float x[32];
+          ptx::tmem_ld32(t_lane + 128 + h * 32, x);
+          ptx::tmem_ld_wait();
+          if (lane < 16) {
+#pragma unroll
+            for (int j8 = 0; j8 < 4; ++j8)
+              *reinterpret_cast<uint4 *>(stg + lane * 64 + ((j8 ^ ((lane >> 1) & 3)) << 4)) =
+                  pack8(x + 8 * j8);
+          }
+          __syncwarp();
+          uint8_t *dst = recg + Rr::OI + h * (kC * 64) + quarter * 1024;
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int p = i * 512 + lane * 16, R = p >> 6, j = ((p >> 4) & 3) ^ ((R >> 1) & 3);
+            *reinterpret_cast<uint4 *>(dst + R * 64 + j * 16) =
+                *reinterpret_cast<const uint4 *>(stg + p);
+          }
+          __syncwarp();
         }
       }
     }
