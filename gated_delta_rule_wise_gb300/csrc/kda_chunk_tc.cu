@@ -157,20 +157,23 @@ __device__ __forceinline__ void fma4(float4 &acc, float a, const float4 &b) {
 }
 
 // T = (I + A)^-1 for the strictly lower A (float, row stride kLD), in blocks
-// of 16.  The diagonal blocks by right-looking forward substitution (one
-// column per thread, partial sums in registers); then, right-looking over the
-// block columns, S_ij accumulates A_im T_mj as soon as T_mj exists and
-// T_ij = -T_ii S_ij, every block product done by 64 threads on 1 x 4 strips.
+// of 16: T_ij = -T_ii sum_{m=j..i-1} A_im T_mj.  The diagonal blocks by
+// forward substitution (one column per thread, partial sums in registers);
+// then G_im = T_ii A_im for the six blocks below the diagonal at once, and
+// T_ij = -sum_m G_im T_mj along the block subdiagonals (three blocks, then
+// two, then one), every block product done by 64 threads on 1 x 4 strips.
 // The float row stride kLD = C + 4 keeps column reads across rows and 16-byte
 // row accesses free of bank conflicts, and lets every inner-loop address be an
 // immediate offset.  Leaves T (float, lower blocks) in TF and the bf16 K-major
 // [C][C] tile of T (zeros above the diagonal) in TT.  All 256 threads call
-// it; XS (6 x 256 floats) is scratch inside TT.
+// it; G (6 blocks, rows kGLD floats apart) is scratch inside TT.
 // `late` runs on threads 64..255 while threads 0..63 form the last block of
 // T, after the last read of AF: the caller may reuse AF's space there.
 struct NoLateWork {
   __device__ void operator()() const {}
 };
+constexpr int kGLD = 20;  // row stride (floats) of the G blocks: row reads conflict-free
+static_assert(6 * 16 * kGLD * 4 <= kC * kC * 2, "G scratch fits the T tile");
 template <class Late = NoLateWork>
 __device__ __forceinline__ void blocked_unit_lower_inverse(const float *AF, float *TF, uint8_t *TT,
                                                            int tid, const Late &late = Late()) {
@@ -193,66 +196,55 @@ __device__ __forceinline__ void blocked_unit_lower_inverse(const float *AF, floa
   }
   __syncthreads();
   const int r = (tid & 63) >> 2, c0 = (tid & 3) * 4, g = tid >> 6;
-  // out (+)= L (16 x 16, rows li.., cols lj..) * R (16 x 16 at rows ri.., cols rj..)
-  auto strip = [&](const float *Lm, int li, int lj, const float *Rm, int ri, int rj) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float *lrow = Lm + (li + r) * kLD + lj;
-    const float *rcol = Rm + ri * kLD + rj + c0;
+  // acc += sum_s L[r][s] R[s][c0..c0+3] over one 16 x 16 block pair
+  auto strip = [&](float4 &acc, const float *lrow, const float *rblk) {
 #pragma unroll
     for (int s2 = 0; s2 < 16; ++s2)
-      fma4(acc, lrow[s2], *reinterpret_cast<const float4 *>(rcol + s2 * kLD));
-    return acc;
+      fma4(acc, lrow[s2], *reinterpret_cast<const float4 *>(rblk + s2 * kLD + c0));
   };
-  auto xs = [&](int slot) -> float4 & { return *reinterpret_cast<float4 *>(XS + slot * 256 + r * 16 + c0); };
-  auto tf = [&](int bi, int bj) -> float4 & {
-    return *reinterpret_cast<float4 *>(TF + (bi * 16 + r) * kLD + bj * 16 + c0);
+  auto gs = [&](int slot) { return XS + slot * 16 * kGLD + r * kGLD; };  // row r of G slot
+  auto tb = [&](int bi, int bj) { return TF + (bi * 16) * kLD + bj * 16; };  // block (bi, bj)
+  auto put = [&](int bi, int bj, const float4 &acc) {
+    *reinterpret_cast<float4 *>(TF + (bi * 16 + r) * kLD + bj * 16 + c0) =
+        make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
   };
-  auto neg_tii_x = [&](int bi, int bj, int slot) {  // T_ij = -T_ii S_ij
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float *trow = TF + (bi * 16 + r) * kLD + bi * 16;
-    const float *xcol = XS + slot * 256 + c0;
-#pragma unroll
-    for (int s2 = 0; s2 < 16; ++s2) fma4(acc, trow[s2], *reinterpret_cast<const float4 *>(xcol + s2 * 16));
-    tf(bi, bj) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-  };
-  // S_ij = A_ij T_jj for the six blocks below the diagonal (slots 0..5:
-  // (1,0) (2,1) (3,2) (2,0) (3,1) (3,0))
+  // G_im = T_ii A_im, slots 0..5: (1,0) (2,1) (3,2) (2,0) (3,1) (3,0)
   for (int w = tid; w < 6 * 64; w += 256) {
     const int sl = w >> 6;
     const int bi = sl < 3 ? sl + 1 : (sl == 5 ? 3 : sl - 1);
     const int bj = sl < 3 ? sl : (sl == 5 ? 0 : sl - 3);
     const int rr = (w & 63) >> 2, cc = (w & 3) * 4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float *lrow = AF + (bi * 16 + rr) * kLD + bj * 16;
-    const float *rcol = TF + (bj * 16) * kLD + bj * 16 + cc;
+    const float *lrow = TF + (bi * 16 + rr) * kLD + bi * 16;
+    const float *rblk = AF + (bi * 16) * kLD + bj * 16 + cc;
 #pragma unroll
     for (int s2 = 0; s2 < 16; ++s2)
-      fma4(acc, lrow[s2], *reinterpret_cast<const float4 *>(rcol + s2 * kLD));
-    *reinterpret_cast<float4 *>(XS + sl * 256 + rr * 16 + cc) = acc;
+      fma4(acc, lrow[s2], *reinterpret_cast<const float4 *>(rblk + s2 * kLD));
+    *reinterpret_cast<float4 *>(XS + sl * 16 * kGLD + rr * kGLD + cc) = acc;
   }
   __syncthreads();
-  if (g < 3) neg_tii_x(g + 1, g, g);                 // T_10, T_21, T_32
-  __syncthreads();
-  if (g < 3) {                                        // S_20 += A_21 T_10; S_31 += A_32 T_21; S_30 += A_31 T_10
-    const int sl = 3 + g;
-    const int bi = g == 0 ? 2 : 3, bm = g == 0 ? 1 : (g == 1 ? 2 : 1), bj = g == 1 ? 1 : 0;
-    const float4 a = strip(AF, bi * 16, bm * 16, TF, bm * 16, bj * 16);
-    float4 &x = xs(sl);
-    x.x += a.x; x.y += a.y; x.z += a.z; x.w += a.w;
+  if (g < 3) {                                   // T_10, T_21, T_32 = -G_(i+1)i T_ii
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    strip(acc, gs(g), tb(g, g));
+    put(g + 1, g, acc);
   }
   __syncthreads();
-  if (g < 2) neg_tii_x(g + 2, g, 3 + g);             // T_20, T_31
-  __syncthreads();
-  if (g == 0) {                                       // S_30 += A_32 T_20
-    const float4 a = strip(AF, 48, 32, TF, 32, 0);
-    float4 &x = xs(5);
-    x.x += a.x; x.y += a.y; x.z += a.z; x.w += a.w;
+  if (g < 2) {                                   // T_20, T_31 = -(G_(i+2)i T_ii + G_(i+2)(i+1) T_(i+1)i)
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    strip(acc, gs(3 + g), tb(g, g));
+    strip(acc, gs(1 + g), tb(g + 1, g));
+    put(g + 2, g, acc);
   }
   __syncthreads();
-  if (g == 0)
-    neg_tii_x(3, 0, 5);                               // T_30
-  else
+  if (g == 0) {                                  // T_30 = -(G_30 T_00 + G_31 T_10 + G_32 T_20)
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    strip(acc, gs(5), tb(0, 0));
+    strip(acc, gs(4), tb(1, 0));
+    strip(acc, gs(2), tb(2, 0));
+    put(3, 0, acc);
+  } else {
     late();
+  }
   __syncthreads();
   for (int u = tid; u < kC * 8; u += 256) {  // bf16 operand tile, zeros above the diagonal blocks
     const int row = u >> 3, c8 = u & 7;
@@ -868,14 +860,13 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
       report_error(hdr, KDA_ERR_TIMEOUT, 0x100u);
     }
     float ld[R];
+    if (la_bulk) {  // one straight run of shared loads
 #pragma unroll
-    for (int i = 0; i < R; ++i) {
-      const int rr = min(r0 + i, valid - 1);
-      ld[i] = 0.f;
-      if (la_bulk)
-        ld[i] = EG[(r0 + i) * D + c];
-      else if (alpha_mode == KDA_ALPHA_SCALAR)
-        ld[i] = log_alpha[row0 + rr];
+      for (int i = 0; i < R; ++i) ld[i] = EG[(r0 + i) * D + c];
+    } else {
+#pragma unroll
+      for (int i = 0; i < R; ++i)
+        ld[i] = alpha_mode == KDA_ALPHA_SCALAR ? log_alpha[row0 + min(r0 + i, valid - 1)] : 0.f;
     }
     float psum = 0.f;
 #pragma unroll
@@ -1008,14 +999,17 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
     {
       const int rr = quarter * 16 + lane;  // token row (lanes < 16 of the M = 64 layout)
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const int cb = colhalf * 128 + h * 32;
-        float x[32];
+      for (int h = 0; h < 2; ++h) {
+        const int cb = colhalf * 128 + h * 64;
+        float x[32], y[32];
         ptx::tmem_ld32(t_lane + cb, x);
+        ptx::tmem_ld32(t_lane + cb + 32, y);
         ptx::tmem_ld_wait();
         if (lane < 16) {
 #pragma unroll
           for (int j8 = 0; j8 < 4; ++j8) st_chunk(X1, rr, (cb >> 3) + j8, 128, x + 8 * j8);
+#pragma unroll
+          for (int j8 = 0; j8 < 4; ++j8) st_chunk(X1, rr, (cb >> 3) + 4 + j8, 128, y + 8 * j8);
         }
       }
     }
@@ -1043,18 +1037,15 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
         uint8_t *stg = X1 + 32768 + (quarter >> 1) * 16384 + kC * 128 + (quarter & 1) * 4096;
 #pragma unroll 1
         for (int a = 0; a < 2; ++a) {
+          float x[64];
+          ptx::tmem_ld32(t_lane + a * 64, *reinterpret_cast<float(*)[32]>(x));
+          ptx::tmem_ld32(t_lane + a * 64 + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+          ptx::tmem_ld_wait();
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            float x[32];
-            ptx::tmem_ld32(t_lane + a * 64 + hh * 32, x);
-            ptx::tmem_ld_wait();
+          for (int j = 0; j < 64; ++j) x[j] *= gk;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) x[j] *= gk;
-#pragma unroll
-            for (int j8 = 0; j8 < 4; ++j8)  // same swizzle as the record tile (rows 32q + lane)
-              *reinterpret_cast<uint4 *>(stg + lane * 128 + (((hh * 4 + j8) ^ (lane & 7)) << 4)) =
-                  pack8(x + 8 * j8);
-          }
+          for (int j8 = 0; j8 < 8; ++j8)  // same swizzle as the record tile (rows 32q + lane)
+            *reinterpret_cast<uint4 *>(stg + lane * 128 + ((j8 ^ (lane & 7)) << 4)) = pack8(x + 8 * j8);
           __syncwarp();
           uint8_t *dst = recg + Rr::AP + a * (D * 128) + quarter * 4096;
 #pragma unroll
@@ -1066,25 +1057,29 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
       } else {
         uint8_t *stg = TT + quarter * 2048;
 #pragma unroll 1
-        for (int h = 0; h < 4; ++h) {
-          float x[32];
-          ptx::tmem_ld32(t_lane + 128 + h * 32, x);
+        for (int h2 = 0; h2 < 2; ++h2) {
+          float x[64];
+          ptx::tmem_ld32(t_lane + 128 + h2 * 64, *reinterpret_cast<float(*)[32]>(x));
+          ptx::tmem_ld32(t_lane + 128 + h2 * 64 + 32, *reinterpret_cast<float(*)[32]>(x + 32));
           ptx::tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) x[j] *= gk;
+          for (int j = 0; j < 64; ++j) x[j] *= gk;
 #pragma unroll
-          for (int j8 = 0; j8 < 4; ++j8)  // 64-byte rows, chunks rotated for conflict-free writes
-            *reinterpret_cast<uint4 *>(stg + lane * 64 + ((j8 ^ ((lane >> 1) & 3)) << 4)) =
-                pack8(x + 8 * j8);
-          __syncwarp();
-          uint8_t *dst = recg + Rr::BI + h * (128 * 64) + quarter * 2048;
+          for (int hb = 0; hb < 2; ++hb) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int p = i * 512 + lane * 16, R = p >> 6, j = ((p >> 4) & 3) ^ ((R >> 1) & 3);
-            *reinterpret_cast<uint4 *>(dst + R * 64 + j * 16) =
-                *reinterpret_cast<const uint4 *>(stg + p);
+            for (int j8 = 0; j8 < 4; ++j8)  // 64-byte rows, chunks rotated for conflict-free writes
+              *reinterpret_cast<uint4 *>(stg + lane * 64 + ((j8 ^ ((lane >> 1) & 3)) << 4)) =
+                  pack8(x + 32 * hb + 8 * j8);
+            __syncwarp();
+            uint8_t *dst = recg + Rr::BI + (h2 * 2 + hb) * (128 * 64) + quarter * 2048;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int p = i * 512 + lane * 16, R = p >> 6, j = ((p >> 4) & 3) ^ ((R >> 1) & 3);
+              *reinterpret_cast<uint4 *>(dst + R * 64 + j * 16) =
+                  *reinterpret_cast<const uint4 *>(stg + p);
+            }
+            __syncwarp();
           }
-          __syncwarp();
         }
       }
     }
@@ -1122,21 +1117,18 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
         uint8_t *stg = X1 + quarter * 2048;
 #pragma unroll 1
         for (int a = 0; a < 2; ++a) {
+          float x[64];
+          ptx::tmem_ld32(t_lane + a * 64, *reinterpret_cast<float(*)[32]>(x));
+          ptx::tmem_ld32(t_lane + a * 64 + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+          ptx::tmem_ld_wait();
+          if (lane < 16) {
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            float x[32];
-            ptx::tmem_ld32(t_lane + a * 64 + hh * 32, x);
-            ptx::tmem_ld_wait();
-            if (lane < 16) {
+            for (int cc = 0; cc < 8; ++cc) {
+              float qg[8];
+              ld_chunk(X1, kC + rr, a * 8 + cc, 128, qg);
 #pragma unroll
-              for (int j8 = 0; j8 < 4; ++j8) {
-                const int cc = hh * 4 + j8;
-                float qg[8];
-                ld_chunk(X1, kC + rr, a * 8 + cc, 128, qg);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) qg[j] -= x[8 * j8 + j];
-                *reinterpret_cast<uint4 *>(stg + lane * 128 + ((cc ^ (lane & 7)) << 4)) = pack8(qg);
-              }
+              for (int j = 0; j < 8; ++j) qg[j] -= x[8 * cc + j];
+              *reinterpret_cast<uint4 *>(stg + lane * 128 + ((cc ^ (lane & 7)) << 4)) = pack8(qg);
             }
           }
           __syncwarp();
@@ -1150,25 +1142,29 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
       } else {
         uint8_t *stg = TT + quarter * 1024;
 #pragma unroll 1
-        for (int h = 0; h < 4; ++h) {
-          float x[32];
-          ptx::tmem_ld32(t_lane + 128 + h * 32, x);
+        for (int h2 = 0; h2 < 2; ++h2) {
+          float x[64];
+          ptx::tmem_ld32(t_lane + 128 + h2 * 64, *reinterpret_cast<float(*)[32]>(x));
+          ptx::tmem_ld32(t_lane + 128 + h2 * 64 + 32, *reinterpret_cast<float(*)[32]>(x + 32));
           ptx::tmem_ld_wait();
-          if (lane < 16) {
 #pragma unroll
-            for (int j8 = 0; j8 < 4; ++j8)
-              *reinterpret_cast<uint4 *>(stg + lane * 64 + ((j8 ^ ((lane >> 1) & 3)) << 4)) =
-                  pack8(x + 8 * j8);
-          }
-          __syncwarp();
-          uint8_t *dst = recg + Rr::OI + h * (kC * 64) + quarter * 1024;
+          for (int hb = 0; hb < 2; ++hb) {
+            if (lane < 16) {
 #pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            const int p = i * 512 + lane * 16, R = p >> 6, j = ((p >> 4) & 3) ^ ((R >> 1) & 3);
-            *reinterpret_cast<uint4 *>(dst + R * 64 + j * 16) =
-                *reinterpret_cast<const uint4 *>(stg + p);
+              for (int j8 = 0; j8 < 4; ++j8)
+                *reinterpret_cast<uint4 *>(stg + lane * 64 + ((j8 ^ ((lane >> 1) & 3)) << 4)) =
+                    pack8(x + 32 * hb + 8 * j8);
+            }
+            __syncwarp();
+            uint8_t *dst = recg + Rr::OI + (h2 * 2 + hb) * (kC * 64) + quarter * 1024;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const int p = i * 512 + lane * 16, R = p >> 6, j = ((p >> 4) & 3) ^ ((R >> 1) & 3);
+              *reinterpret_cast<uint4 *>(dst + R * 64 + j * 16) =
+                  *reinterpret_cast<const uint4 *>(stg + p);
+            }
+            __syncwarp();
           }
-          __syncwarp();
         }
       }
     }
