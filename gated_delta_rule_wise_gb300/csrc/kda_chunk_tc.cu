@@ -1216,10 +1216,10 @@ struct ScanSmem64 {
 };
 
 // D = 128: three warp groups.  A producer warp streams records through a ring
-// of kStages stages.  Four state warps (TMEM lane = key channel) own S: per
-// chunk they wait for the previous state products, read S, write its bf16
-// copy (row-major, read MN-major by the MMA) and gamma_C * S + Kbar^T U back
-// to TMEM; then one of them issues S += Ap S (8 MMAs).  Four output warps
+// of kStages stages.  Four state warps own S (thread = key channel, its row in
+// registers as float): per chunk they write its bf16 copy (row-major, read
+// MN-major by the MMA), one of them issues P = Ap S into TMEM (8 MMAs), and
+// they form gamma_C * S + Kbar^T U while it runs, then add P.  Four output warps
 // (same TMEM lane quarters) issue o = Qp S into one of two output
 // accumulators as soon as the bf16 copy exists, wait for it, add M U and store
 // o.  Only the state products and the state conversion are on the serial
@@ -1360,91 +1360,79 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
     }
   } else {
     // ---------------------------------------------------------- state warps
+    // Thread r keeps row r of S (key channel r, this CTA's NB value columns)
+    // in registers as float.  Per chunk: its bf16 copy goes to the operand
+    // buffer, one thread issues P = Ap S into TMEM, and while the product
+    // runs each thread forms gamma_C S + B; then S <- that + P.
     const int r = tid;  // key channel = TMEM lane
-    const uint32_t tS = t_lane;
+    const uint32_t tP = t_lane;
+    float sr[NB];
     {
-      const size_t s0 = (size_t)bh * D * D;
+      const size_t s0 = (size_t)bh * D * D + (size_t)r * D + j0;
 #pragma unroll
-      for (int cb = 0; cb < NB; cb += 16) {
-        float x[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) x[j] = h0 ? h0[s0 + (size_t)r * D + j0 + cb + j] : 0.f;
-        ptx::tmem_st16(tS + cb, x);
-      }
-      ptx::tmem_st_wait();
+      for (int j = 0; j < NB; ++j) sr[j] = h0 ? h0[s0 + j] : 0.f;
     }
     for (int i = 0; i < NC; ++i) {
       const int s = i % kStages;
       uint8_t *st = sm + s * L::STAGE;
       uint8_t *sb = sb_of(i);
-      if (i > 0 && ok && !ptx::mbar_wait(mS, (i - 1) & 1, kWaitLimit)) {
-        ok = false;
-        report_error(hdr, KDA_ERR_TIMEOUT, 0x201u);
-      }
       if (i > 1 && ok && !ptx::mbar_wait(&mO[i & 1], ((i - 2) >> 1) & 1, kWaitLimit)) {
         ok = false;  // the bf16 copy of chunk i-2 has been read by its output products
         report_error(hdr, KDA_ERR_TIMEOUT, 0x203u);
       }
-      ptx::tc_fence_after();
       if (ok && !ptx::mbar_wait(&full[s], (i / kStages) & 1, kWaitLimit)) {
         ok = false;
         report_error(hdr, KDA_ERR_TIMEOUT, 0x202u);
       }
-      {  // S -> bf16 operand; S <- gamma_C * S + B
-        const float gam = reinterpret_cast<const float *>(st + L::GC_S)[r];
-        const uint8_t *brow = st + L::BI_S + (size_t)r * NB * 2;
 #pragma unroll
-        for (int cb = 0; cb < NB; cb += 16) {
-          float x[16];
-          ptx::tmem_ld16(tS + cb, x);
-          ptx::tmem_ld_wait();
-          st_chunk(sb, r, cb >> 3, 128, x);
-          st_chunk(sb, r, (cb >> 3) + 1, 128, x + 8);
-          const uint4 a = *reinterpret_cast<const uint4 *>(brow + cb * 2);
-          const uint4 c2 = *reinterpret_cast<const uint4 *>(brow + cb * 2 + 16);
-          const uint32_t w[8] = {a.x, a.y, a.z, a.w, c2.x, c2.y, c2.z, c2.w};
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const __nv_bfloat162 p2 = *reinterpret_cast<const __nv_bfloat162 *>(&w[e]);
-            x[2 * e] = gam * x[2 * e] + __low2float(p2);
-            x[2 * e + 1] = gam * x[2 * e + 1] + __high2float(p2);
-          }
-          ptx::tmem_st16(tS + cb, x);
-        }
-      }
-      ptx::tmem_st_wait();
+      for (int c8 = 0; c8 < NB / 8; ++c8) st_chunk(sb, r, c8, 128, sr + 8 * c8);
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
-      ptx::named_barrier(1, 128);
+      ptx::named_barrier(1, 128);  // bf16 S complete; every thread has read the last P
       if (tid == 0) {
         ptx::tc_fence_after();
         const uint32_t sAP = ptx::smem_u32(st + R::AP), sSB = ptx::smem_u32(sb);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)  // S += Ap S   (S read MN-major)
+        for (int ks = 0; ks < D / 16; ++ks)  // P = Ap S   (S read MN-major)
           ptx::mma_bf16_ss(tmem, umma::sdesc_k(sAP, D, ks), umma::sdesc_mn(sSB, 128, ks),
-                           umma::idesc_bf16_bmn(128, NB), 1);
+                           umma::idesc_bf16_bmn(128, NB), ks > 0);
         ptx::mma_commit(mS);
         ptx::mbar_arrive(&sbready[i & 1]);
         if (i > 0) ptx::mbar_arrive(&empty[(i - 1) % kStages]);  // state side done with chunk i-1
       }
-    }
-    if (NC > 0 && ok && !ptx::mbar_wait(mS, (NC - 1) & 1, kWaitLimit)) {
-      ok = false;
-      report_error(hdr, KDA_ERR_TIMEOUT, 0x204u);
-    }
-    ptx::tc_fence_after();
-    if (hT) {
-      const size_t s0 = (size_t)bh * D * D;
+      {  // gamma_C S + B while the product runs
+        const float gam = reinterpret_cast<const float *>(st + L::GC_S)[r];
+        const uint4 *brow = reinterpret_cast<const uint4 *>(st + L::BI_S + (size_t)r * NB * 2);
 #pragma unroll
-      for (int cb = 0; cb < NB; cb += 16) {
-        float x[16];
-        ptx::tmem_ld16(tS + cb, x);
-        ptx::tmem_ld_wait();
-        float4 *dst = reinterpret_cast<float4 *>(hT + s0 + (size_t)r * D + j0 + cb);
+        for (int q4 = 0; q4 < NB / 8; ++q4) {
+          const uint4 a = brow[q4];
+          const uint32_t w[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-        for (int j4 = 0; j4 < 4; ++j4)
-          dst[j4] = make_float4(x[4 * j4], x[4 * j4 + 1], x[4 * j4 + 2], x[4 * j4 + 3]);
+          for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 p2 = *reinterpret_cast<const __nv_bfloat162 *>(&w[e]);
+            sr[8 * q4 + 2 * e] = gam * sr[8 * q4 + 2 * e] + __low2float(p2);
+            sr[8 * q4 + 2 * e + 1] = gam * sr[8 * q4 + 2 * e + 1] + __high2float(p2);
+          }
+        }
       }
+      if (ok && !ptx::mbar_wait(mS, i & 1, kWaitLimit)) {
+        ok = false;
+        report_error(hdr, KDA_ERR_TIMEOUT, 0x201u);
+      }
+      ptx::tc_fence_after();
+      {
+        float x[NB];
+        ptx::tmem_ld32(tP, x);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < NB; ++j) sr[j] += x[j];
+      }
+    }
+    if (hT) {
+      float4 *dst = reinterpret_cast<float4 *>(hT + (size_t)bh * D * D + (size_t)r * D + j0);
+#pragma unroll
+      for (int j4 = 0; j4 < NB / 4; ++j4)
+        dst[j4] = make_float4(sr[4 * j4], sr[4 * j4 + 1], sr[4 * j4 + 2], sr[4 * j4 + 3]);
     }
   }
   ptx::tc_fence_before();
