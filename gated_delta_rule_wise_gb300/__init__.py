@@ -24,6 +24,7 @@ __all__ = [
     "kda_chunk_fwd", "kda_chunk_fwd_ex", "kda_chunk_fwd_workspace_size",
     "kda_chunk_fwd_status", "kda_decode_step", "kda_selftest_wait_timeout",
     "kda_chunk_fwd_launches", "kda_chunk_fwd_kernel_names", "kernel_sources",
+    "kda_chunk_fwd_host", "kda_chunk_fwd_host_buffer_size", "host_buffer_for",
     "chunk_fwd", "decode_step", "workspace_for",
     "KDA_F32", "KDA_BF16", "KDA_ALPHA_NONE", "KDA_ALPHA_SCALAR", "KDA_ALPHA_CHANNEL",
     "KDA_PATH_AUTO", "KDA_PATH_CUDA_CORE", "KDA_PATH_TENSOR",
@@ -86,6 +87,10 @@ def load_library():
         lib.kda_chunk_fwd_status.argtypes = [_P, _P]
         lib.kda_decode_step.restype = _I
         lib.kda_decode_step.argtypes = [_P] * 7 + [_I] * 6 + [_P]
+        lib.kda_chunk_fwd_host_buffer_size.restype = _SZ
+        lib.kda_chunk_fwd_host_buffer_size.argtypes = [_I] * 9
+        lib.kda_chunk_fwd_host.restype = _I
+        lib.kda_chunk_fwd_host.argtypes = [_P] * 8 + [_I] * 9 + [_P, _SZ, _P]
         lib.kda_selftest_wait_timeout.restype = _I
         lib.kda_selftest_wait_timeout.argtypes = [_P, _SZ, ctypes.c_uint, _P]
         if lib.kda_abi_version() != ABI_VERSION:
@@ -174,6 +179,48 @@ def kda_chunk_fwd_ex(q, k, v, beta, log_alpha, h0, o, hT, C, workspace, stream=N
 
 def kda_chunk_fwd(q, k, v, beta, log_alpha, h0, o, hT, C, workspace, stream=None):
     kda_chunk_fwd_ex(q, k, v, beta, log_alpha, h0, o, hT, C, workspace, stream, KDA_PATH_AUTO)
+
+
+def _host_ptr(t):
+    if t is None:
+        return None
+    if t.is_cuda:
+        raise ValueError("kda_chunk_fwd_host takes host tensors")
+    if not t.is_contiguous():
+        raise ValueError("libkda takes contiguous tensors")
+    return t.data_ptr()
+
+
+def kda_chunk_fwd_host_buffer_size(B, H, T, dk, dv, C, dtype, alpha_mode, group_heads=0) -> int:
+    return load_library().kda_chunk_fwd_host_buffer_size(B, H, T, dk, dv, C, dtype, alpha_mode,
+                                                         group_heads)
+
+
+def host_buffer_for(q, v, C, log_alpha=None, group_heads=0, device=None):
+    """Device buffer for ``kda_chunk_fwd_host`` on host tensors q [B,H,T,dk], v."""
+    B, H, T, dk = q.shape
+    n = kda_chunk_fwd_host_buffer_size(B, H, T, dk, v.shape[-1], C, _dtype_code(q),
+                                       _alpha_mode(log_alpha, 3), group_heads)
+    if n == 0:
+        raise KdaError(KDA_ERR_UNSUPPORTED, "kda_chunk_fwd_host_buffer_size")
+    buf = torch.empty(n, dtype=torch.uint8, device=device or torch.device("cuda"))
+    buf[:256].zero_()
+    return buf
+
+
+def kda_chunk_fwd_host(q, k, v, beta, log_alpha, h0, o, hT, C, dev_buffer, group_heads=0,
+                       stream=None):
+    """Prefill with q, k, v, beta, log_alpha, h0 and the outputs o, hT in host
+    (ideally pinned) memory; ``dev_buffer`` from ``host_buffer_for``.  Returns
+    once enqueued; synchronise ``stream`` before reading o / hT."""
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    st = load_library().kda_chunk_fwd_host(
+        _host_ptr(q), _host_ptr(k), _host_ptr(v), _host_ptr(beta), _host_ptr(log_alpha),
+        _host_ptr(h0), _host_ptr(o), _host_ptr(hT), B, H, T, dk, dv, C, _dtype_code(q),
+        _alpha_mode(log_alpha, 3), group_heads, _ptr(dev_buffer),
+        dev_buffer.numel() * dev_buffer.element_size(), _stream(stream))
+    _check(st, "kda_chunk_fwd_host")
 
 
 def kda_chunk_fwd_launches(B, H, T, dk, dv, C, dtype, alpha_mode, path=KDA_PATH_AUTO) -> int:

@@ -200,6 +200,42 @@ kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
 kda_status kda_chunk_fwd_status(void *workspace, kda_stream_t stream);
 
 /*
+ * kda_chunk_fwd for inputs and outputs in HOST memory, with the transfers
+ * overlapped with the prefill.  The pages have no counterpart (they do not
+ * discuss where the inputs live); the prefill itself is kda_chunk_fwd.
+ *
+ *   q, k, v, beta, log_alpha, h0   host, same shapes and types as kda_chunk_fwd
+ *   o, hT                          host outputs (hT may be NULL; h0 may be NULL)
+ *   group_heads                    (batch, head) pairs per pipeline step;
+ *                                  0 = about an eighth of B*H
+ *   dev_buffer, dev_bytes          device memory, 256-byte aligned, at least
+ *                                  kda_chunk_fwd_host_buffer_size(...) bytes,
+ *                                  owned by the caller; it holds the shared
+ *                                  workspace (its start: read device errors
+ *                                  with kda_chunk_fwd_status(dev_buffer, ...))
+ *                                  and two staging slots of group_heads pairs
+ *
+ * The (batch, head) pairs are cut into groups; while group g runs on `stream`,
+ * group g + 1 is copied in and group g - 1 copied out on two streams that the
+ * call creates and releases (nothing is kept between calls).  Host memory
+ * should be page-locked (cudaHostAlloc / cudaHostRegister): from pageable
+ * memory the copies are correct but do not overlap.  The call returns once
+ * everything is enqueued; all of it, copies included, completes on `stream`
+ * (synchronise `stream` before reading o or hT).  Results equal those of
+ * kda_chunk_fwd on device copies of the inputs, bit for bit.  Errors: as
+ * kda_chunk_fwd, plus KDA_ERR_INVALID_ARG for a null or misaligned dev_buffer
+ * or dev_bytes below the required size; checked before anything is enqueued.
+ */
+size_t kda_chunk_fwd_host_buffer_size(int B, int H, int T, int dk, int dv, int C,
+                                      kda_dtype dt, kda_alpha_mode am, int group_heads);
+kda_status kda_chunk_fwd_host(const void *q, const void *k, const void *v,
+                              const float *beta, const float *log_alpha,
+                              const float *h0, void *o, float *hT,
+                              int B, int H, int T, int dk, int dv, int C,
+                              kda_dtype dt, kda_alpha_mode am, int group_heads,
+                              void *dev_buffer, size_t dev_bytes, kda_stream_t stream);
+
+/*
  * One recurrent decode step for N x H independent states, in place
  * ("22,580: From GPT-2 to Kimi K3" (yichencityu.github.io), section 5.2, with
  * t = 1 and the cached state; decay as in kda_chunk_fwd):
