@@ -43,7 +43,7 @@ _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "libkda_oracle.so")
 
 ALPHA_NONE, ALPHA_SCALAR, ALPHA_CHANNEL = 0, 1, 2
-_VERSION = 1
+_VERSION = 2
 
 _lib = None
 _lock = threading.Lock()
@@ -76,6 +76,11 @@ def open_library(path):
     f = lib.kda_oracle_recurrent
     f.restype = ctypes.c_int
     f.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int, ctypes.c_void_p,
+                                         ctypes.c_long, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_void_p, ctypes.c_void_p]
+    f = lib.kda_oracle_linear
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int, ctypes.c_void_p,
                                          ctypes.c_long, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_void_p, ctypes.c_void_p]
     return lib
@@ -135,6 +140,69 @@ def recurrent(q, k, v, beta, log_alpha=None, h0=None, lib=None):
     if rc != 0:
         raise RuntimeError(f"kda_oracle_recurrent failed with {rc}")
     return o, hT
+
+
+def linear(q, k, v, log_alpha=None, h0=None, lib=None):
+    """Token-by-token linear attention for one head, in float64:
+    S = Diag(a_t) S + k_t v_t^T, o_t = S^T q_t (see kda_oracle_linear).
+
+    q, k: [T, dk]; v: [T, dv]; log_alpha: None, [T] or [T, dk]; h0: None or
+    [dk, dv].  Returns (o [T, dv], hT [dk, dv]) as float64.
+    """
+    lib = lib or _load()
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    T, dk = q.shape
+    dv = v.shape[1]
+    if k.shape != (T, dk) or v.shape != (T, dv):
+        raise ValueError("shape mismatch")
+    mode = alpha_mode_of(log_alpha, T, dk)
+    la = _f32(log_alpha)
+    h0d = None if h0 is None else np.ascontiguousarray(h0, dtype=np.float64)
+    o = np.empty((T, dv), dtype=np.float64)
+    hT = np.empty((dk, dv), dtype=np.float64)
+    rc = lib.kda_oracle_linear(_ptr(q), _ptr(k), _ptr(v), _ptr(la), mode, _ptr(h0d), T, dk,
+                               dv, _ptr(o), _ptr(hT))
+    if rc != 0:
+        raise RuntimeError(f"kda_oracle_linear failed with {rc}")
+    return o, hT
+
+
+def linear_heads(q, k, v, log_alpha=None, h0=None):
+    """``linear`` for every (b, h) of ``[B, H, T, d]`` inputs; (o [B*H, T, dv], hT [B*H, dk, dv])."""
+    B, H, T, dk = q.shape
+    mode = ALPHA_NONE if log_alpha is None else (ALPHA_SCALAR if np.ndim(log_alpha) == 3
+                                                 else ALPHA_CHANNEL)
+    os_, hs = [], []
+    for b in range(B):
+        for h in range(H):
+            o, hT = linear(q[b, h], k[b, h], v[b, h], _alpha_slice(log_alpha, mode, b, h),
+                           None if h0 is None else h0[b, h])
+            os_.append(o)
+            hs.append(hT)
+    return np.stack(os_), np.stack(hs)
+
+
+def input_maps(q=None, k=None, beta_logit=None):
+    """The maps the pages apply to the projections before the delta rule
+    ("22,580: From GPT-2 to Kimi K3" (yichencityu.github.io), section 5.2,
+    the DeltaNet forward: q = normalize(silu(q)), k = normalize(silu(k)) along
+    the head dimension, beta = sigmoid(w_beta x)), in float64 on the stored
+    values.
+
+    silu(x) = x / (1 + exp(-x)); normalize(x) = x / max(||x||_2, 1e-12) over
+    the last axis; sigmoid(x) = 1 / (1 + exp(-x)).  Returns the mapped arrays
+    (None for an argument given as None).
+    """
+    def silu_norm(x):
+        x = np.asarray(x, dtype=np.float64)
+        s = x / (1.0 + np.exp(-x))
+        n = np.sqrt((s * s).sum(axis=-1, keepdims=True))
+        return s / np.maximum(n, 1e-12)
+
+    out_q = None if q is None else silu_norm(q)
+    out_k = None if k is None else silu_norm(k)
+    out_b = None if beta_logit is None else 1.0 / (1.0 + np.exp(-np.asarray(beta_logit, np.float64)))
+    return out_q, out_k, out_b
 
 
 def _alpha_slice(log_alpha, mode, b, h):

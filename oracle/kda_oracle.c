@@ -112,5 +112,52 @@ int kda_oracle_recurrent(const float *q, const float *k, const float *v,
   return 0;
 }
 
+/*
+ * Linear attention, one head, float64, token by token:
+ *
+ *   S   = Diag(a_t) S + k_t v_t^T      decay first (rows = key channels), then add
+ *   o_t = S^T q_t                      read-out after the write
+ *
+ * Source: "22,580: From GPT-2 to Kimi K3" (yichencityu.github.io), section
+ * 6.2: the state accumulates k^T v chunk after chunk and each query reads the
+ * state of all earlier chunks plus the masked (diagonal included) scores of
+ * its own chunk, i.e. the token loop above with a_t = 1.  The decayed form
+ * (a_t as in kda_oracle_recurrent) is the same decay applied before each
+ * write; the pages print only a_t = 1.  No normaliser (the pages' section 6.2
+ * form, not the feature-map-with-denominator variant of the interlude).
+ * Same layouts and return codes as kda_oracle_recurrent; there is no beta.
+ */
+int kda_oracle_linear(const float *q, const float *k, const float *v,
+                      const float *log_alpha, int alpha_mode, const double *h0,
+                      long T, int dk, int dv, double *o, double *hT) {
+  if (T < 0 || dk <= 0 || dv <= 0 || !o || !hT) return -1;
+  if (alpha_mode < 0 || alpha_mode > 2) return -1;
+  if (alpha_mode != ORACLE_ALPHA_NONE && !log_alpha) return -1;
+  if (T > 0 && (!q || !k || !v)) return -1;
+  double *state = hT;
+  if (h0)
+    memcpy(state, h0, sizeof(double) * (size_t)dk * (size_t)dv);
+  else
+    memset(state, 0, sizeof(double) * (size_t)dk * (size_t)dv);
+  for (long t = 0; t < T; ++t) {
+    for (int c = 0; c < dk; ++c) {
+      double decay = 1.0;
+      if (alpha_mode == ORACLE_ALPHA_CHANNEL)
+        decay = exp(-exp((double)log_alpha[t * dk + c]));
+      else if (alpha_mode == ORACLE_ALPHA_SCALAR)
+        decay = exp(-exp((double)log_alpha[t]));
+      const double kc = (double)k[t * dk + c];
+      double *srow = state + (size_t)c * dv;
+      for (int e = 0; e < dv; ++e) srow[e] = decay * srow[e] + kc * (double)v[t * dv + e];
+    }
+    for (int e = 0; e < dv; ++e) {
+      double acc = 0.0;
+      for (int c = 0; c < dk; ++c) acc += (double)q[t * dk + c] * state[(size_t)c * dv + e];
+      o[t * dv + e] = acc;
+    }
+  }
+  return 0;
+}
+
 /* Interface version, so the Python side can refuse a stale build. */
-int kda_oracle_version(void) { return 1; }
+int kda_oracle_version(void) { return 2; }
