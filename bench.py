@@ -361,6 +361,37 @@ def run_ours(args, rank, world, local, dist):
             "tensor_tflops_per_call": alg_flops / (ms_step * 1e-3) / 1e12}
     roof["frac"] = roof["achieved"] / roof["peak"]
 
+    # ---- the other update rule and the fused input maps, same workload
+    def time_variant(rule, maps):
+        beta_arg = None if rule == kda.KDA_RULE_LINEAR else d["beta"]
+
+        def call():
+            kda.kda_chunk_fwd_rule(d["q"], d["k"], d["v"], beta_arg, d["log_alpha"], d["h0"], o,
+                                   hT, w.C, ws, rule, maps, stream)
+
+        for _ in range(args.warmup):
+            call()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(dist, torch)
+        a.record(stream)
+        for _ in range(args.steps):
+            call()
+        b.record(stream)
+        barrier(dist, torch)
+        kda.kda_chunk_fwd_status(ws, stream)
+        ms = max_over_ranks(a.elapsed_time(b) / args.steps, dist, dev)
+        return {"value": world * tokens / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+                "steps": args.steps}
+
+    variants = {
+        "linear_attention": dict(
+            time_variant(kda.KDA_RULE_LINEAR, 0),
+            rule="S = Diag(a) S + k v^T, o = S^T q (kda_chunk_fwd_rule, KDA_RULE_LINEAR)"),
+        "fused_input_maps": dict(
+            time_variant(kda.KDA_RULE_DELTA, kda.KDA_MAP_QK_SILU_NORM | kda.KDA_MAP_BETA_SIGMOID),
+            maps="q, k <- normalize(silu(.)), beta <- sigmoid(.) inside the prep kernel"),
+    }
+
     # ---- end to end through the public API with host buffers
     h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
     o_host = torch.empty_like(o, device="cpu").pin_memory()
@@ -466,7 +497,7 @@ def run_ours(args, rank, world, local, dist):
                            "parallelism": f"replicas x{world}"},
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches_per_call * args.steps,
-                "clocks": clocks, "decode": dec}
+                "clocks": clocks, "decode": dec, "variants": variants}
         print(json.dumps(line), flush=True)
     return 0
 

@@ -25,6 +25,8 @@ __all__ = [
     "kda_chunk_fwd_status", "kda_decode_step", "kda_selftest_wait_timeout",
     "kda_chunk_fwd_launches", "kda_chunk_fwd_kernel_names", "kernel_sources",
     "kda_chunk_fwd_host", "kda_chunk_fwd_host_buffer_size", "host_buffer_for",
+    "kda_chunk_fwd_rule", "KDA_RULE_DELTA", "KDA_RULE_LINEAR", "KDA_MAP_QK_SILU_NORM",
+    "KDA_MAP_BETA_SIGMOID",
     "chunk_fwd", "decode_step", "workspace_for",
     "KDA_F32", "KDA_BF16", "KDA_ALPHA_NONE", "KDA_ALPHA_SCALAR", "KDA_ALPHA_CHANNEL",
     "KDA_PATH_AUTO", "KDA_PATH_CUDA_CORE", "KDA_PATH_TENSOR",
@@ -87,6 +89,8 @@ def load_library():
         lib.kda_chunk_fwd_status.argtypes = [_P, _P]
         lib.kda_decode_step.restype = _I
         lib.kda_decode_step.argtypes = [_P] * 7 + [_I] * 6 + [_P]
+        lib.kda_chunk_fwd_rule.restype = _I
+        lib.kda_chunk_fwd_rule.argtypes = chunk_args[:16] + [_I, ctypes.c_uint] + chunk_args[16:]
         lib.kda_chunk_fwd_host_buffer_size.restype = _SZ
         lib.kda_chunk_fwd_host_buffer_size.argtypes = [_I] * 9
         lib.kda_chunk_fwd_host.restype = _I
@@ -179,6 +183,24 @@ def kda_chunk_fwd_ex(q, k, v, beta, log_alpha, h0, o, hT, C, workspace, stream=N
 
 def kda_chunk_fwd(q, k, v, beta, log_alpha, h0, o, hT, C, workspace, stream=None):
     kda_chunk_fwd_ex(q, k, v, beta, log_alpha, h0, o, hT, C, workspace, stream, KDA_PATH_AUTO)
+
+
+KDA_RULE_DELTA, KDA_RULE_LINEAR = 0, 1
+KDA_MAP_QK_SILU_NORM, KDA_MAP_BETA_SIGMOID = 1, 2
+
+
+def kda_chunk_fwd_rule(q, k, v, beta, log_alpha, h0, o, hT, C, workspace, rule=KDA_RULE_DELTA,
+                       maps=0, stream=None):
+    """``kda_chunk_fwd`` with an update rule (KDA_RULE_DELTA / KDA_RULE_LINEAR)
+    and input maps (KDA_MAP_* bits) applied on the fly; beta may be None for
+    the linear rule."""
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    st = load_library().kda_chunk_fwd_rule(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(log_alpha), _ptr(h0), _ptr(o), _ptr(hT),
+        B, H, T, dk, dv, C, _dtype_code(q), _alpha_mode(log_alpha, 3), rule, maps,
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "kda_chunk_fwd_rule")
 
 
 def _host_ptr(t):

@@ -131,6 +131,46 @@ kda_status kda_chunk_fwd_ex(const void *q, const void *k, const void *v, const f
                            hdr, s, timer);
 }
 
+kda_status kda_chunk_fwd_rule(const void *q, const void *k, const void *v, const float *beta,
+                              const float *log_alpha, const float *h0, void *o, float *hT, int B,
+                              int H, int T, int dk, int dv, int C, kda_dtype dt,
+                              kda_alpha_mode am, kda_rule rule, unsigned maps, void *workspace,
+                              size_t ws_bytes, kda_stream_t stream) {
+  const unsigned known = KDA_MAP_QK_SILU_NORM | KDA_MAP_BETA_SIGMOID;
+  if (rule != KDA_RULE_DELTA && rule != KDA_RULE_LINEAR) return KDA_ERR_INVALID_ARG;
+  if ((maps & ~known) != 0u) return KDA_ERR_INVALID_ARG;
+  if (rule == KDA_RULE_LINEAR && (maps & KDA_MAP_BETA_SIGMOID)) return KDA_ERR_INVALID_ARG;
+  if (rule == KDA_RULE_DELTA && maps == 0u)
+    return kda_chunk_fwd_ex(q, k, v, beta, log_alpha, h0, o, hT, B, H, T, dk, dv, C, dt, am,
+                            workspace, ws_bytes, stream, KDA_PATH_AUTO, nullptr, 0);
+  // everything else: the d = 128 tensor path
+  kda_status st = check_chunk_shape(B, H, T, dk, dv, C, dt, am, KDA_PATH_TENSOR);
+  if (st != KDA_OK) return st;
+  if (dk != 128 || dv != 128) return KDA_ERR_UNSUPPORTED;
+  const bool has_tokens = (long long)B * H * T > 0;
+  const bool need_beta = rule == KDA_RULE_DELTA;
+  if (has_tokens) {
+    if (!q || !k || !v || !o || (need_beta && !beta)) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+        (beta && !aligned16(beta)))
+      return KDA_ERR_INVALID_ARG;
+  }
+  if (am == KDA_ALPHA_NONE) {
+    if (log_alpha) return KDA_ERR_INVALID_ARG;
+  } else if (has_tokens && (!log_alpha || !aligned16(log_alpha))) {
+    return KDA_ERR_INVALID_ARG;
+  }
+  if ((h0 && !aligned16(h0)) || (hT && !aligned16(hT))) return KDA_ERR_INVALID_ARG;
+  if (!workspace || !aligned256(workspace)) return KDA_ERR_INVALID_ARG;
+  if (ws_bytes < workspace_bytes(B, H, T, dk, dv, C, dt, am, KDA_PATH_TENSOR))
+    return KDA_ERR_INVALID_ARG;
+  if (chunk_tc_launches(B * H, T, hT != nullptr) == 0) return KDA_OK;
+  LaunchTimer timer;
+  timer.s = reinterpret_cast<cudaStream_t>(stream);
+  return launch_chunk_tc(q, k, v, beta, log_alpha, h0, o, hT, B, H, T, dk, dv, C, am, workspace,
+                         ws_bytes, timer.s, timer, (int)rule, maps);
+}
+
 kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const float *beta,
                          const float *log_alpha, const float *h0, void *o, float *hT, int B,
                          int H, int T, int dk, int dv, int C, kda_dtype dt, kda_alpha_mode am,

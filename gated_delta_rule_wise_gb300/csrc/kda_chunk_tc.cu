@@ -742,13 +742,16 @@ __device__ __forceinline__ uint4 pack8(const float *x) {
                     pack_bf16x2(x[6], x[7]));
 }
 
+// kGeneral = false compiles the plain gated delta rule (rule and maps fixed
+// at 0, their code folded away); true reads them at run time.
+template <bool kGeneral>
 __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
                                           const __nv_bfloat16 *__restrict__ k,
                                           const __nv_bfloat16 *__restrict__ v,
                                           const float *__restrict__ beta,
                                           const float *__restrict__ log_alpha, int alpha_mode,
                                           int T, int NC, int total, uint8_t *__restrict__ ws,
-                                          uint8_t *sm) {
+                                          uint8_t *sm, int rule, unsigned maps) {
   constexpr int D = 128;
   using Rr = Rec<128>;
   using L = PrepSmem128;
@@ -819,13 +822,22 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
     issue_lkv(blockIdx.x);
     issue_q(blockIdx.x);
   }
-  float b_next = 0.f;  // beta of the next chunk's row tid (tid < C)
-  if ((int)blockIdx.x < total && tid < kC) {
-    int valid;
-    size_t row0;
-    rows_of(blockIdx.x, valid, row0);
-    b_next = tid < valid ? beta[row0 + tid] : 0.f;
+  if constexpr (!kGeneral) {
+    rule = KDA_RULE_DELTA;
+    maps = 0u;
   }
+  const bool linear = rule == KDA_RULE_LINEAR;  // W = 0, U = V: no beta, no solve
+  auto beta_of = [&](int idx) -> float {        // beta of row tid of a chunk (tid < C)
+    int vn;
+    size_t rn;
+    rows_of(idx, vn, rn);
+    if (tid >= vn) return 0.f;
+    if (linear) return 1.f;
+    const float b = beta[rn + tid];
+    return (maps & KDA_MAP_BETA_SIGMOID) ? 1.f / (1.f + __expf(-b)) : b;
+  };
+  float b_next = 0.f;  // beta of the next chunk's row tid (tid < C)
+  if ((int)blockIdx.x < total && tid < kC) b_next = beta_of(blockIdx.x);
   uint32_t mma_phase = 0;
 
   auto wait_mma = [&](unsigned code) {
@@ -918,6 +930,27 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
       unpack8(rk[m], kf);
       unpack8(rq[m], qf);
       unpack8(rv[m], vf);
+      if (maps & KDA_MAP_QK_SILU_NORM) {  // q, k <- silu / ||silu||, the row's 16 lanes reduce
+        float sq = 0.f, sk = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          qf[e] = __fdividef(qf[e], 1.f + __expf(-qf[e]));
+          kf[e] = __fdividef(kf[e], 1.f + __expf(-kf[e]));
+          sq += qf[e] * qf[e];
+          sk += kf[e] * kf[e];
+        }
+#pragma unroll
+        for (int off = 1; off < 16; off <<= 1) {
+          sq += __shfl_xor_sync(0xffffffffu, sq, off);
+          sk += __shfl_xor_sync(0xffffffffu, sk, off);
+        }
+        const float iq = rsqrtf(fmaxf(sq, 1e-24f)), ik = rsqrtf(fmaxf(sk, 1e-24f));
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          qf[e] *= iq;
+          kf[e] *= ik;
+        }
+      }
       const float4 e0 = *reinterpret_cast<const float4 *>(EG + r * D + c8 * 8);
       const float4 e1 = *reinterpret_cast<const float4 *>(EG + r * D + c8 * 8 + 4);
       eg[0] = e0.x; eg[1] = e0.y; eg[2] = e0.z; eg[3] = e0.w;
@@ -926,7 +959,7 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
       float kb[8], qg[8], vb[8], kh[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        kb[e] = bt * kf[e] * eg[e];
+        kb[e] = linear ? 0.f : bt * kf[e] * eg[e];
         qg[e] = qf[e] * eg[e];
         vb[e] = bt * vf[e];
         kh[e] = kf[e] * __fdividef(1.f, eg[e]);
@@ -947,6 +980,24 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
       ptx::mma_commit(bar);
     }
     wait_mma(0x101u);
+
+    auto read_m = [&]() {  // lanes 64..127 (M, lower incl.) -> bf16 tile in A's space
+      if (quarter >= 2) {
+        const int r = quarter * 32 + lane - kC;
+        const int cb = colhalf * 32;
+        float x[32];
+        ptx::tmem_ld32(t_lane + cb, x);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = (cb + j <= r) ? x[j] : 0.f;
+#pragma unroll
+        for (int j8 = 0; j8 < 4; ++j8) st_chunk(MM, r, (cb >> 3) + j8, kC, x + 8 * j8);
+      }
+    };
+    if (linear) {  // [W | U] = [0 | V] already sits in rows 0-63 of the tile area
+      read_m();
+      sync_for_mma();
+    } else {
 
     // ---- (3) lanes 0..63: A (strict lower) as float, 32 columns per warp
     if (quarter < 2) {
@@ -970,19 +1021,7 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
 
     // ---- (4) T = (I + A)^-1; lanes 64..127 (M, lower incl.) to a bf16 tile
     // in A's space once A is no longer read
-    blocked_unit_lower_inverse(AF, TF, TT, tid, [&]() {
-      if (quarter >= 2) {
-        const int r = quarter * 32 + lane - kC;
-        const int cb = colhalf * 32;
-        float x[32];
-        ptx::tmem_ld32(t_lane + cb, x);
-        ptx::tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = (cb + j <= r) ? x[j] : 0.f;
-#pragma unroll
-        for (int j8 = 0; j8 < 4; ++j8) st_chunk(MM, r, (cb >> 3) + j8, kC, x + 8 * j8);
-      }
-    });
+    blocked_unit_lower_inverse(AF, TF, TT, tid, read_m);
     sync_for_mma();
 
     // ---- (5) [W | U] = T [K_beta | beta V]   -> TMEM cols [0, 256), M = 64 layout
@@ -1014,6 +1053,7 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
       }
     }
     sync_for_mma();
+    }  // delta rule
 
     // ---- (7) (K/gamma)^T [W | U] -> cols [0, 256)
     if (tid == 0) {
@@ -1100,12 +1140,7 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
     // A's space and blocks 2-3 are free: fetch the next chunk's log_alpha, k, v
     if (has_next) {
       if (tid == 0) issue_lkv(idx_next);
-      if (tid < kC) {
-        int vn;
-        size_t rn;
-        rows_of(idx_next, vn, rn);
-        b_next = tid < vn ? beta[rn + tid] : 0.f;
-      }
+      if (tid < kC) b_next = beta_of(idx_next);
     }
 
     // ---- (10) token rows (lanes < 16): Qp = Q*gamma - M W (warps 0-3), O = M U
@@ -1183,17 +1218,17 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
   }
 }
 
-template <int D>
+template <int D, bool kGeneral>
 __global__ void __launch_bounds__(256, D == 128 ? 2 : 1)
 kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                 const __nv_bfloat16 *__restrict__ v, const float *__restrict__ beta,
                 const float *__restrict__ log_alpha, int alpha_mode, int T, int NC, int total,
-                uint8_t *__restrict__ ws) {
+                uint8_t *__restrict__ ws, int rule, unsigned maps) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));
   if constexpr (D == 128)
-    prep_d128(q, k, v, beta, log_alpha, alpha_mode, T, NC, total, ws, sm);
+    prep_d128<kGeneral>(q, k, v, beta, log_alpha, alpha_mode, T, NC, total, ws, sm, rule, maps);
   else
     prep_d64(q, k, v, beta, log_alpha, alpha_mode, T, NC, total, ws, sm);
 }
@@ -1665,13 +1700,18 @@ constexpr int scan_nb() { return 32; }
 template <int D>
 kda_status launch_d(const void *q, const void *k, const void *v, const float *beta,
                     const float *log_alpha, const float *h0, void *o, float *hT, int BH, int T,
-                    kda_alpha_mode am, uint8_t *ws, cudaStream_t st, LaunchTimer &timer) {
+                    kda_alpha_mode am, uint8_t *ws, cudaStream_t st, LaunchTimer &timer,
+                    int rule, unsigned maps) {
   constexpr int NB = scan_nb<D>();
   const int NC = (T + kC - 1) / kC;
   const uint32_t prep_smem = (D == 128 ? PrepSmem128::BYTES : PrepSmem<64>::BYTES) + 1024;
   const uint32_t scan_smem =
       (D == 128 ? ScanSmem128<NB>::BYTES : ScanSmem64<NB>::BYTES) + 1024;
-  if (cudaFuncSetAttribute(kda_prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto prep = kda_prep_kernel<D, false>;
+  if constexpr (D == 128) {
+    if (rule != 0 || maps != 0u) prep = kda_prep_kernel<D, true>;
+  }
+  if (cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)prep_smem) != cudaSuccess ||
       cudaFuncSetAttribute(kda_scan_kernel<D, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)scan_smem) != cudaSuccess)
@@ -1686,9 +1726,10 @@ kda_status launch_d(const void *q, const void *k, const void *v, const float *be
     const long long slots = (long long)sms * (D == 128 ? 2 : 1);  // persistent CTAs per SM
     const int grid = (int)(total < slots ? total : slots);
     timer.mark();
-    kda_prep_kernel<D><<<grid, 256, prep_smem, st>>>(
+    prep<<<grid, 256, prep_smem, st>>>(
         static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
-        static_cast<const __nv_bfloat16 *>(v), beta, log_alpha, (int)am, T, NC, (int)total, ws);
+        static_cast<const __nv_bfloat16 *>(v), beta, log_alpha, (int)am, T, NC, (int)total, ws,
+        rule, maps);
   }
   timer.mark();
   kda_scan_kernel<D, NB><<<dim3(D / NB, BH), D == 128 ? kScan128Threads : 128, scan_smem, st>>>(
@@ -1724,13 +1765,14 @@ kda_status launch_chunk_tc(const void *q, const void *k, const void *v, const fl
                            const float *log_alpha, const float *h0, void *o, float *hT, int B,
                            int H, int T, int dk, int /*dv*/, int /*C*/, kda_alpha_mode am,
                            void *workspace, size_t /*ws_bytes*/, cudaStream_t stream,
-                           LaunchTimer &timer) {
+                           LaunchTimer &timer, int rule, unsigned maps) {
   const int BH = B * H;
   if (chunk_tc_launches(BH, T, hT != nullptr) == 0) return KDA_OK;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   if (dk == 128)
-    return launch_d<128>(q, k, v, beta, log_alpha, h0, o, hT, BH, T, am, ws, stream, timer);
-  return launch_d<64>(q, k, v, beta, log_alpha, h0, o, hT, BH, T, am, ws, stream, timer);
+    return launch_d<128>(q, k, v, beta, log_alpha, h0, o, hT, BH, T, am, ws, stream, timer, rule,
+                         maps);
+  return launch_d<64>(q, k, v, beta, log_alpha, h0, o, hT, BH, T, am, ws, stream, timer, 0, 0u);
 }
 
 }  // namespace kda

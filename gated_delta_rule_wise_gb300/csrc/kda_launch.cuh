@@ -39,11 +39,13 @@ int chunk_tc_launches(int BH, int T, bool has_hT);
 const char *chunk_tc_kernel_name(int T, int i);
 bool chunk_tc_supported(int dk, int dv, int C, kda_dtype dt);
 size_t chunk_tc_workspace_bytes(int B, int H, int T, int dk, int dv, int C);
+// rule: KDA_RULE_DELTA / KDA_RULE_LINEAR; maps: KDA_MAP_* bits (both other
+// than 0 only for dk = dv = 128).
 kda_status launch_chunk_tc(const void *q, const void *k, const void *v, const float *beta,
                            const float *log_alpha, const float *h0, void *o, float *hT,
                            int B, int H, int T, int dk, int dv, int C, kda_alpha_mode am,
                            void *workspace, size_t workspace_bytes, cudaStream_t stream,
-                           LaunchTimer &timer);
+                           LaunchTimer &timer, int rule = 0, unsigned maps = 0);
 kda_status launch_selftest_wait(WorkspaceHeader *hdr, unsigned spin_limit,
                                 cudaStream_t stream);
 }  // namespace kda

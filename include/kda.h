@@ -200,6 +200,40 @@ kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
 kda_status kda_chunk_fwd_status(void *workspace, kda_stream_t stream);
 
 /*
+ * kda_chunk_fwd with a choice of update rule and of maps applied to the
+ * inputs on the fly (no extra pass over memory).
+ *
+ * rule:
+ *   KDA_RULE_DELTA   the gated delta rule of kda_chunk_fwd.
+ *   KDA_RULE_LINEAR  linear attention ("22,580: From GPT-2 to Kimi K3"
+ *                    (yichencityu.github.io), section 6.2: the state sums
+ *                    k^T v, each query reads the state and its own chunk's
+ *                    masked scores), with the same optional decay applied
+ *                    first:  S = Diag(a_t) S + k_t v_t^T,  o_t = S^T q_t.
+ *                    No normaliser; beta is not read (may be NULL).
+ * input_maps (bit set), the maps the same page's section 5.2 applies to the
+ * projections before the delta rule:
+ *   KDA_MAP_QK_SILU_NORM  q, k <- silu(x) / max(||silu(x)||_2, 1e-12) per
+ *                         (token, head), silu(x) = x / (1 + exp(-x))
+ *   KDA_MAP_BETA_SIGMOID  beta <- 1 / (1 + exp(-beta))   (not with LINEAR)
+ *
+ * Other arguments as kda_chunk_fwd (same workspace size).  rule DELTA with
+ * no maps is kda_chunk_fwd (every shape); anything else runs on the tensor
+ * path only: bf16, C = 64, dk = dv = 128, else KDA_ERR_UNSUPPORTED.  An
+ * unknown rule or map bit, or BETA_SIGMOID with LINEAR: KDA_ERR_INVALID_ARG.
+ */
+typedef enum { KDA_RULE_DELTA = 0, KDA_RULE_LINEAR = 1 } kda_rule;
+#define KDA_MAP_QK_SILU_NORM 1u
+#define KDA_MAP_BETA_SIGMOID 2u
+kda_status kda_chunk_fwd_rule(const void *q, const void *k, const void *v,
+                              const float *beta, const float *log_alpha,
+                              const float *h0, void *o, float *hT,
+                              int B, int H, int T, int dk, int dv, int C,
+                              kda_dtype dt, kda_alpha_mode am, kda_rule rule,
+                              unsigned input_maps, void *workspace, size_t workspace_bytes,
+                              kda_stream_t stream);
+
+/*
  * kda_chunk_fwd for inputs and outputs in HOST memory, with the transfers
  * overlapped with the prefill.  The pages have no counterpart (they do not
  * discuss where the inputs live); the prefill itself is kda_chunk_fwd.
