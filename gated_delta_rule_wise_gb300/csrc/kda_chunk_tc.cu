@@ -1034,23 +1034,20 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
     }
     wait_mma(0x102u);
 
-    // ---- (6) [W | U] rows -> natural tile over K_beta and beta V (both consumed)
+    // ---- (6) [W | U] rows -> natural tile over K_beta and beta V (both consumed).
+    // M = 64 layout: a warp's 16 rows sit in lanes 0-15 of its quarter; threads
+    // 0-15 read columns c.., threads 16-31 the same rows at c + 64..
     {
-      const int rr = quarter * 16 + lane;  // token row (lanes < 16 of the M = 64 layout)
+      const int rr = quarter * 16 + (lane & 15), side = lane >> 4;
+      float x[32], y[32];
+      ptx::tmem_ld32_halves<64>(t_lane + colhalf * 128, x);
+      ptx::tmem_ld32_halves<64>(t_lane + colhalf * 128 + 32, y);
+      ptx::tmem_ld_wait();
+      const int c8 = (colhalf * 128 + side * 64) >> 3;  // first chunk of this thread's 64 columns
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int cb = colhalf * 128 + h * 64;
-        float x[32], y[32];
-        ptx::tmem_ld32(t_lane + cb, x);
-        ptx::tmem_ld32(t_lane + cb + 32, y);
-        ptx::tmem_ld_wait();
-        if (lane < 16) {
+      for (int j8 = 0; j8 < 4; ++j8) st_chunk(X1, rr, c8 + j8, 128, x + 8 * j8);
 #pragma unroll
-          for (int j8 = 0; j8 < 4; ++j8) st_chunk(X1, rr, (cb >> 3) + j8, 128, x + 8 * j8);
-#pragma unroll
-          for (int j8 = 0; j8 < 4; ++j8) st_chunk(X1, rr, (cb >> 3) + 4 + j8, 128, y + 8 * j8);
-        }
-      }
+      for (int j8 = 0; j8 < 4; ++j8) st_chunk(X1, rr, c8 + 4 + j8, 128, y + 8 * j8);
     }
     sync_for_mma();
     }  // delta rule
@@ -1143,63 +1140,56 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
       if (tid < kC) b_next = beta_of(idx_next);
     }
 
-    // ---- (10) token rows (lanes < 16): Qp = Q*gamma - M W (warps 0-3), O = M U
-    // (warps 4-7); staged per warp (the consumed W rows, the T tile) as in (8):
-    // 2 KB of Qp per K atom, 1 KB of O per 32-column block
+    // ---- (10) token rows: Qp = Q*gamma - M W (warps 0-3), O = M U (warps 4-7).
+    // M = 64 layout read as in (6): threads 0-15 hold columns 0-63 of the
+    // warp's 16 rows, threads 16-31 columns 64-127.  Staged per warp (the
+    // consumed W rows, the T tile) as in (8): Qp as two 2 KB pieces (one per
+    // K atom), O as 1 KB pieces (one per 32-column block).
     {
-      const int rr = quarter * 16 + lane;
+      const int rr = quarter * 16 + (lane & 15), side = lane >> 4, row = lane & 15;
+      float x[64];
+      ptx::tmem_ld32_halves<64>(t_lane + colhalf * 128, *reinterpret_cast<float(*)[32]>(x));
+      ptx::tmem_ld32_halves<64>(t_lane + colhalf * 128 + 32,
+                                *reinterpret_cast<float(*)[32]>(x + 32));
+      ptx::tmem_ld_wait();
       if (colhalf == 0) {
-        uint8_t *stg = X1 + quarter * 2048;
-#pragma unroll 1
+        uint8_t *stg = X1 + (quarter >> 1) * 16384 + (quarter & 1) * 4096;  // 4 KB
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {  // this thread's K atom is `side`
+          float qg[8];
+          ld_chunk(X1, kC + rr, side * 8 + cc, 128, qg);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) qg[j] -= x[8 * cc + j];
+          *reinterpret_cast<uint4 *>(stg + side * 2048 + row * 128 + ((cc ^ (row & 7)) << 4)) =
+              pack8(qg);
+        }
+        __syncwarp();
+#pragma unroll
         for (int a = 0; a < 2; ++a) {
-          float x[64];
-          ptx::tmem_ld32(t_lane + a * 64, *reinterpret_cast<float(*)[32]>(x));
-          ptx::tmem_ld32(t_lane + a * 64 + 32, *reinterpret_cast<float(*)[32]>(x + 32));
-          ptx::tmem_ld_wait();
-          if (lane < 16) {
-#pragma unroll
-            for (int cc = 0; cc < 8; ++cc) {
-              float qg[8];
-              ld_chunk(X1, kC + rr, a * 8 + cc, 128, qg);
-#pragma unroll
-              for (int j = 0; j < 8; ++j) qg[j] -= x[8 * cc + j];
-              *reinterpret_cast<uint4 *>(stg + lane * 128 + ((cc ^ (lane & 7)) << 4)) = pack8(qg);
-            }
-          }
-          __syncwarp();
           uint8_t *dst = recg + Rr::QP + a * (kC * 128) + quarter * 2048;
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             *reinterpret_cast<uint4 *>(dst + i * 512 + lane * 16) =
-                *reinterpret_cast<const uint4 *>(stg + i * 512 + lane * 16);
-          __syncwarp();
+                *reinterpret_cast<const uint4 *>(stg + a * 2048 + i * 512 + lane * 16);
         }
       } else {
-        uint8_t *stg = TT + quarter * 1024;
-#pragma unroll 1
-        for (int h2 = 0; h2 < 2; ++h2) {
-          float x[64];
-          ptx::tmem_ld32(t_lane + 128 + h2 * 64, *reinterpret_cast<float(*)[32]>(x));
-          ptx::tmem_ld32(t_lane + 128 + h2 * 64 + 32, *reinterpret_cast<float(*)[32]>(x + 32));
-          ptx::tmem_ld_wait();
+        uint8_t *stg = TT + quarter * 2048;  // two 1 KB pieces: blocks hb (side 0), hb + 2 (side 1)
 #pragma unroll
-          for (int hb = 0; hb < 2; ++hb) {
-            if (lane < 16) {
+        for (int hb = 0; hb < 2; ++hb) {
 #pragma unroll
-              for (int j8 = 0; j8 < 4; ++j8)
-                *reinterpret_cast<uint4 *>(stg + lane * 64 + ((j8 ^ ((lane >> 1) & 3)) << 4)) =
-                    pack8(x + 32 * hb + 8 * j8);
-            }
-            __syncwarp();
-            uint8_t *dst = recg + Rr::OI + (h2 * 2 + hb) * (kC * 64) + quarter * 1024;
+          for (int j8 = 0; j8 < 4; ++j8)  // 64-byte rows, chunks rotated for conflict-free writes
+            *reinterpret_cast<uint4 *>(stg + side * 1024 + row * 64 +
+                                       ((j8 ^ ((row >> 1) & 3)) << 4)) = pack8(x + 32 * hb + 8 * j8);
+          __syncwarp();
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-              const int p = i * 512 + lane * 16, R = p >> 6, j = ((p >> 4) & 3) ^ ((R >> 1) & 3);
-              *reinterpret_cast<uint4 *>(dst + R * 64 + j * 16) =
-                  *reinterpret_cast<const uint4 *>(stg + p);
-            }
-            __syncwarp();
+          for (int i = 0; i < 4; ++i) {
+            const int p = i * 512 + lane * 16, piece = p >> 10, pp = p & 1023;
+            const int R = pp >> 6, j = ((pp >> 4) & 3) ^ ((R >> 1) & 3);
+            *reinterpret_cast<uint4 *>(recg + Rr::OI + (hb + 2 * piece) * (kC * 64) +
+                                       quarter * 1024 + R * 64 + j * 16) =
+                *reinterpret_cast<const uint4 *>(stg + p);
           }
+          __syncwarp();
         }
       }
     }

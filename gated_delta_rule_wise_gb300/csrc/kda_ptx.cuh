@@ -165,6 +165,27 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&r)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) r[i] = __uint_as_float(x[i]);
 }
+// 16 lanes x 32 bits, two column ranges: threads 0-15 of the warp get lanes
+// (base lane + t), columns [col, col + 32); threads 16-31 get lanes
+// (base lane + t - 16), columns [col + kSplit, col + kSplit + 32).  Reads an
+// M = 64 accumulator (16 rows per lane quarter) with every thread busy.
+template <int kSplit>
+__device__ __forceinline__ void tmem_ld32_halves(uint32_t taddr, float (&r)[32]) {
+  uint32_t x[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32], %33;"
+      : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5]), "=r"(x[6]),
+        "=r"(x[7]), "=r"(x[8]), "=r"(x[9]), "=r"(x[10]), "=r"(x[11]), "=r"(x[12]),
+        "=r"(x[13]), "=r"(x[14]), "=r"(x[15]), "=r"(x[16]), "=r"(x[17]), "=r"(x[18]),
+        "=r"(x[19]), "=r"(x[20]), "=r"(x[21]), "=r"(x[22]), "=r"(x[23]), "=r"(x[24]),
+        "=r"(x[25]), "=r"(x[26]), "=r"(x[27]), "=r"(x[28]), "=r"(x[29]), "=r"(x[30]),
+        "=r"(x[31])
+      : "r"(taddr), "n"(kSplit));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) r[i] = __uint_as_float(x[i]);
+}
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
