@@ -157,11 +157,11 @@ __device__ __forceinline__ void fma4(float4 &acc, float a, const float4 &b) {
 }
 
 // T = (I + A)^-1 for the strictly lower A (float, row stride kLD), in blocks
-// of 16: T_ij = -T_ii sum_{m=j..i-1} A_im T_mj.  The diagonal blocks by
-// forward substitution (one column per thread, partial sums in registers);
-// then G_im = T_ii A_im for the six blocks below the diagonal at once, and
-// T_ij = -sum_m G_im T_mj along the block subdiagonals (three blocks, then
-// two, then one), every block product done by 64 threads on 1 x 4 strips.
+// of 16: T_ij = -T_ii sum_{m=j..i-1} A_im T_mj.  The diagonal blocks T_ii and
+// the six G_im = T_ii A_im below the diagonal, all at once by forward
+// substitution (one right-hand column per thread, partial sums in registers);
+// then T_ij = -sum_m G_im T_mj along the block subdiagonals (three blocks,
+// then two, then one), every block product done by 64 threads on 1 x 4 strips.
 // The float row stride kLD = C + 4 keeps column reads across rows and 16-byte
 // row accesses free of bank conflicts, and lets every inner-loop address be an
 // immediate offset.  Leaves T (float, lower blocks) in TF and the bf16 K-major
@@ -178,21 +178,36 @@ template <class Late = NoLateWork>
 __device__ __forceinline__ void blocked_unit_lower_inverse(const float *AF, float *TF, uint8_t *TT,
                                                            int tid, const Late &late = Late()) {
   float *XS = reinterpret_cast<float *>(TT);
-  if (tid < kC) {
-    const int b = tid >> 4, j = tid & 15, o = b * 16;
-    const float *Ab = AF + o * kLD + o;
+  // One stage of 160 column solves, (I + A_ii) x = rhs by forward substitution
+  // (partial sums in registers): 4 x 16 columns of the identity give the
+  // diagonal blocks T_ii, 6 x 16 columns of A_im give G_im = T_ii A_im,
+  // slots 0..5 = (1,0) (2,1) (3,2) (2,0) (3,1) (3,0).
+  if (tid < 10 * 16) {
+    const int blk = tid >> 4, j = tid & 15;
+    const bool diag = blk < 4;
+    const int sl = blk - 4;
+    const int bi = diag ? blk : (sl < 3 ? sl + 1 : (sl == 5 ? 3 : sl - 1));
+    const int bj = diag ? blk : (sl < 3 ? sl : (sl == 5 ? 0 : sl - 3));
+    const float *Ab = AF + (bi * 16) * kLD + bi * 16;
+    const float *rc = AF + (bi * 16) * kLD + bj * 16 + j;  // column j of A_(bi,bj)
     float t[16], p[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) p[i] = 0.f;
+    for (int i = 0; i < 16; ++i) p[i] = diag ? 0.f : -rc[i * kLD];
 #pragma unroll
     for (int kk = 0; kk < 16; ++kk) {
-      t[kk] = (kk == j) ? 1.f : ((kk < j) ? 0.f : -p[kk]);
+      t[kk] = diag ? ((kk == j) ? 1.f : ((kk < j) ? 0.f : -p[kk])) : -p[kk];
 #pragma unroll
       for (int i = kk + 1; i < 16; ++i) p[i] += Ab[i * kLD + kk] * t[kk];
     }
-    float *Tb = TF + o * kLD + o + j;
+    if (diag) {
+      float *Tb = TF + (bi * 16) * kLD + bi * 16 + j;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) Tb[i * kLD] = t[i];
+      for (int i = 0; i < 16; ++i) Tb[i * kLD] = t[i];
+    } else {
+      float *Gb = XS + sl * 16 * kGLD + j;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) Gb[i * kGLD] = t[i];
+    }
   }
   __syncthreads();
   const int r = (tid & 63) >> 2, c0 = (tid & 3) * 4, g = tid >> 6;
@@ -208,21 +223,6 @@ __device__ __forceinline__ void blocked_unit_lower_inverse(const float *AF, floa
     *reinterpret_cast<float4 *>(TF + (bi * 16 + r) * kLD + bj * 16 + c0) =
         make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
   };
-  // G_im = T_ii A_im, slots 0..5: (1,0) (2,1) (3,2) (2,0) (3,1) (3,0)
-  for (int w = tid; w < 6 * 64; w += 256) {
-    const int sl = w >> 6;
-    const int bi = sl < 3 ? sl + 1 : (sl == 5 ? 3 : sl - 1);
-    const int bj = sl < 3 ? sl : (sl == 5 ? 0 : sl - 3);
-    const int rr = (w & 63) >> 2, cc = (w & 3) * 4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float *lrow = TF + (bi * 16 + rr) * kLD + bi * 16;
-    const float *rblk = AF + (bi * 16) * kLD + bj * 16 + cc;
-#pragma unroll
-    for (int s2 = 0; s2 < 16; ++s2)
-      fma4(acc, lrow[s2], *reinterpret_cast<const float4 *>(rblk + s2 * kLD));
-    *reinterpret_cast<float4 *>(XS + sl * 16 * kGLD + rr * kGLD + cc) = acc;
-  }
-  __syncthreads();
   if (g < 3) {                                   // T_10, T_21, T_32 = -G_(i+1)i T_ii
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     strip(acc, gs(g), tb(g, g));
