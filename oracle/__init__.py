@@ -205,6 +205,27 @@ def input_maps(q=None, k=None, beta_logit=None):
     return out_q, out_k, out_b
 
 
+def attn_res(V, w, eps=1e-6):
+    """Depth mixing of AttnRes ("22,580: From GPT-2 to Kimi K3"
+    (yichencityu.github.io), section 12, block_attn_res), in float64.
+
+    V: [N+1, ..., D], the stacked block representations (blocks and the
+    partial block); w: [D], the learned scoring vector.  Keys are the
+    RMS-normalised values, K_n = V_n / sqrt(mean(V_n^2) + eps) (the pages'
+    `norm`, read as the RMSNorm they use elsewhere, without a learned scale);
+    logits_n = w . K_n; a = softmax over the block axis; h = sum_n a_n V_n.
+    Returns h [..., D] as float64.
+    """
+    V = np.asarray(V, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    K = V / np.sqrt((V * V).mean(axis=-1, keepdims=True) + eps)
+    logits = K @ w                                   # [N+1, ...]
+    logits = logits - logits.max(axis=0, keepdims=True)
+    a = np.exp(logits)
+    a = a / a.sum(axis=0, keepdims=True)
+    return (a[..., None] * V).sum(axis=0)
+
+
 def _alpha_slice(log_alpha, mode, b, h):
     if mode == ALPHA_NONE or log_alpha is None:
         return None
