@@ -471,6 +471,35 @@ def run_ours(args, rank, world, local, dist):
         del S, pool, od
         torch.cuda.empty_cache()
 
+    # ---- AttnRes depth mixing: 9 stacked blocks (8 AttnRes blocks and the
+    # partial one) of 4096 tokens x 7168, bf16; HBM-bound
+    ar_nb, ar_rows, ar_D = 9, 4096, 7168
+    g = torch.Generator(device=dev).manual_seed(5)
+    Var = torch.randn((ar_nb, ar_rows, ar_D), device=dev, generator=g).to(torch.bfloat16)
+    war = torch.randn(ar_D, device=dev, generator=g) / ar_D ** 0.5
+    har = torch.empty((ar_rows, ar_D), dtype=torch.bfloat16, device=dev)
+    for _ in range(args.warmup):
+        kda.kda_attn_res(Var, war, har, 1e-6, stream)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ar_steps = max(args.steps, 10)
+    barrier(dist, torch)
+    a.record(stream)
+    for _ in range(ar_steps):
+        kda.kda_attn_res(Var, war, har, 1e-6, stream)
+    b.record(stream)
+    barrier(dist, torch)
+    ar_ms = max_over_ranks(a.elapsed_time(b) / ar_steps, dist, dev)
+    ar_bytes = (ar_nb + 1) * ar_rows * ar_D * 2 + ar_D * 4
+    attn_res = {"workload": f"n_blocks={ar_nb} rows={ar_rows} D={ar_D} bf16 (synthetic; the pages "
+                            f"give the block count, not the model width)",
+                "value": world * ar_bytes / (ar_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "us_per_call": ar_ms * 1e3, "steps": ar_steps,
+                "roofline": {"kernel": "attn_res_kernel", "bound": "hbm", "unit": "GB/s",
+                             "achieved": ar_bytes / (ar_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+                             "frac": ar_bytes / (ar_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                             "algorithmic_bytes_per_launch": ar_bytes}}
+    del Var, war, har
+
     # ---- CPU baseline (rank 0, one GPU only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -497,7 +526,7 @@ def run_ours(args, rank, world, local, dist):
                            "parallelism": f"replicas x{world}"},
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches_per_call * args.steps,
-                "clocks": clocks, "decode": dec, "variants": variants}
+                "clocks": clocks, "decode": dec, "variants": variants, "attn_res": attn_res}
         print(json.dumps(line), flush=True)
     return 0
 

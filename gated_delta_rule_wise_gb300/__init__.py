@@ -26,7 +26,7 @@ __all__ = [
     "kda_chunk_fwd_launches", "kda_chunk_fwd_kernel_names", "kernel_sources",
     "kda_chunk_fwd_host", "kda_chunk_fwd_host_buffer_size", "host_buffer_for",
     "kda_chunk_fwd_rule", "KDA_RULE_DELTA", "KDA_RULE_LINEAR", "KDA_MAP_QK_SILU_NORM",
-    "KDA_MAP_BETA_SIGMOID",
+    "KDA_MAP_BETA_SIGMOID", "kda_attn_res", "attn_res",
     "chunk_fwd", "decode_step", "workspace_for",
     "KDA_F32", "KDA_BF16", "KDA_ALPHA_NONE", "KDA_ALPHA_SCALAR", "KDA_ALPHA_CHANNEL",
     "KDA_PATH_AUTO", "KDA_PATH_CUDA_CORE", "KDA_PATH_TENSOR",
@@ -91,6 +91,8 @@ def load_library():
         lib.kda_decode_step.argtypes = [_P] * 7 + [_I] * 6 + [_P]
         lib.kda_chunk_fwd_rule.restype = _I
         lib.kda_chunk_fwd_rule.argtypes = chunk_args[:16] + [_I, ctypes.c_uint] + chunk_args[16:]
+        lib.kda_attn_res.restype = _I
+        lib.kda_attn_res.argtypes = [_P, _I, _P, _P, ctypes.c_longlong, _I, _I, ctypes.c_float, _P]
         lib.kda_chunk_fwd_host_buffer_size.restype = _SZ
         lib.kda_chunk_fwd_host_buffer_size.argtypes = [_I] * 9
         lib.kda_chunk_fwd_host.restype = _I
@@ -203,6 +205,23 @@ def kda_chunk_fwd_rule(q, k, v, beta, log_alpha, h0, o, hT, C, workspace, rule=K
     _check(st, "kda_chunk_fwd_rule")
 
 
+def kda_attn_res(V, w, h, eps=1e-6, stream=None):
+    """AttnRes depth mixing: V [n_blocks, ..., D] (float32 or bf16), w [D]
+    float32, h [..., D] of V's dtype (written)."""
+    nb, D = V.shape[0], V.shape[-1]
+    rows = V[0].numel() // D
+    st = load_library().kda_attn_res(_ptr(V), nb, _ptr(w), _ptr(h), rows, D, _dtype_code(V),
+                                     float(eps), _stream(stream))
+    _check(st, "kda_attn_res")
+
+
+def attn_res(V, w, eps=1e-6, stream=None):
+    """Allocate h and run ``kda_attn_res``; returns h [..., D]."""
+    h = torch.empty(V.shape[1:], dtype=V.dtype, device=V.device)
+    kda_attn_res(V, w, h, eps, stream)
+    return h
+
+
 def _host_ptr(t):
     if t is None:
         return None
@@ -263,6 +282,7 @@ KERNEL_SOURCES = {
     "decode_step_kernel": ["kda_decode.cu"],
     "kda_prep_kernel": ["kda_chunk_tc.cu"],
     "kda_scan_kernel": ["kda_chunk_tc.cu"],
+    "attn_res_kernel": ["kda_attnres.cu"],
 }
 
 

@@ -234,6 +234,25 @@ kda_status kda_chunk_fwd_rule(const void *q, const void *k, const void *v,
                               kda_stream_t stream);
 
 /*
+ * AttnRes depth mixing ("22,580: From GPT-2 to Kimi K3"
+ * (yichencityu.github.io), section 12, block_attn_res): for every row r,
+ *
+ *   K_n = V_n / sqrt(mean_d(V_n^2) + eps)          RMS-normalised keys
+ *   a_n = softmax over n of (w . K_n)              over the block axis
+ *   h   = sum_n a_n V_n
+ *
+ *   V   [n_blocks, rows, D]  dtype dt   the stacked block representations
+ *   w   [D]                  float32    the learned scoring vector
+ *   h   [rows, D]            dtype dt   output
+ *
+ * The pages' `norm` is read as RMSNorm without a learned scale.  1 <= n_blocks
+ * <= 32 and D a multiple of 8 (else KDA_ERR_UNSUPPORTED); eps >= 0; pointers
+ * 16-byte aligned.  Arithmetic in float32.  Asynchronous on `stream`.
+ */
+kda_status kda_attn_res(const void *V, int n_blocks, const float *w, void *h,
+                        long long rows, int D, kda_dtype dt, float eps, kda_stream_t stream);
+
+/*
  * kda_chunk_fwd for inputs and outputs in HOST memory, with the transfers
  * overlapped with the prefill.  The pages have no counterpart (they do not
  * discuss where the inputs live); the prefill itself is kda_chunk_fwd.
