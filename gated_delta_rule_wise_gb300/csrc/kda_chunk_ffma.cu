@@ -14,6 +14,7 @@
 //   A  = strict_lower(diag(beta) Kg Kh^T),  M = lower_incl(Qg Kh^T)
 //   [W | U] = (I + A)^-1 [diag(beta) Kg | diag(beta) V]   (forward substitution)
 //   u = U - W S;   o = Qg S + M u;   S = Diag(gamma_C) (S + Kh^T u)
+// (the tiles are kept relative to gamma at mid-chunk; see step 1)
 // With no decay this is the chunked DeltaNet loop of "22,580: From GPT-2 to
 // Kimi K3" (yichencityu.github.io), section 6.3 (forward substitution on the
 // C x C unit lower-triangular matrix, W = T K_beta, U = T V_beta, then
@@ -39,7 +40,7 @@ struct FfmaSmem {
   static size_t floats(int C, int DVB) {
     const int LDC = C + 1, LDV = DVB + 1;
     return (size_t)4 * C * LDK + (size_t)2 * C * LDC + (size_t)2 * C * LDV +
-           (size_t)DK * LDV + DK + C;
+           (size_t)DK * LDV + 3 * DK + C;
   }
 };
 
@@ -63,7 +64,9 @@ chunk_ffma_kernel(const TI *__restrict__ q, const TI *__restrict__ k,
   float *Vu = Ub + C * LDV;         // [C][LDV]  V, then u
   float *Sm = Vu + C * LDV;         // [DK][LDV] state block
   float *gC = Sm + DK * LDV;        // [DK]      gamma at chunk end
-  float *bet = gC + DK;             // [C]       beta (0 on padded rows)
+  float *gCm = gC + DK;             // [DK]      gamma at chunk end / gamma at mid-chunk
+  float *em = gCm + DK;             // [DK]      gamma at mid-chunk
+  float *bet = em + DK;             // [C]       beta (0 on padded rows)
 
   const int tid = threadIdx.x;
   const int bh = blockIdx.y;
@@ -84,27 +87,38 @@ chunk_ffma_kernel(const TI *__restrict__ q, const TI *__restrict__ k,
     __syncthreads();  // previous chunk finished with every tile
 
     // (1) decay prefix in log space, decayed tiles; one thread per key channel.
+    // The tiles carry gamma relative to its value m at the middle of the chunk
+    // (the split factors e^(g-m), e^(m-g) stay within the half chunk's decay,
+    // so they stay finite up to about e^87 per half chunk); A and M only see
+    // ratios, and the chunk-start values are restored where they are needed.
     if (tid < DK) {
       const int c = tid;
-      float acc = 0.f;
+      auto ld_of = [&](int r) -> float {
+        if (r >= valid) return 0.f;
+        if (alpha_mode == KDA_ALPHA_CHANNEL)
+          return log_decay_of(log_alpha[qk_base + (size_t)(t0 + r) * DK + c]);
+        if (alpha_mode == KDA_ALPHA_SCALAR) return log_decay_of(log_alpha[(size_t)bh * T + t0 + r]);
+        return 0.f;
+      };
+      float mid = 0.f;
+      for (int r = 0; r < C / 2; ++r) mid += ld_of(r);
+      float acc = -mid;
       for (int r = 0; r < C; ++r) {
-        float kv = 0.f, qv = 0.f, ld = 0.f;
+        float kv = 0.f, qv = 0.f;
         if (r < valid) {
           const size_t e = qk_base + (size_t)(t0 + r) * DK + c;
           kv = Io<TI>::ld(k + e);
           qv = Io<TI>::ld(q + e);
-          if (alpha_mode == KDA_ALPHA_CHANNEL)
-            ld = log_decay_of(log_alpha[e]);
-          else if (alpha_mode == KDA_ALPHA_SCALAR)
-            ld = log_decay_of(log_alpha[(size_t)bh * T + t0 + r]);
         }
-        acc += ld;
+        acc += ld_of(r);
         const float gm = expf(acc), gi = expf(-acc);
         Kg[r * LDK + c] = kv * gm;
         Kh[r * LDK + c] = kv * gi;
         Qg[r * LDK + c] = qv * gm;
       }
-      gC[c] = expf(acc);
+      gC[c] = expf(acc + mid);
+      gCm[c] = expf(acc);
+      em[c] = expf(mid);
     }
     for (int r = tid; r < C; r += kFfmaThreads)
       bet[r] = (r < valid) ? beta[(size_t)bh * T + t0 + r] : 0.f;
@@ -131,7 +145,7 @@ chunk_ffma_kernel(const TI *__restrict__ q, const TI *__restrict__ k,
     }
     for (int idx = tid; idx < C * DK; idx += kFfmaThreads) {
       const int r = idx / DK, c = idx % DK;
-      Wm[r * LDK + c] = bet[r] * Kg[r * LDK + c];
+      Wm[r * LDK + c] = bet[r] * Kg[r * LDK + c] * em[c];  // beta K gamma, chunk-start gamma
     }
     for (int idx = tid; idx < C * DVB; idx += kFfmaThreads) {
       const int r = idx / DVB, j = idx % DVB;
@@ -174,7 +188,7 @@ chunk_ffma_kernel(const TI *__restrict__ q, const TI *__restrict__ k,
       if (r < valid) {
         float acc = 0.f;
         const float *qr = Qg + r * LDK;
-        for (int c = 0; c < DK; ++c) acc += qr[c] * Sm[c * LDV + j];
+        for (int c = 0; c < DK; ++c) acc += qr[c] * em[c] * Sm[c * LDV + j];
         const float *mr = Mm + r * LDC;
         for (int m = 0; m <= r; ++m) acc += mr[m] * Vu[m * LDV + j];
         Io<TI>::st(o + v_base + (size_t)(t0 + r) * dv + j0 + j, acc);
@@ -182,12 +196,12 @@ chunk_ffma_kernel(const TI *__restrict__ q, const TI *__restrict__ k,
     }
     __syncthreads();
 
-    // (7) S = Diag(gamma_C) (S + Kh^T u)
+    // (7) S = Diag(gamma_C) S + Kbar^T u, Kbar = K gamma_C / gamma = Kh gamma_C / gamma_mid
     for (int idx = tid; idx < DK * DVB; idx += kFfmaThreads) {
       const int c = idx / DVB, j = idx % DVB;
-      float acc = Sm[c * LDV + j];
+      float acc = 0.f;
       for (int r = 0; r < C; ++r) acc += Kh[r * LDK + c] * Vu[r * LDV + j];
-      Sm[c * LDV + j] = gC[c] * acc;
+      Sm[c * LDV + j] = gC[c] * Sm[c * LDV + j] + gCm[c] * acc;
     }
   }
   __syncthreads();

@@ -712,8 +712,9 @@ struct PrepSmem128 {
   static constexpr uint32_t RA = X1 + 65536;
   static constexpr uint32_t EG = RA, AF = RA, TF = RA + kC * kLD * 4, MM = RA;
   static constexpr uint32_t TT = align1k(RA + 2 * kC * kLD * 4);  // T bf16; solve scratch before
-  static constexpr uint32_t GCS = TT + kC * kC * 2;  // gamma_C float [D]
-  static constexpr uint32_t BETA = GCS + D * 4;      // float [C]
+  static constexpr uint32_t GCS = TT + kC * kC * 2;  // gamma_C / gamma_mid float [D]
+  static constexpr uint32_t GMID = GCS + D * 4;      // gamma_mid float [D]
+  static constexpr uint32_t BETA = GMID + D * 4;     // float [C]
   static constexpr uint32_t PART = BETA + kC * 4;    // float [2][D]
   static constexpr uint32_t BAR = PART + 2 * D * 4;
   static constexpr uint32_t LBAR = BAR + 8;   // log_alpha, k, v rows landed
@@ -762,6 +763,7 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
   uint8_t *TT = sm + L::TT, *MM = sm + L::MM, *X1 = sm + L::X1;
   const uint8_t *rawq = sm + L::RAWQ, *rawk = sm + L::RAWK, *rawv = sm + L::RAWV;
   float *gcs = reinterpret_cast<float *>(sm + L::GCS);
+  float *gmid = reinterpret_cast<float *>(sm + L::GMID);
   float *betas = reinterpret_cast<float *>(sm + L::BETA);
   float *part = reinterpret_cast<float *>(sm + L::PART);
   uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::BAR);
@@ -889,17 +891,21 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
     part[half * D + c] = psum;
     __syncthreads();
     {
+      // gamma measured from the middle of the chunk (g at row C/2 - 1 = p0):
+      // the split factors gamma and 1/gamma then stay within exp(|half-chunk
+      // decay|), so float and bf16 hold them up to a decay of about 87 per
+      // half chunk; the chunk-start values are restored where they are needed
       const float p0 = part[c], p1 = part[D + c];
-      float g = half ? p0 : 0.f;
+      float g = half ? 0.f : -p0;
 #pragma unroll
       for (int i = 0; i < R; ++i) {
         g += ld[i];
         EG[(r0 + i) * D + c] = __expf(g);
       }
       if (half == 0) {
-        const float e = __expf(p0 + p1);
-        gcs[c] = e;
-        reinterpret_cast<float *>(recg + Rr::GC)[c] = e;
+        gcs[c] = __expf(p1);   // gamma_C / gamma_mid: scales (K/gamma)^T into Kbar^T
+        gmid[c] = __expf(p0);  // gamma_mid: turns Q*gamma (mid-referenced) into Q*gamma
+        reinterpret_cast<float *>(recg + Rr::GC)[c] = __expf(p0 + p1);
       }
     }
     if (ok && !ptx::mbar_wait(qbar, it & 1, kWaitLimit)) {
@@ -1044,6 +1050,15 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
       ptx::tmem_ld32_halves<64>(t_lane + colhalf * 128 + 32, y);
       ptx::tmem_ld_wait();
       const int c8 = (colhalf * 128 + side * 64) >> 3;  // first chunk of this thread's 64 columns
+      if (colhalf == 0) {  // W: K_beta carried gamma / gamma_mid; back to chunk-start gamma
+        const float4 *gm = reinterpret_cast<const float4 *>(gmid + side * 64);
+#pragma unroll
+        for (int j4 = 0; j4 < 8; ++j4) {
+          const float4 a = gm[j4], b = gm[8 + j4];
+          x[4 * j4] *= a.x; x[4 * j4 + 1] *= a.y; x[4 * j4 + 2] *= a.z; x[4 * j4 + 3] *= a.w;
+          y[4 * j4] *= b.x; y[4 * j4 + 1] *= b.y; y[4 * j4 + 2] *= b.z; y[4 * j4 + 3] *= b.w;
+        }
+      }
 #pragma unroll
       for (int j8 = 0; j8 < 4; ++j8) st_chunk(X1, rr, c8 + j8, 128, x + 8 * j8);
 #pragma unroll
@@ -1158,8 +1173,11 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
         for (int cc = 0; cc < 8; ++cc) {  // this thread's K atom is `side`
           float qg[8];
           ld_chunk(X1, kC + rr, side * 8 + cc, 128, qg);
+          const float4 m0 = *reinterpret_cast<const float4 *>(gmid + side * 64 + cc * 8);
+          const float4 m1 = *reinterpret_cast<const float4 *>(gmid + side * 64 + cc * 8 + 4);
+          const float gm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
 #pragma unroll
-          for (int j = 0; j < 8; ++j) qg[j] -= x[8 * cc + j];
+          for (int j = 0; j < 8; ++j) qg[j] = qg[j] * gm[j] - x[8 * cc + j];
           *reinterpret_cast<uint4 *>(stg + side * 2048 + row * 128 + ((cc ^ (row & 7)) << 4)) =
               pack8(qg);
         }

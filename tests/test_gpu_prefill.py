@@ -163,6 +163,18 @@ def test_prefill_then_decode_equals_longer_prefill():
     assert rel_err(S.cpu().numpy(), h_long.cpu().numpy()) <= 1e-2
 
 
+@pytest.mark.parametrize("path", ["auto", "cuda_core"])
+def test_strong_decay(path):
+    """Fast-forgetting channels: exp(log_alpha) about 1.7 per token, so one
+    64-token chunk decays by about e^-108 per channel.  On the d = 128 tensor
+    path the split factors e^g and e^-g are taken from the middle of the
+    chunk, which keeps them inside float range up to about e^-87 per half
+    chunk; a chunk-start reference would overflow here."""
+    w = W.Prefill("strong", B=1, H=2, T=3 * 64 + 20, dk=128, dv=128, C=64, dtype="bf16",
+                  alpha="channel", la_mu=0.4, la_sd=0.5, h0_sd=0.05, seed=77)
+    check_full(w, path)
+
+
 def test_identity_and_no_decay_limits():
     """beta = 0 with no decay leaves S = h0; log_alpha = -inf equals no decay."""
     w = W.GDN_BF16.with_(B=1, H=2, T=200, seed=3)
