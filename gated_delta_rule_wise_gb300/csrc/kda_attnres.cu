@@ -182,6 +182,7 @@ attn_res_fixed_kernel(const T *__restrict__ V, const float *__restrict__ w, T *_
     float dot[NB], ss[NB];
 #pragma unroll
     for (int n = 0; n < NB; ++n) dot[n] = ss[n] = 0.f;
+#pragma unroll 2
     for (int pc = tid; pc < npieces; pc += kAttnThreads) {
       float x[NB][E];
 #pragma unroll
@@ -240,6 +241,7 @@ attn_res_fixed_kernel(const T *__restrict__ V, const float *__restrict__ w, T *_
 #pragma unroll
     for (int n = 0; n < NB; ++n) al[n] = alpha[n];
     T *hr = h + (size_t)row * D;
+#pragma unroll 2
     for (int pc = tid; pc < npieces; pc += kAttnThreads) {
       float x[NB][E];
 #pragma unroll

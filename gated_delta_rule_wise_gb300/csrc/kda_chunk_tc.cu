@@ -707,10 +707,13 @@ struct PrepSmem128 {
   // phase 6 on.  Before phase 1 blocks 0, 2 and 3 receive the raw q, k and v rows.
   static constexpr uint32_t X1 = 0;
   static constexpr uint32_t RAWQ = X1, RAWK = X1 + 32768, RAWV = X1 + 49152;
-  // R_A: log_alpha, then gamma, as float [C][D] (phases 0-1) | A, T float (3-4) |
-  // M tile (4-9)
+  // R_A: log_alpha as float [C][D], then gamma in two channel planes (channels
+  // 8k..8k+3 | 8k+4..8k+7 of each row; the second plane 64 B further, so the
+  // per-channel writes and the 16-byte row reads are both conflict-free)
+  // (phases 0-1) | A, T float (3-4) | M tile (4-9)
   static constexpr uint32_t RA = X1 + 65536;
   static constexpr uint32_t EG = RA, AF = RA, TF = RA + kC * kLD * 4, MM = RA;
+  static constexpr uint32_t EG_PLANE = kC * (D / 2) * 4 + 64;  // bytes from plane 0 to plane 1
   static constexpr uint32_t TT = align1k(RA + 2 * kC * kLD * 4);  // T bf16; solve scratch before
   static constexpr uint32_t GCS = TT + kC * kC * 2;  // gamma_C / gamma_mid float [D]
   static constexpr uint32_t GMID = GCS + D * 4;      // gamma_mid float [D]
@@ -722,7 +725,8 @@ struct PrepSmem128 {
   static constexpr uint32_t TMEMP = QBAR + 8;
   static constexpr uint32_t BYTES = TMEMP + 8;
   static constexpr uint32_t TMEM_COLS = 256;
-  static_assert(kC * D * 4 <= 2 * kC * kLD * 4, "gamma tile fits R_A");
+  static_assert(kC * D * 4 <= 2 * kC * kLD * 4 && EG_PLANE + kC * (D / 2) * 4 <= 2 * kC * kLD * 4,
+                "log_alpha and gamma tiles fit R_A");
   static_assert(kC * kC * 2 <= kC * kLD * 4, "M tile fits A's space");
   static_assert((RA & 1023u) == 0 && (TT & 1023u) == 0, "tile alignment");
   // two CTAs per SM: 228 KB per SM, 1 KB reserved per CTA, 1 KB alignment slack
@@ -900,7 +904,8 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
 #pragma unroll
       for (int i = 0; i < R; ++i) {
         g += ld[i];
-        EG[(r0 + i) * D + c] = __expf(g);
+        EG[((c >> 2) & 1) * (L::EG_PLANE / 4) + (r0 + i) * (D / 2) + (c >> 3) * 4 + (c & 3)] =
+            __expf(g);
       }
       if (half == 0) {
         gcs[c] = __expf(p1);   // gamma_C / gamma_mid: scales (K/gamma)^T into Kbar^T
@@ -957,8 +962,9 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
           kf[e] *= ik;
         }
       }
-      const float4 e0 = *reinterpret_cast<const float4 *>(EG + r * D + c8 * 8);
-      const float4 e1 = *reinterpret_cast<const float4 *>(EG + r * D + c8 * 8 + 4);
+      const float4 e0 = *reinterpret_cast<const float4 *>(EG + r * (D / 2) + c8 * 4);
+      const float4 e1 =
+          *reinterpret_cast<const float4 *>(EG + L::EG_PLANE / 4 + r * (D / 2) + c8 * 4);
       eg[0] = e0.x; eg[1] = e0.y; eg[2] = e0.z; eg[3] = e0.w;
       eg[4] = e1.x; eg[5] = e1.y; eg[6] = e1.z; eg[7] = e1.w;
       const float bt = betas[r];
