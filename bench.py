@@ -497,6 +497,10 @@ def run_ours(args, rank, world, local, dist):
                 "roofline": {"kernel": "attn_res_kernel", "bound": "hbm", "unit": "GB/s",
                              "achieved": ar_bytes / (ar_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
                              "frac": ar_bytes / (ar_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                             "peak_source": f"{peak_src} hbm_gbs (burst copy)",
+                             "traffic": recorded_traffic(
+                                 "attn_res_kernel",
+                                 kernel_source_hash(kda.kernel_sources("attn_res_kernel"))),
                              "algorithmic_bytes_per_launch": ar_bytes}}
     del Var, war, har
 

@@ -21,17 +21,19 @@
 //   S' = (Diag(gamma_C) + Ap) S + Kbar^T U,      Ap = -Kbar^T W   (D x D)
 //   o  = Qp S + M U,                              Qp = Q*gamma - M W  (C x D)
 // Everything except S is known per chunk before the pass starts, so
-//  - kda_prep_kernel (one CTA per chunk, fully parallel) computes the decay
-//    prefix, the decayed tiles, A and M (one tcgen05 MMA), T by forward
-//    substitution in shared memory, W and U (tcgen05), Ap and M W (tcgen05),
-//    and writes Ap, Qp, Kbar^T, M, U^T and gamma_C for the chunk to the
-//    workspace, already in the swizzled operand layout;
-//  - kda_scan_kernel (one CTA per (head, block of NB value columns)) keeps S
-//    in tensor memory as float32 and, per chunk, scales it by gamma_C in
-//    place, writes a bf16 copy as the MMA operand, and runs
-//    S += Ap S + Kbar^T U and o = Qp S + M U as tcgen05 MMAs on operands
-//    double-buffered by bulk copies.  One MMA round trip per chunk sits on
-//    the serial path.
+//  - kda_prep_kernel (persistent CTAs, chunks taken in turn, fully parallel)
+//    computes the decay prefix, the decayed tiles, A and M (one tcgen05 MMA
+//    group), T by a blocked inverse in shared memory, W and U, then the
+//    chunk's record: for D = 128 Ap and Qp as swizzled operand tiles and the
+//    additive terms B = Kbar^T U and O = M U already multiplied out; for
+//    D = 64 Ap, Qp, Kbar^T, M and U^T tiles.  gamma_C closes each record.
+//  - kda_scan_kernel (one CTA per (head, block of NB value columns)) walks the
+//    chunks in order with the records streamed in by bulk copies; per chunk
+//    it writes a bf16 copy of S as the MMA operand, forms
+//    S' = gamma_C S + B + Ap S (one group of tcgen05 MMAs) and, off the
+//    serial path, o = Qp S + O.  One MMA round trip per chunk sits on the
+//    serial path.
+// The D = 128 kernels are described in detail above prep_d128 and scan_d128.
 // A partial last chunk is padded with k = q = v = 0, beta = 0, a = 1, which
 // adds nothing; padded rows of o are not stored.
 #include <type_traits>
@@ -76,7 +78,7 @@ struct Rec<128> {
   static constexpr uint32_t OI = 81920;    // O     [4][C][32] bf16
   static constexpr uint32_t GC = 98304;    // gamma_C [128] float
   static constexpr uint32_t BYTES = 98816;
-  static constexpr uint32_t PRE = BI;      // Ap | Qp^T
+  static constexpr uint32_t PRE = BI;      // Ap | Qp
   static constexpr int BLK = 32;           // value columns per block of B and O
 };
 
@@ -112,39 +114,28 @@ __device__ __forceinline__ void ld_chunk(const uint8_t *tile, int row, int c8, i
 
 // ============================================================== prep kernel
 
-template <int D>
-struct PrepSmem {
-  using R = Rec<D>;
-  // Staging of the stored record (D = 64: the whole record; D = 128: Ap | Qp^T
-  // | gamma_C), and the operand tiles Kbar^T, M, U^T (inside the record for
-  // D = 64, separate for D = 128).
-  static constexpr uint32_t AP_S = 0;
-  static constexpr uint32_t QP_S = R::QP;
-  static constexpr uint32_t GC_S = (D == 128) ? R::PRE : R::GC;
-  static constexpr uint32_t KBT_S = (D == 128) ? align1k(R::PRE + D * 4) : Rec<64>::KBT;
-  static constexpr uint32_t MM_S = (D == 128) ? KBT_S + D * kC * 2 : Rec<64>::MM;
-  static constexpr uint32_t UT_S = (D == 128) ? MM_S + kC * kC * 2 : Rec<64>::UT;
-  static constexpr uint32_t STG_END = (D == 128) ? UT_S + D * kC * 2 : Rec<64>::BYTES;
-  static constexpr uint32_t X1 = align1k(STG_END);         // [K_beta; Q*gamma] [128 rows][D]
+// Shared memory of the D = 64 prep (one CTA per SM).
+struct PrepSmem64 {
+  static constexpr int D = 64;
+  using R = Rec<64>;
+  // the whole record is staged here and leaves with one bulk copy
+  static constexpr uint32_t AP_S = 0, QP_S = R::QP, GC_S = R::GC;
+  static constexpr uint32_t KBT_S = R::KBT, MM_S = R::MM, UT_S = R::UT;
+  static constexpr uint32_t X1 = align1k(R::BYTES);         // [K_beta; Q*gamma] [128 rows][D]
   static constexpr uint32_t TT = X1 + 128 * D * 2;         // T bf16 [C rows][C]; solve scratch before
   static constexpr uint32_t TF = TT + kC * kC * 2;         // T float [C][kLD] during the solve
   static constexpr uint32_t WT = TF;                       // W^T [D rows][C] afterwards
   static constexpr uint32_t AS = align1k(TF + kC * kLD * 4);  // A float [C][kLD]
-  // D = 128 keeps X2 and Khat in the Ap and Qp staging slots (both dead before
-  // Ap and Qp^T are written); D = 64 gives them their own space.
-  static constexpr uint32_t X2 = (D == 128) ? AP_S : AS + kC * kLD * 4;    // [K_beta^T; (beta V)^T] [2D rows][C]
-  static constexpr uint32_t KH = (D == 128) ? QP_S : X2 + 2 * D * kC * 2;  // K/gamma  [C rows][D]
-  // D = 128: [I | -M], the B operand of Qp^T = [(Q*gamma)^T | W^T] [I | -M]^T, in the
-  // Qp slot between Khat's last use and Qp^T's write.
-  static constexpr uint32_t IM = QP_S;
-  static constexpr uint32_t RAW = (D == 128) ? AS + kC * kLD * 4 : KH + kC * D * 2;  // q | k | v [C][D] bf16
+  static constexpr uint32_t X2 = AS + kC * kLD * 4;        // [K_beta^T; (beta V)^T] [2D rows][C]
+  static constexpr uint32_t KH = X2 + 2 * D * kC * 2;      // K/gamma  [C rows][D]
+  static constexpr uint32_t RAW = KH + kC * D * 2;         // q | k | v [C][D] bf16
   static constexpr uint32_t BETA = RAW + 3 * kC * D * 2;   // float [C]
   static constexpr uint32_t PART = BETA + kC * 4;          // float [4][D] partial decay sums
   static constexpr uint32_t BAR = PART + 4 * D * 4;        // mbarrier (MMA commits)
   static constexpr uint32_t LBAR = BAR + 8;                // mbarrier (raw loads)
   static constexpr uint32_t TMEMP = LBAR + 8;              // TMEM base address
   static constexpr uint32_t BYTES = TMEMP + 8;
-  static constexpr uint32_t TMEM_COLS = (D == 128) ? 512 : 128;
+  static constexpr uint32_t TMEM_COLS = 128;
   static_assert(kC * kLD * 4 >= D * kC * 2, "W^T must fit the float T region");
   static_assert((X2 & 1023u) == 0 && (KH & 1023u) == 0 && (AS & 1023u) == 0 && (TF & 1023u) == 0 &&
                     (KBT_S & 1023u) == 0 && (MM_S & 1023u) == 0 && (UT_S & 1023u) == 0,
@@ -262,7 +253,8 @@ __device__ __forceinline__ void blocked_unit_lower_inverse(const float *AF, floa
   }
 }
 
-// D = 64 prep (also the structure the D = 128 prep started from).
+// D = 64 prep: one CTA per SM, chunks taken in turn; the whole record is
+// staged in shared memory and leaves with one bulk copy.
 __device__ __forceinline__ void prep_d64(const __nv_bfloat16 *__restrict__ q,
                                          const __nv_bfloat16 *__restrict__ k,
                                          const __nv_bfloat16 *__restrict__ v,
@@ -271,7 +263,7 @@ __device__ __forceinline__ void prep_d64(const __nv_bfloat16 *__restrict__ q,
                                          int NC, int total, uint8_t *__restrict__ ws, uint8_t *sm) {
   constexpr int D = 64;
   using Rr = Rec<D>;
-  using L = PrepSmem<D>;
+  using L = PrepSmem64;
   constexpr int Q4 = 256 / D;          // threads per key channel
   constexpr int R = kC / Q4;           // rows per thread in the elementwise phase
   uint8_t *stg = sm;  // staging of the stored record
@@ -282,7 +274,6 @@ __device__ __forceinline__ void prep_d64(const __nv_bfloat16 *__restrict__ q,
   float *TF = reinterpret_cast<float *>(sm + L::TF);
   uint8_t *X2 = sm + L::X2;
   uint8_t *KH = sm + L::KH;
-  uint8_t *IM = sm + L::IM;
   uint8_t *rawq = sm + L::RAW, *rawk = rawq + kC * D * 2, *rawv = rawk + kC * D * 2;
   float *part = reinterpret_cast<float *>(sm + L::PART);
   uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::BAR);
@@ -319,9 +310,8 @@ __device__ __forceinline__ void prep_d64(const __nv_bfloat16 *__restrict__ q,
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_ptr;
   const uint32_t sX1 = ptx::smem_u32(X1), sKH = ptx::smem_u32(KH), sX2 = ptx::smem_u32(X2);
-  const uint32_t sTT = ptx::smem_u32(TT), sWT = ptx::smem_u32(WT), sIM = ptx::smem_u32(IM);
+  const uint32_t sTT = ptx::smem_u32(TT), sWT = ptx::smem_u32(WT);
   const uint32_t sKBT = ptx::smem_u32(sm + L::KBT_S);
-  const uint32_t sMMs = ptx::smem_u32(sm + L::MM_S), sUTs = ptx::smem_u32(sm + L::UT_S);
   if (tid == 0 && (int)blockIdx.x < total) issue_raw(blockIdx.x);
   uint32_t mma_phase = 0;
 
@@ -353,10 +343,9 @@ __device__ __forceinline__ void prep_d64(const __nv_bfloat16 *__restrict__ q,
   float *betas = reinterpret_cast<float *>(sm + L::BETA);
 
   for (int idx = blockIdx.x, it = 0; idx < total; idx += gridDim.x, ++it) {
-    const int bh = idx / NC, n = idx % NC;
+    const int n = idx % NC;
     const int t0 = n * kC;
     const int valid = min(kC, T - t0);
-    const size_t row0 = (size_t)bh * T + t0;
 
     // ---- (1) decay inputs (loaded during the previous chunk), then the raw rows
     float ld[R];
@@ -466,16 +455,6 @@ __device__ __forceinline__ void prep_d64(const __nv_bfloat16 *__restrict__ q,
           for (int j = 0; j < 16; ++j) mrow[j] = (cb + j <= r) ? x[j] : 0.f;
           st_chunk(sm + L::MM_S, r, cb >> 3, kC, mrow);
           st_chunk(sm + L::MM_S, r, (cb >> 3) + 1, kC, mrow + 8);
-          if (D == 128) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) mrow[j] = -mrow[j];
-            st_chunk(IM, r, 8 + (cb >> 3), kC, mrow);               // K atom 1: -M
-            st_chunk(IM, r, 8 + (cb >> 3) + 1, kC, mrow + 8);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) mrow[j] = (cb + j == r) ? 1.f : 0.f;
-            st_chunk(IM, r, cb >> 3, kC, mrow);                     // K atom 0: I
-            st_chunk(IM, r, (cb >> 3) + 1, kC, mrow + 8);
-          }
         }
       }
     }
@@ -516,11 +495,10 @@ __device__ __forceinline__ void prep_d64(const __nv_bfloat16 *__restrict__ q,
           float x[16];
           ptx::tmem_ld16(ta + 64 + 64 * h + cb, x);
           ptx::tmem_ld_wait();
-          // D = 128: h = 0 holds W^T rows (= lane), h = 1 U^T rows.
-          // D = 64:  lanes 0..63 W^T rows, lanes 64..127 U^T rows.
+          // lanes 0..63 W^T rows, lanes 64..127 U^T rows
           const int lane_row = tid;
-          const bool isW = (D == 128) ? (h == 0) : (lane_row < D);
-          const int row = (D == 128) ? lane_row : (lane_row % D);
+          const bool isW = lane_row < D;
+          const int row = lane_row % D;
           uint8_t *dst = isW ? WT : sm + L::UT_S;
           st_chunk(dst, row, cb >> 3, D, x);
           st_chunk(dst, row, (cb >> 3) + 1, D, x + 8);
@@ -532,34 +510,9 @@ __device__ __forceinline__ void prep_d64(const __nv_bfloat16 *__restrict__ q,
     __syncthreads();
     ptx::tc_fence_after();
 
-    // ---- (7) Kbar^T W, and Qp (D = 128: Qp^T directly; D = 64: M W)
+    // ---- (7) [Kbar^T; M] W
     if (tid == 0) {
-      if (D == 128) {
-        // cols [0, 128): Kbar^T W  (M = 128, N = 128)
-#pragma unroll
-        for (int ks = 0; ks < kC / 16; ++ks)
-          ptx::mma_bf16_ss(tmem, umma::sdesc_k(sKBT, D, ks), umma::sdesc_k(sWT, D, ks),
-                           umma::idesc_bf16(128, D), ks > 0);
-        // cols [128, 192): Qp^T = (Q*gamma)^T I - W^T M^T: A = [(Q*gamma)^T | W^T]
-        // (the first half read MN-major from the Q*gamma rows of X1), B^T = [I | -M]
-#pragma unroll
-        for (int ks = 0; ks < kC / 16; ++ks)
-          ptx::mma_bf16_ss(tmem + 128, umma::sdesc_mn(sX1 + 8192, 128, ks),
-                           umma::sdesc_k(sIM, kC, ks), umma::idesc_bf16_amn(128, kC), ks > 0);
-#pragma unroll
-        for (int ks = 0; ks < kC / 16; ++ks)
-          ptx::mma_bf16_ss(tmem + 128, umma::sdesc_k(sWT, D, ks),
-                           umma::sdesc_k(sIM, kC, 4 + ks), umma::idesc_bf16(128, kC), 1);
-        // cols [256, 384): B = Kbar^T U;  cols [384, 512): O = M U (M = 64 layout)
-#pragma unroll
-        for (int ks = 0; ks < kC / 16; ++ks)
-          ptx::mma_bf16_ss(tmem + 256, umma::sdesc_k(sKBT, D, ks), umma::sdesc_k(sUTs, D, ks),
-                           umma::idesc_bf16(128, D), ks > 0);
-#pragma unroll
-        for (int ks = 0; ks < kC / 16; ++ks)
-          ptx::mma_bf16_ss(tmem + 384, umma::sdesc_k(sMMs, kC, ks), umma::sdesc_k(sUTs, D, ks),
-                           umma::idesc_bf16(64, D), ks > 0);
-      } else {
+      {
         // cols [0, 64): [Kbar^T; M] W  (Kbar^T and M are adjacent in the record)
 #pragma unroll
         for (int ks = 0; ks < kC / 16; ++ks)
@@ -580,53 +533,7 @@ __device__ __forceinline__ void prep_d64(const __nv_bfloat16 *__restrict__ q,
     if (warp < 4) {
       const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16);
       const int lane_row = tid;
-      if (D == 128) {
-#pragma unroll
-        for (int cb = 0; cb < D; cb += 16) {
-          float x[16];
-          ptx::tmem_ld16(ta + cb, x);
-          ptx::tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) x[j] = -x[j];
-          st_chunk(stg + L::AP_S, lane_row, cb >> 3, D, x);
-          st_chunk(stg + L::AP_S, lane_row, (cb >> 3) + 1, D, x + 8);
-        }
-        // Qp^T: lane = key channel, column = token
-#pragma unroll
-        for (int cb = 0; cb < kC; cb += 16) {
-          float x[16];
-          ptx::tmem_ld16(ta + 128 + cb, x);
-          ptx::tmem_ld_wait();
-          st_chunk(stg + L::QP_S, lane_row, cb >> 3, D, x);
-          st_chunk(stg + L::QP_S, lane_row, (cb >> 3) + 1, D, x + 8);
-        }
-        // B and O straight to the record (plain row-major, 32-column blocks)
-        uint8_t *recg = ws + sizeof(WorkspaceHeader) + (size_t)idx * Rr::BYTES;
-        const int lane = tid & 31;
-        const int orow = warp * 16 + lane;  // M = 64 layout: lanes 32w + (0..15)
-#pragma unroll
-        for (int cb = 0; cb < D; cb += 16) {
-          float x[16], y[16];
-          ptx::tmem_ld16(ta + 256 + cb, x);
-          ptx::tmem_ld16(ta + 384 + cb, y);
-          ptx::tmem_ld_wait();
-          const uint32_t blk = (uint32_t)(cb >> 5), cin = (uint32_t)(cb & 31);
-          uint4 *db = reinterpret_cast<uint4 *>(recg + Rec<128>::BI + blk * (128u * 64u) +
-                                                (uint32_t)lane_row * 64u + cin * 2u);
-          db[0] = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]),
-                             pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
-          db[1] = make_uint4(pack_bf16x2(x[8], x[9]), pack_bf16x2(x[10], x[11]),
-                             pack_bf16x2(x[12], x[13]), pack_bf16x2(x[14], x[15]));
-          if (lane < 16) {
-            uint4 *dq = reinterpret_cast<uint4 *>(recg + Rec<128>::OI + blk * (uint32_t)(kC * 64) +
-                                                  (uint32_t)orow * 64u + cin * 2u);
-            dq[0] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
-                               pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
-            dq[1] = make_uint4(pack_bf16x2(y[8], y[9]), pack_bf16x2(y[10], y[11]),
-                               pack_bf16x2(y[12], y[13]), pack_bf16x2(y[14], y[15]));
-          }
-        }
-      } else {
+      {
 #pragma unroll
         for (int cb = 0; cb < D; cb += 16) {
           float x[16];
@@ -659,12 +566,7 @@ __device__ __forceinline__ void prep_d64(const __nv_bfloat16 *__restrict__ q,
     // the record region is written again)
     if (tid == 0) {
       uint8_t *dst = ws + sizeof(WorkspaceHeader) + (size_t)idx * Rr::BYTES;
-      if (D == 128) {
-        ptx::bulk_s2g(dst, stg, Rr::PRE);                           // Ap | Qp^T
-        ptx::bulk_s2g(dst + Rr::GC, stg + L::GC_S, D * 4);          // gamma_C
-      } else {
-        ptx::bulk_s2g(dst, stg, Rr::BYTES);
-      }
+      ptx::bulk_s2g(dst, stg, Rr::BYTES);
       ptx::bulk_commit();
     }
   }
@@ -696,7 +598,8 @@ __device__ __forceinline__ void prep_d64(const __nv_bfloat16 *__restrict__ q,
 //  (8) Ap = -gamma_C (K/gamma)^T W and B = gamma_C (K/gamma)^T U to the record
 //  (9) M [W | U]                                        4 MMAs (M = 64, N = 256)
 // (10) Qp = Q*gamma - M W and O = M U to the record.
-// Record tiles go to global memory straight from registers, already swizzled.
+// Each warp assembles its contiguous pieces of the record tiles in staging
+// slots of consumed shared memory and stores them with coalesced writes.
 // The next chunk's log_alpha, k and v rows are bulk-copied as soon as the last
 // product has read A's space and blocks 2-3 (after (9)), its q rows after (10).
 struct PrepSmem128 {
@@ -1718,7 +1621,7 @@ kda_status launch_d(const void *q, const void *k, const void *v, const float *be
                     int rule, unsigned maps) {
   constexpr int NB = scan_nb<D>();
   const int NC = (T + kC - 1) / kC;
-  const uint32_t prep_smem = (D == 128 ? PrepSmem128::BYTES : PrepSmem<64>::BYTES) + 1024;
+  const uint32_t prep_smem = (D == 128 ? PrepSmem128::BYTES : PrepSmem64::BYTES) + 1024;
   const uint32_t scan_smem =
       (D == 128 ? ScanSmem128<NB>::BYTES : ScanSmem64<NB>::BYTES) + 1024;
   auto prep = kda_prep_kernel<D, false>;
