@@ -1167,17 +1167,21 @@ struct ScanSmem64 {
   static constexpr uint32_t TMEM_COLS = NB <= 32 ? 32 : 64;
 };
 
-// D = 128: three warp groups.  A producer warp streams records through a ring
-// of kStages stages.  Four state warps own S (thread = key channel, its row in
+// D = 128: four roles.  A producer warp streams records through a ring of
+// kStages stages.  Four state warps own S (thread = key channel, its row in
 // registers as float): per chunk they write its bf16 copy (row-major, read
-// MN-major by the MMA), one of them issues P = Ap S into TMEM (8 MMAs), and
-// they form gamma_C * S + Kbar^T U while it runs, then add P.  Four output warps
-// (same TMEM lane quarters) issue o = Qp S into one of two output
-// accumulators as soon as the bf16 copy exists, wait for it, add M U and store
-// o.  Only the state products and the state conversion are on the serial
-// path.
+// MN-major by the MMA), signal the issuer, form gamma_C * S + Kbar^T U while
+// the product runs, then add P = Ap S.  One issuer warp issues every MMA of
+// the CTA from a single thread: P = Ap S (8 MMAs), then o = Qp S (8 MMAs)
+// into one of three output accumulators.  A tcgen05.mma costs about the
+// same issue time whatever its shape, and MMAs issued from several warps
+// serialise with a large penalty, so one issuer keeps the pipe in order: the
+// output products run while the state warps wait for P's completion and do
+// their own arithmetic.  Four output warps (same TMEM lane quarters) wait
+// for an output product, add M U and store o.
 constexpr int kStages = 3;
-constexpr int kScan128Threads = 288;  // 4 state warps, 4 output warps, 1 producer warp
+constexpr int kOutBufs = 3;
+constexpr int kScan128Threads = 320;  // 4 state warps, 4 output warps, producer, issuer
 template <int NB>
 struct ScanSmem128 {
   using R = Rec<128>;
@@ -1188,11 +1192,12 @@ struct ScanSmem128 {
   static constexpr uint32_t STAGE_BYTES = GC_S + 128 * 4;
   static constexpr uint32_t STAGE = align1k(STAGE_BYTES);
   static constexpr uint32_t SB = kStages * STAGE;            // 2 x bf16 S [128 rows][64 cols]
-  // full[3], empty[3], mS, sbready[2], mO[2]
+  // full[kStages], empty[kStages], mS, mO[kOutBufs], ofree[kOutBufs]
   static constexpr uint32_t BAR = SB + 2 * 128 * 64 * 2;
-  static constexpr uint32_t TMEMP = BAR + (2 * kStages + 5) * 8;
+  static constexpr uint32_t TMEMP = BAR + (2 * kStages + 1 + 2 * kOutBufs) * 8;
   static constexpr uint32_t BYTES = TMEMP + 8;
-  static constexpr uint32_t TMEM_COLS = 128;                 // S | o[0] | o[1]
+  static constexpr uint32_t TMEM_COLS = 128;                 // P | o[0] | o[1] | o[2]
+  static_assert(NB * (1 + kOutBufs) <= TMEM_COLS, "TMEM columns");
   static_assert(BYTES + 1024 <= 232448, "scan shared memory");
 };
 
@@ -1201,13 +1206,14 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
                                           float *__restrict__ hT, int T, int NC,
                                           uint8_t *__restrict__ ws, uint8_t *sm) {
   constexpr int D = 128;
+  constexpr uint32_t kSyncThreads = 128 + 32;  // state warps + issuer warp
   using R = Rec<128>;
   using L = ScanSmem128<NB>;
   uint64_t *full = reinterpret_cast<uint64_t *>(sm + L::BAR);
   uint64_t *empty = full + kStages;
   uint64_t *mS = empty + kStages;
-  uint64_t *sbready = mS + 1;
-  uint64_t *mO = sbready + 2;
+  uint64_t *mO = mS + 1;
+  uint64_t *ofree = mO + kOutBufs;
   uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(sm + L::TMEMP);
   WorkspaceHeader *hdr = reinterpret_cast<WorkspaceHeader *>(ws);
 
@@ -1219,12 +1225,12 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&full[s], 1);
-      ptx::mbar_init(&empty[s], 2);  // released by the state warps and by the output warps
+      ptx::mbar_init(&empty[s], 2);  // released by the issuer (state side) and by the output warps
     }
     ptx::mbar_init(mS, 1);
-    for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(&sbready[b], 1);
+    for (int b = 0; b < kOutBufs; ++b) {
       ptx::mbar_init(&mO[b], 1);
+      ptx::mbar_init(&ofree[b], 1);
     }
     ptx::fence_mbar_init();
   }
@@ -1244,7 +1250,7 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
     if (lane == 0) {
       for (int j = 0; j < NC; ++j) {
         const int s = j % kStages;
-        if (j >= kStages && ok && !ptx::mbar_wait(&empty[s], ((j / kStages) - 1) & 1, kWaitLimit)) {
+        if (j >= kStages && ok && !ptx::mbar_wait_fast(&empty[s], ((j / kStages) - 1) & 1, kWaitLimit)) {
           ok = false;
           report_error(hdr, KDA_ERR_TIMEOUT, 0x210u);
         }
@@ -1258,33 +1264,60 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
         ptx::bulk_g2s(st + L::GC_S, rec + R::GC, 128 * 4, &full[s]);
       }
     }
-  } else if (warp >= 4) {
-    // ---------------------------------------------------------- output warps
-    const int orow = (warp - 4) * 16 + lane;  // output row (M = 64 layout: lanes 32w + 0..15)
-    for (int j = 0; j < NC; ++j) {
-      const int b = j & 1;
-      if (tid == 128) {  // issue o = Qp S for chunk j once its bf16 S exists
-        if (ok && !ptx::mbar_wait(&sbready[b], (j >> 1) & 1, kWaitLimit)) {
-          ok = false;
-          report_error(hdr, KDA_ERR_TIMEOUT, 0x220u);
-        }
+  } else if (warp == 9) {
+    // ---------------------------------------------------------- issuer
+    for (int i = 0; i < NC; ++i) {
+      const int s = i % kStages, b = i % kOutBufs;
+      ptx::named_barrier(1, kSyncThreads);  // bf16 S_i written, P_{i-1} read by every state thread
+      if (lane == 0) {
         ptx::tc_fence_after();
-        const uint8_t *st = sm + (j % kStages) * L::STAGE;
-        const uint32_t sQP = ptx::smem_u32(st + R::QP), sSB = ptx::smem_u32(sb_of(j));
+        if (ok && !ptx::mbar_wait_fast(&full[s], (i / kStages) & 1, kWaitLimit)) {
+          ok = false;
+          report_error(hdr, KDA_ERR_TIMEOUT, 0x202u);
+        }
+        const uint8_t *st = sm + s * L::STAGE;
+        const uint32_t sAP = ptx::smem_u32(st + R::AP), sQP = ptx::smem_u32(st + R::QP);
+        const uint32_t sSB = ptx::smem_u32(sb_of(i));
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)  // P = Ap S   (S read MN-major)
+          ptx::mma_bf16_ss(tmem, umma::sdesc_k(sAP, D, ks), umma::sdesc_mn(sSB, 128, ks),
+                           umma::idesc_bf16_bmn(128, NB), ks > 0);
+        ptx::mma_commit(mS);
+        if (i > 0) ptx::mbar_arrive(&empty[(i - 1) % kStages]);  // state side done with chunk i-1
+        if (i >= kOutBufs && ok &&
+            !ptx::mbar_wait_fast(&ofree[b], ((i / kOutBufs) - 1) & 1, kWaitLimit)) {
+          ok = false;  // the output warps have read accumulator b (chunk i - kOutBufs)
+          report_error(hdr, KDA_ERR_TIMEOUT, 0x222u);
+        }
         const uint32_t tOc = tmem + NB * (1 + b);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)  // S read MN-major
+        for (int ks = 0; ks < D / 16; ++ks)  // o = Qp S
           ptx::mma_bf16_ss(tOc, umma::sdesc_k(sQP, kC, ks), umma::sdesc_mn(sSB, 128, ks),
                            umma::idesc_bf16_bmn(64, NB), ks > 0);
         ptx::mma_commit(&mO[b]);
       }
-      if (ok && !ptx::mbar_wait(&mO[b], (j >> 1) & 1, kWaitLimit)) {
+      __syncwarp();
+    }
+    if (lane == 0 && !ok) {  // after a timeout: let this thread's MMAs finish before TMEM is freed
+      ptx::mma_commit(mS);
+      ptx::mbar_wait(mS, NC & 1, kWaitLimit);
+    }
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------- output warps
+    const int orow = (warp - 4) * 16 + lane;  // output row (M = 64 layout: lanes 32w + 0..15)
+    for (int j = 0; j < NC; ++j) {
+      const int b = j % kOutBufs, s = j % kStages;
+      if (ok && !ptx::mbar_wait(&mO[b], (j / kOutBufs) & 1, kWaitLimit)) {
         ok = false;
         report_error(hdr, KDA_ERR_TIMEOUT, 0x221u);
       }
+      if (ok && !ptx::mbar_wait_fast(&full[s], (j / kStages) & 1, kWaitLimit)) {
+        ok = false;  // already complete: orders the record's bulk copy before the reads below
+        report_error(hdr, KDA_ERR_TIMEOUT, 0x223u);
+      }
       ptx::tc_fence_after();
       const uint32_t tO = t_lane + NB * (1 + b);
-      const uint8_t *oi = sm + (j % kStages) * L::STAGE + L::OI_S + (size_t)orow * NB * 2;
+      const uint8_t *oi = sm + s * L::STAGE + L::OI_S + (size_t)orow * NB * 2;
       const int t = j * kC + orow;
 #pragma unroll
       for (int cb = 0; cb < NB; cb += 16) {
@@ -1307,15 +1340,19 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
         }
       }
       ptx::tc_fence_before();
-      ptx::named_barrier(2, 128);  // all output rows of chunk j read before the buffer is reused
-      if (tid == 128) ptx::mbar_arrive(&empty[j % kStages]);
+      ptx::named_barrier(2, 128);  // all output rows of chunk j read
+      if (tid == 128) {
+        ptx::mbar_arrive(&ofree[b]);
+        ptx::mbar_arrive(&empty[s]);
+      }
     }
   } else {
     // ---------------------------------------------------------- state warps
     // Thread r keeps row r of S (key channel r, this CTA's NB value columns)
     // in registers as float.  Per chunk: its bf16 copy goes to the operand
-    // buffer, one thread issues P = Ap S into TMEM, and while the product
-    // runs each thread forms gamma_C S + B; then S <- that + P.
+    // buffer (free again: the products that read it two chunks ago completed
+    // before the last P), the issuer is told, each thread forms
+    // gamma_C S + B while the product runs, then S <- that + P.
     const int r = tid;  // key channel = TMEM lane
     const uint32_t tP = t_lane;
     float sr[NB];
@@ -1326,31 +1363,16 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
     }
     for (int i = 0; i < NC; ++i) {
       const int s = i % kStages;
-      uint8_t *st = sm + s * L::STAGE;
+      const uint8_t *st = sm + s * L::STAGE;
       uint8_t *sb = sb_of(i);
-      if (i > 1 && ok && !ptx::mbar_wait(&mO[i & 1], ((i - 2) >> 1) & 1, kWaitLimit)) {
-        ok = false;  // the bf16 copy of chunk i-2 has been read by its output products
-        report_error(hdr, KDA_ERR_TIMEOUT, 0x203u);
-      }
-      if (ok && !ptx::mbar_wait(&full[s], (i / kStages) & 1, kWaitLimit)) {
-        ok = false;
-        report_error(hdr, KDA_ERR_TIMEOUT, 0x202u);
-      }
 #pragma unroll
       for (int c8 = 0; c8 < NB / 8; ++c8) st_chunk(sb, r, c8, 128, sr + 8 * c8);
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
-      ptx::named_barrier(1, 128);  // bf16 S complete; every thread has read the last P
-      if (tid == 0) {
-        ptx::tc_fence_after();
-        const uint32_t sAP = ptx::smem_u32(st + R::AP), sSB = ptx::smem_u32(sb);
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)  // P = Ap S   (S read MN-major)
-          ptx::mma_bf16_ss(tmem, umma::sdesc_k(sAP, D, ks), umma::sdesc_mn(sSB, 128, ks),
-                           umma::idesc_bf16_bmn(128, NB), ks > 0);
-        ptx::mma_commit(mS);
-        ptx::mbar_arrive(&sbready[i & 1]);
-        if (i > 0) ptx::mbar_arrive(&empty[(i - 1) % kStages]);  // state side done with chunk i-1
+      ptx::named_arrive(1, kSyncThreads);
+      if (ok && !ptx::mbar_wait_fast(&full[s], (i / kStages) & 1, kWaitLimit)) {
+        ok = false;
+        report_error(hdr, KDA_ERR_TIMEOUT, 0x204u);
       }
       {  // gamma_C S + B while the product runs
         const float gam = reinterpret_cast<const float *>(st + L::GC_S)[r];

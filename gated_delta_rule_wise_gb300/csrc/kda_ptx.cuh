@@ -53,9 +53,30 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
   return false;
 }
 
+// Non-blocking test of the phase with the given parity, then the bounded
+// wait: a phase that has already completed costs one test instead of a
+// potentially suspending try_wait.
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_fast(uint64_t *bar, uint32_t parity, uint32_t limit) {
+  return mbar_test(bar, parity) || mbar_wait(bar, parity, limit);
+}
 // Barrier among `count` threads (a multiple of 32) under id `id` (1..15).
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// Arrive at named barrier `id` without waiting (producer side of a barrier
+// whose consumers call named_barrier with the same id and count).
+__device__ __forceinline__ void named_arrive(uint32_t id, uint32_t count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ---------------------------------------------------------------- TMA (bulk)
