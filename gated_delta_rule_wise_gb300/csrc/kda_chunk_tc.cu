@@ -1268,6 +1268,12 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
     // ---------------------------------------------------------- issuer
     for (int i = 0; i < NC; ++i) {
       const int s = i % kStages, b = i % kOutBufs;
+      // descriptors of the K-slices are the tile's descriptor plus a constant
+      // (shared memory addresses stay below 2^18): form them before the wait
+      const uint8_t *st = sm + s * L::STAGE;
+      const uint64_t dAP = umma::sdesc(ptx::smem_u32(st + R::AP));
+      const uint64_t dQP = umma::sdesc(ptx::smem_u32(st + R::QP));
+      const uint64_t dSB = umma::sdesc_mn(ptx::smem_u32(sb_of(i)), 128, 0);
       ptx::named_barrier(1, kSyncThreads);  // bf16 S_i written, P_{i-1} read by every state thread
       if (lane == 0) {
         ptx::tc_fence_after();
@@ -1275,13 +1281,10 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
           ok = false;
           report_error(hdr, KDA_ERR_TIMEOUT, 0x202u);
         }
-        const uint8_t *st = sm + s * L::STAGE;
-        const uint32_t sAP = ptx::smem_u32(st + R::AP), sQP = ptx::smem_u32(st + R::QP);
-        const uint32_t sSB = ptx::smem_u32(sb_of(i));
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)  // P = Ap S   (S read MN-major)
-          ptx::mma_bf16_ss(tmem, umma::sdesc_k(sAP, D, ks), umma::sdesc_mn(sSB, 128, ks),
-                           umma::idesc_bf16_bmn(128, NB), ks > 0);
+          ptx::mma_bf16_ss(tmem, dAP + (uint64_t)(((ks >> 2) * D * 128 + (ks & 3) * 32) >> 4),
+                           dSB + (uint64_t)(ks * 2048 >> 4), umma::idesc_bf16_bmn(128, NB), ks > 0);
         ptx::mma_commit(mS);
         if (i > 0) ptx::mbar_arrive(&empty[(i - 1) % kStages]);  // state side done with chunk i-1
         if (i >= kOutBufs && ok &&
@@ -1292,8 +1295,8 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
         const uint32_t tOc = tmem + NB * (1 + b);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)  // o = Qp S
-          ptx::mma_bf16_ss(tOc, umma::sdesc_k(sQP, kC, ks), umma::sdesc_mn(sSB, 128, ks),
-                           umma::idesc_bf16_bmn(64, NB), ks > 0);
+          ptx::mma_bf16_ss(tOc, dQP + (uint64_t)(((ks >> 2) * kC * 128 + (ks & 3) * 32) >> 4),
+                           dSB + (uint64_t)(ks * 2048 >> 4), umma::idesc_bf16_bmn(64, NB), ks > 0);
         ptx::mma_commit(&mO[b]);
       }
       __syncwarp();
