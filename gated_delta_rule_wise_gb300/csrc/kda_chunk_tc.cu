@@ -67,9 +67,11 @@ struct Rec<64> {
 };
 // D = 128: the two operands of the state products as swizzled K-major tiles,
 // then the chunk's additive terms already multiplied out: B = Kbar^T U
-// [128 keys][128 values] and O = M U [C tokens][128 values], plain row-major
-// bf16 stored as four 32-column blocks each (a scan CTA owns one block), then
-// gamma_C.
+// [128 keys][128 values] and O = M U [C tokens][128 values], bf16 stored as
+// four 32-column blocks each (a scan CTA owns one block) of 64-byte rows whose
+// four 16-byte chunks are rotated: chunk q of row r sits at position
+// q ^ ((r >> 1) & 3) (rotated_chunk), so that eight threads reading eight
+// consecutive rows hit distinct banks; then gamma_C.
 template <>
 struct Rec<128> {
   static constexpr uint32_t AP = 0;        // Ap    [128 rows][128]
@@ -83,6 +85,10 @@ struct Rec<128> {
 };
 
 __host__ __device__ constexpr uint32_t align1k(uint32_t x) { return (x + 1023u) & ~1023u; }
+// Byte offset of 16-byte chunk q of row r in a block of 64-byte rows (B, O).
+__host__ __device__ constexpr uint32_t rotated_chunk(int r, int q) {
+  return (uint32_t)r * 64u + ((uint32_t)(q ^ ((r >> 1) & 3)) << 4);
+}
 constexpr int kLD = kC + 4;  // row stride (floats) of the float A and T tiles of the solve
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -1028,17 +1034,14 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
 #pragma unroll
           for (int hb = 0; hb < 2; ++hb) {
 #pragma unroll
-            for (int j8 = 0; j8 < 4; ++j8)  // 64-byte rows, chunks rotated for conflict-free writes
-              *reinterpret_cast<uint4 *>(stg + lane * 64 + ((j8 ^ ((lane >> 1) & 3)) << 4)) =
-                  pack8(x + 32 * hb + 8 * j8);
+            for (int j8 = 0; j8 < 4; ++j8)  // record layout: rotated chunks (conflict-free writes)
+              *reinterpret_cast<uint4 *>(stg + rotated_chunk(lane, j8)) = pack8(x + 32 * hb + 8 * j8);
             __syncwarp();
             uint8_t *dst = recg + Rr::BI + (h2 * 2 + hb) * (128 * 64) + quarter * 2048;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int p = i * 512 + lane * 16, R = p >> 6, j = ((p >> 4) & 3) ^ ((R >> 1) & 3);
-              *reinterpret_cast<uint4 *>(dst + R * 64 + j * 16) =
-                  *reinterpret_cast<const uint4 *>(stg + p);
-            }
+            for (int i = 0; i < 4; ++i)
+              *reinterpret_cast<uint4 *>(dst + i * 512 + lane * 16) =
+                  *reinterpret_cast<const uint4 *>(stg + i * 512 + lane * 16);
             __syncwarp();
           }
         }
@@ -1104,17 +1107,15 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
 #pragma unroll
-          for (int j8 = 0; j8 < 4; ++j8)  // 64-byte rows, chunks rotated for conflict-free writes
-            *reinterpret_cast<uint4 *>(stg + side * 1024 + row * 64 +
-                                       ((j8 ^ ((row >> 1) & 3)) << 4)) = pack8(x + 32 * hb + 8 * j8);
+          for (int j8 = 0; j8 < 4; ++j8)  // record layout: rotated chunks (conflict-free writes)
+            *reinterpret_cast<uint4 *>(stg + side * 1024 + rotated_chunk(row, j8)) =
+                pack8(x + 32 * hb + 8 * j8);
           __syncwarp();
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const int p = i * 512 + lane * 16, piece = p >> 10, pp = p & 1023;
-            const int R = pp >> 6, j = ((pp >> 4) & 3) ^ ((R >> 1) & 3);
-            *reinterpret_cast<uint4 *>(recg + Rr::OI + (hb + 2 * piece) * (kC * 64) +
-                                       quarter * 1024 + R * 64 + j * 16) =
-                *reinterpret_cast<const uint4 *>(stg + p);
+            const int p = i * 512 + lane * 16, piece = p >> 10;
+            *reinterpret_cast<uint4 *>(recg + Rr::OI + (hb + 2 * piece) * (kC * 64) + quarter * 1024 +
+                                       (p & 1023)) = *reinterpret_cast<const uint4 *>(stg + p);
           }
           __syncwarp();
         }
@@ -1320,7 +1321,7 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
       }
       ptx::tc_fence_after();
       const uint32_t tO = t_lane + NB * (1 + b);
-      const uint8_t *oi = sm + s * L::STAGE + L::OI_S + (size_t)orow * NB * 2;
+      const uint8_t *oi = sm + s * L::STAGE + L::OI_S;
       const int t = j * kC + orow;
 #pragma unroll
       for (int cb = 0; cb < NB; cb += 16) {
@@ -1328,8 +1329,8 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
         ptx::tmem_ld16(tO + cb, x);
         ptx::tmem_ld_wait();
         if (lane < 16 && t < T) {
-          const uint4 a = *reinterpret_cast<const uint4 *>(oi + cb * 2);
-          const uint4 c2 = *reinterpret_cast<const uint4 *>(oi + cb * 2 + 16);
+          const uint4 a = *reinterpret_cast<const uint4 *>(oi + rotated_chunk(orow, cb / 8));
+          const uint4 c2 = *reinterpret_cast<const uint4 *>(oi + rotated_chunk(orow, cb / 8 + 1));
           const uint32_t w[8] = {a.x, a.y, a.z, a.w, c2.x, c2.y, c2.z, c2.w};
           uint32_t pk[8];
 #pragma unroll
@@ -1379,10 +1380,9 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
       }
       {  // gamma_C S + B while the product runs
         const float gam = reinterpret_cast<const float *>(st + L::GC_S)[r];
-        const uint4 *brow = reinterpret_cast<const uint4 *>(st + L::BI_S + (size_t)r * NB * 2);
 #pragma unroll
         for (int q4 = 0; q4 < NB / 8; ++q4) {
-          const uint4 a = brow[q4];
+          const uint4 a = *reinterpret_cast<const uint4 *>(st + L::BI_S + rotated_chunk(r, q4));
           const uint32_t w[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {

@@ -37,8 +37,12 @@ def untile(buf, rows, K):
 
 
 def bf16_blocks(buf, rows):
-    """[4][rows][32] bf16 blocks -> float64 [rows, 128]."""
-    u16 = np.frombuffer(buf, dtype=np.uint16).reshape(4, rows, 32)
+    """[4][rows][32] bf16 blocks of 64-byte rows whose 16-byte chunk q sits at
+    position q ^ ((row >> 1) & 3) -> float64 [rows, 128]."""
+    u16 = np.frombuffer(buf, dtype=np.uint16).reshape(4, rows, 4, 8)
+    r = np.arange(rows)[:, None]
+    pos = np.arange(4)[None, :] ^ ((r >> 1) & 3)          # [rows, 4]: position of chunk q
+    u16 = u16[:, r, pos, :].reshape(4, rows, 32)
     f = (u16.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     return np.concatenate([f[b] for b in range(4)], axis=1)
 
