@@ -11,39 +11,45 @@
 // (per-channel alpha)", applied before the read.)
 //
 // The step is HBM-bound (about 0.9 flop per byte of state), so the kernel is
-// one streaming pass: each CTA owns one state, loads all of it into
-// registers with 128-bit streaming loads, forms the two column reductions
-// S'^T k and S'^T q, and writes S' + k u^T back with 128-bit streaming stores.
-// One read and one write of the state, nothing else touches HBM in bulk.
+// one streaming pass: each CTA owns a block of up to 64 value columns of one
+// state (the columns never mix: S'^T k, S'^T q and u are per column), loads
+// it into registers with 128-bit streaming loads, forms the two column
+// reductions and writes S' + k u^T back with 128-bit streaming stores.  One
+// read and one write of the state, nothing else touches HBM in bulk; column
+// blocks keep several small CTAs per SM in flight.
 #include "kda_launch.cuh"
 
 namespace kda {
 namespace {
 
 constexpr int kDecodeThreads = 256;
+constexpr int kDecodeCols = 64;  // value columns per CTA (at most)
 
 template <int DK, int DV, typename TI>
-__global__ void __launch_bounds__(kDecodeThreads, 2)
+__global__ void __launch_bounds__(kDecodeThreads, 4)
 decode_step_kernel(const TI *__restrict__ q, const TI *__restrict__ k,
                    const TI *__restrict__ v, const float *__restrict__ beta,
                    const float *__restrict__ log_alpha, int alpha_mode,
                    float *__restrict__ S, TI *__restrict__ o) {
   constexpr int NT = kDecodeThreads;
-  constexpr int C4 = DV / 4;               // float4 column groups per row
+  constexpr int DVB = DV < kDecodeCols ? DV : kDecodeCols;  // this CTA's value columns
+  constexpr int NBLK = DV / DVB;
+  constexpr int C4 = DVB / 4;              // float4 column groups per row
   constexpr int G = NT / C4;               // threads that share a column group
   constexpr int PER = (DK + G - 1) / G;    // float4s held per thread
   static_assert(NT % C4 == 0, "column groups must tile the block");
 
   __shared__ float s_k[DK], s_q[DK], s_a[DK];
   __shared__ float4 red_k[NT], red_q[NT];
-  __shared__ __align__(16) float s_u[DV];
+  __shared__ __align__(16) float s_u[DVB];
   __shared__ float s_kq;
 
-  const int sid = blockIdx.x;  // state index n * H + h
+  const int sid = blockIdx.x / NBLK;  // state index n * H + h
+  const int j0 = (blockIdx.x % NBLK) * DVB;
   const int tid = threadIdx.x;
   const int c4 = tid % C4;
   const int r0 = tid / C4;
-  float *Sp = S + (size_t)sid * DK * DV;
+  float *Sp = S + (size_t)sid * DK * DV + j0;
 
   // Issue every state load first: the whole 64 KiB (at 128 x 128) is in
   // flight before anything waits on it.
@@ -103,9 +109,9 @@ decode_step_kernel(const TI *__restrict__ q, const TI *__restrict__ k,
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int col = tid * 4 + e;
-      const float u = bt * (Io<TI>::ld(v + (size_t)sid * DV + col) - skv[e]);
+      const float u = bt * (Io<TI>::ld(v + (size_t)sid * DV + j0 + col) - skv[e]);
       s_u[col] = u;
-      Io<TI>::st(o + (size_t)sid * DV + col, sqv[e] + kq * u);
+      Io<TI>::st(o + (size_t)sid * DV + j0 + col, sqv[e] + kq * u);
     }
   }
   __syncthreads();
@@ -127,7 +133,9 @@ template <int DK, typename TI>
 kda_status launch_dk(const void *q, const void *k, const void *v, const float *beta,
                      const float *la, float *S, void *o, int NH, int dv, int am,
                      cudaStream_t st) {
-  const dim3 grid(NH), block(kDecodeThreads);
+  const int nblk = dv < kDecodeCols ? 1 : dv / kDecodeCols;
+  if ((long long)NH * nblk > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
+  const dim3 grid(NH * nblk), block(kDecodeThreads);
   const TI *qq = static_cast<const TI *>(q), *kk = static_cast<const TI *>(k),
            *vv = static_cast<const TI *>(v);
   TI *oo = static_cast<TI *>(o);
