@@ -398,10 +398,10 @@ def run_ours(args, rank, world, local, dist):
     hT_host = torch.empty_like(hT, device="cpu").pin_memory()
     d2h = o_host.numel() * o_host.element_size() + hT_host.numel() * hT_host.element_size()
 
-    # kda_chunk_fwd_host: groups of heads, each group's copy-in, prefill and
-    # copy-out overlapped with its neighbours'
+    # kda_chunk_fwd_host: segments of the sequence (every head, a sixteenth
+    # of T each), each segment's copy-in, prefill and copy-out overlapped with its
+    # neighbours', the state carried from segment to segment
     hbuf = kda.host_buffer_for(host["q"], host["v"], w.C, host["log_alpha"], device=dev)
-    groups = (w.B * w.H + 7) // 8
 
     def e2e_step():
         kda.kda_chunk_fwd_host(host["q"], host["k"], host["v"], host["beta"], host["log_alpha"],
@@ -420,8 +420,8 @@ def run_ours(args, rank, world, local, dist):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, dev)
     e2e = {"value": world * tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-           "api": f"kda_chunk_fwd_host from pinned host memory, {groups} heads per group, "
-                  f"copy-in / prefill / copy-out of neighbouring groups overlapped",
+           "api": "kda_chunk_fwd_host from pinned host memory, 16 segments of T (all heads), "
+                  "copy-in / prefill / copy-out of neighbouring segments overlapped",
            "steps": e2e_steps}
     del d, host, o, hT, ws, o_host, hT_host, hbuf
     torch.cuda.empty_cache()

@@ -252,8 +252,10 @@ def host_buffer_for(q, v, C, log_alpha=None, group_heads=0, device=None):
 def kda_chunk_fwd_host(q, k, v, beta, log_alpha, h0, o, hT, C, dev_buffer, group_heads=0,
                        stream=None):
     """Prefill with q, k, v, beta, log_alpha, h0 and the outputs o, hT in host
-    (ideally pinned) memory; ``dev_buffer`` from ``host_buffer_for``.  Returns
-    once enqueued; synchronise ``stream`` before reading o / hT."""
+    (ideally pinned) memory; ``dev_buffer`` from ``host_buffer_for`` (same
+    ``group_heads``).  ``group_heads`` 0 pipelines segments of the sequence,
+    > 0 groups of that many (batch, head) pairs.  Returns once enqueued;
+    synchronise ``stream`` before reading o / hT."""
     B, H, T, dk = q.shape
     dv = v.shape[-1]
     st = load_library().kda_chunk_fwd_host(

@@ -3,13 +3,20 @@
 // The chunked prefill of a long sequence reads several bytes per token from
 // HBM, but a caller whose q, k, v, beta and log_alpha sit in host memory must
 // first move them over the host link, which is far slower than the kernels.
-// This entry point splits the (batch, head) pairs into groups and runs, for
-// consecutive groups, the host -> device copy of group g + 1, the prefill of
-// group g and the device -> host copy of group g - 1 at the same time: copy-in
-// and copy-out on two streams of their own, the prefill on the caller's stream.
-// Inputs and outputs of a group live in one of two staging slots of the
-// caller's device buffer; the per-chunk workspace is shared by all groups
+// This entry point cuts the work into pipeline steps and runs, for
+// consecutive steps, the host -> device copy of step s + 1, the prefill of
+// step s and the device -> host copy of step s - 1 at the same time: copy-in
+// and copy-out on two streams of their own, the prefill on the caller's
+// stream.  A step's inputs and outputs live in one of two staging slots of
+// the caller's device buffer; the per-chunk workspace is shared by all steps
 // (their prefills run one after another on the caller's stream).
+//
+// Steps are either segments of the sequence (the default: every (batch,
+// head) pair, a chunk-aligned sixteenth of T; the state leaves one segment as
+// hT and enters the next as h0, in float32, so the result is the one-call
+// result bit for bit) or groups of (batch, head) pairs over all of T.  With
+// segments the work left after the last copy-in is one segment's prefill and
+// copy-out, not one group's whole-sequence scan.
 #include <stdint.h>
 
 #include <vector>
@@ -58,6 +65,37 @@ Layout layout(const PerHead &p, int G, size_t ws_bytes) {
   return L;
 }
 
+// Segment mode: a chunk-aligned sixteenth of the sequence per step.
+constexpr int kSegments = 16;
+int seg_len(int T, int C) {
+  const int t = (T + kSegments - 1) / kSegments;
+  const int c = C > 0 ? C : 1;
+  const int l = (t + c - 1) / c * c;
+  return l > 0 ? l : c;
+}
+// Device buffer of the segment mode: workspace, the carried state, two slots.
+struct SegLayout {
+  size_t ws, state, q, k, v, beta, la, o, slot, total;
+};
+SegLayout seg_layout(const PerHead &p1, int BH, int Tl, int T, size_t ws_bytes) {
+  // p1: per-head bytes for the whole sequence; a slot holds Tl tokens of every head
+  SegLayout L;
+  L.ws = up(ws_bytes);
+  L.state = up((size_t)BH * p1.state);
+  const size_t tq = T > 0 ? p1.q / T : 0, tv = T > 0 ? p1.v / T : 0;
+  const size_t tb = T > 0 ? p1.beta / T : 0, tl = T > 0 ? p1.la / T : 0;
+  size_t off = 0;
+  L.q = off;    off += up((size_t)BH * Tl * tq);
+  L.k = off;    off += up((size_t)BH * Tl * tq);
+  L.v = off;    off += up((size_t)BH * Tl * tv);
+  L.beta = off; off += up((size_t)BH * Tl * tb);
+  L.la = off;   off += up((size_t)BH * Tl * tl);
+  L.o = off;    off += up((size_t)BH * Tl * tv);
+  L.slot = off;
+  L.total = L.ws + L.state + 2 * L.slot;
+  return L;
+}
+
 int group_of(int BH, int group_heads) {
   if (group_heads > 0) return group_heads < BH ? group_heads : BH;
   const int g = (BH + 7) / 8;  // eight groups by default
@@ -89,11 +127,99 @@ extern "C" size_t kda_chunk_fwd_host_buffer_size(int B, int H, int T, int dk, in
                                                  int group_heads) {
   if (B < 0 || H < 0 || group_heads < 0) return 0;
   const int BH = B * H;
+  if (group_heads == 0 && T > 0) {  // segments of the sequence
+    const int Tl = seg_len(T, C);
+    const size_t ws = kda_chunk_fwd_workspace_size(1, BH, Tl, dk, dv, C, dt, am);
+    if (ws == 0) return 0;
+    return seg_layout(per_head(T, dk, dv, dt, am), BH, Tl, T, ws).total;
+  }
   const int G = group_of(BH, group_heads);
   const size_t ws = kda_chunk_fwd_workspace_size(1, G, T, dk, dv, C, dt, am);
   if (ws == 0) return 0;
   return layout(per_head(T, dk, dv, dt, am), G, ws).total;
 }
+
+namespace {
+
+// Segment mode of kda_chunk_fwd_host (arguments already checked; T > 0).
+kda_status host_segments(const void *q, const void *k, const void *v, const float *beta,
+                         const float *log_alpha, const float *h0, void *o, float *hT, int BH,
+                         int T, int dk, int dv, int C, kda_dtype dt, kda_alpha_mode am,
+                         uint8_t *base, cudaStream_t s) {
+  const int Tl = seg_len(T, C);
+  const int NS = (T + Tl - 1) / Tl;
+  const PerHead p = per_head(T, dk, dv, dt, am);
+  const size_t tq = p.q / T, tv = p.v / T, tb = p.beta / T, tla = p.la / T;  // bytes per token
+  const size_t ws_bytes = kda_chunk_fwd_workspace_size(1, BH, Tl, dk, dv, C, dt, am);
+  const SegLayout L = seg_layout(p, BH, Tl, T, ws_bytes);
+  uint8_t *ws = base;
+  float *state = reinterpret_cast<float *>(base + L.ws);
+
+  Resources R;
+  if (cudaStreamCreateWithFlags(&R.in, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&R.out, cudaStreamNonBlocking) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  cudaEvent_t start = R.make();
+  if (!start || cudaEventRecord(start, s) != cudaSuccess ||
+      cudaStreamWaitEvent(R.in, start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(R.out, start, 0) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  // the initial state goes in ahead of the first segment (same stream)
+  if (h0 && cudaMemcpyAsync(state, h0, (size_t)BH * p.state, cudaMemcpyHostToDevice, R.in) !=
+                cudaSuccess)
+    return KDA_ERR_CUDA;
+
+  std::vector<cudaEvent_t> out_done(NS, nullptr);
+  for (int sg = 0; sg < NS; ++sg) {
+    const int t0 = sg * Tl;
+    const int Ts = T - t0 < Tl ? T - t0 : Tl;
+    uint8_t *slot = base + L.ws + L.state + (size_t)(sg & 1) * L.slot;
+    cudaEvent_t in_done = R.make(), comp_done = R.make();
+    out_done[sg] = R.make();
+    if (!in_done || !comp_done || !out_done[sg]) return KDA_ERR_CUDA;
+
+    // copy-in: tokens t0 .. t0 + Ts of every (batch, head) pair, one 2-D copy
+    // per tensor (host rows T tokens apart, device rows Ts tokens apart),
+    // after the copy-out of the segment that last used this slot
+    if (sg >= 2 && cudaStreamWaitEvent(R.in, out_done[sg - 2], 0) != cudaSuccess)
+      return KDA_ERR_CUDA;
+    auto h2d = [&](size_t off, const void *src, size_t per_token) {
+      return cudaMemcpy2DAsync(slot + off, Ts * per_token,
+                               static_cast<const uint8_t *>(src) + (size_t)t0 * per_token,
+                               (size_t)T * per_token, Ts * per_token, BH,
+                               cudaMemcpyHostToDevice, R.in) == cudaSuccess;
+    };
+    bool ok = h2d(L.q, q, tq) && h2d(L.k, k, tq) && h2d(L.v, v, tv) && h2d(L.beta, beta, tb);
+    if (ok && am != KDA_ALPHA_NONE) ok = h2d(L.la, log_alpha, tla);
+    if (!ok || cudaEventRecord(in_done, R.in) != cudaSuccess) return KDA_ERR_CUDA;
+
+    // prefill of the segment: the state enters as h0 and leaves as hT
+    if (cudaStreamWaitEvent(s, in_done, 0) != cudaSuccess) return KDA_ERR_CUDA;
+    const bool last = sg == NS - 1;
+    const kda_status st = kda_chunk_fwd(
+        slot + L.q, slot + L.k, slot + L.v, reinterpret_cast<const float *>(slot + L.beta),
+        am != KDA_ALPHA_NONE ? reinterpret_cast<const float *>(slot + L.la) : nullptr,
+        (sg > 0 || h0) ? state : nullptr, slot + L.o, (!last || hT) ? state : nullptr, 1, BH, Ts,
+        dk, dv, C, dt, am, ws, ws_bytes, reinterpret_cast<kda_stream_t>(s));
+    if (st != KDA_OK) return st;
+    if (cudaEventRecord(comp_done, s) != cudaSuccess) return KDA_ERR_CUDA;
+
+    // copy-out of the segment's o (and of the final state)
+    if (cudaStreamWaitEvent(R.out, comp_done, 0) != cudaSuccess) return KDA_ERR_CUDA;
+    if (cudaMemcpy2DAsync(static_cast<uint8_t *>(o) + (size_t)t0 * tv, (size_t)T * tv, slot + L.o,
+                          Ts * tv, Ts * tv, BH, cudaMemcpyDeviceToHost, R.out) != cudaSuccess)
+      return KDA_ERR_CUDA;
+    if (last && hT &&
+        cudaMemcpyAsync(hT, state, (size_t)BH * p.state, cudaMemcpyDeviceToHost, R.out) !=
+            cudaSuccess)
+      return KDA_ERR_CUDA;
+    if (cudaEventRecord(out_done[sg], R.out) != cudaSuccess) return KDA_ERR_CUDA;
+  }
+  if (cudaStreamWaitEvent(s, out_done[NS - 1], 0) != cudaSuccess) return KDA_ERR_CUDA;
+  return KDA_OK;
+}
+
+}  // namespace
 
 extern "C" kda_status kda_chunk_fwd_host(const void *q, const void *k, const void *v,
                                          const float *beta, const float *log_alpha,
@@ -112,6 +238,10 @@ extern "C" kda_status kda_chunk_fwd_host(const void *q, const void *k, const voi
     return KDA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(dev_buffer) & (kAlign - 1)) != 0 || dev_bytes < need)
     return KDA_ERR_INVALID_ARG;
+
+  if (group_heads == 0 && T > 0)
+    return host_segments(q, k, v, beta, log_alpha, h0, o, hT, BH, T, dk, dv, C, dt, am,
+                         static_cast<uint8_t *>(dev_buffer), reinterpret_cast<cudaStream_t>(stream));
 
   const int G = group_of(BH, group_heads);
   const int NG = (BH + G - 1) / G;

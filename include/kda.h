@@ -259,20 +259,26 @@ kda_status kda_attn_res(const void *V, int n_blocks, const float *w, void *h,
  *
  *   q, k, v, beta, log_alpha, h0   host, same shapes and types as kda_chunk_fwd
  *   o, hT                          host outputs (hT may be NULL; h0 may be NULL)
- *   group_heads                    (batch, head) pairs per pipeline step;
- *                                  0 = about an eighth of B*H
+ *   group_heads                    0: pipeline steps are segments of the
+ *                                  sequence (a chunk-aligned sixteenth of T for
+ *                                  every (batch, head) pair; the state is
+ *                                  carried from one segment to the next in
+ *                                  float32); > 0: steps are groups of that
+ *                                  many (batch, head) pairs over all of T
  *   dev_buffer, dev_bytes          device memory, 256-byte aligned, at least
  *                                  kda_chunk_fwd_host_buffer_size(...) bytes,
  *                                  owned by the caller; it holds the shared
  *                                  workspace (its start: read device errors
  *                                  with kda_chunk_fwd_status(dev_buffer, ...))
- *                                  and two staging slots of group_heads pairs
+ *                                  (segments: also the carried state) and two
+ *                                  staging slots of one pipeline step
  *
- * The (batch, head) pairs are cut into groups; while group g runs on `stream`,
- * group g + 1 is copied in and group g - 1 copied out on two streams that the
- * call creates and releases (nothing is kept between calls).  Host memory
- * should be page-locked (cudaHostAlloc / cudaHostRegister): from pageable
- * memory the copies are correct but do not overlap.  The call returns once
+ * While step s runs on `stream`, step s + 1 is copied in and step s - 1
+ * copied out on two streams that the call creates and releases (nothing is
+ * kept between calls).  Segments leave less work after the last copy-in (one
+ * segment's prefill and copy-out instead of one group's whole-sequence scan).
+ * Host memory should be page-locked (cudaHostAlloc / cudaHostRegister): from
+ * pageable memory the copies are correct but do not overlap.  The call returns once
  * everything is enqueued; all of it, copies included, completes on `stream`
  * (synchronise `stream` before reading o or hT).  Results equal those of
  * kda_chunk_fwd on device copies of the inputs, bit for bit.  Errors: as

@@ -1,8 +1,11 @@
-"""kda_chunk_fwd_host: the prefill from and to host memory, head groups
-pipelined over two copy streams.  Its results must equal kda_chunk_fwd on
-device copies of the same inputs bit for bit (the same kernels run on each
-head), for every way of cutting the heads into groups; one case is also held
-against the float64 oracle."""
+"""kda_chunk_fwd_host: the prefill from and to host memory, pipelined over
+two copy streams either by segments of the sequence (group_heads = 0: the
+state carried from segment to segment in float32) or by groups of heads.
+Its results must equal kda_chunk_fwd on device copies of the same inputs bit
+for bit (the same kernels run on the same chunks), for segments (ragged last
+segment, one segment only, with and without initial and final state) and for
+every way of cutting the heads into groups; one case is also held against
+the float64 oracle."""
 import numpy as np
 import pytest
 import torch
@@ -53,10 +56,13 @@ CASES = [
                la_mu=-4.0, h0_sd=0.05, seed=11), [1, 2, 4, 0]),
     # CUDA-core path, scalar decay, no initial state; 5 heads
     (W.Prefill("host_ffma", B=1, H=5, T=130, dk=64, dv=32, C=32, dtype="f32", alpha="scalar",
-               la_mu=-3.0, h0_sd=0.0, seed=12), [2, 5]),
+               la_mu=-3.0, h0_sd=0.0, seed=12), [0, 2, 5]),
     # D = 64 tensor path, no decay
     (W.Prefill("host_d64", B=1, H=4, T=256, dk=64, dv=64, C=64, dtype="bf16", alpha="none",
-               la_mu=0.0, h0_sd=0.02, seed=13), [3]),
+               la_mu=0.0, h0_sd=0.02, seed=13), [0, 3]),
+    # a sequence shorter than one segment's chunk (one segment)
+    (W.Prefill("host_short", B=1, H=2, T=40, dk=128, dv=128, C=64, dtype="bf16", alpha="channel",
+               la_mu=-4.0, h0_sd=0.05, seed=14), [0, 1]),
 ]
 
 
@@ -69,27 +75,30 @@ def test_host_api_equals_device_api(w, groups):
         o, hT = _run_host(w, hx, g)
         assert torch.equal(o, o_ref), f"group_heads={g}: o differs"
         assert torch.equal(hT, hT_ref), f"group_heads={g}: hT differs"
-    o, hT = _run_host(w, hx, groups[0], with_hT=False)
-    assert hT is None and torch.equal(o, o_ref)
+    for g in sorted({groups[0], 0}):
+        o, hT = _run_host(w, hx, g, with_hT=False)
+        assert hT is None and torch.equal(o, o_ref), f"group_heads={g}, no hT"
 
 
-def test_host_api_against_oracle():
+@pytest.mark.parametrize("group_heads", [0, 4])
+def test_host_api_against_oracle(group_heads):
     w = CASES[0][0]
     x = W.prefill_inputs(w)
-    o, hT = _run_host(w, _host_inputs(w, x), 4)
+    o, hT = _run_host(w, _host_inputs(w, x), group_heads)
     ro, rh = oracle.recurrent_heads(x["q"], x["k"], x["v"], x["beta"], x["log_alpha"], x["h0"])
     assert rel_err(o.float().numpy().reshape(ro.shape), ro) <= tol_for(w.dtype)
     assert rel_err(hT.numpy().reshape(rh.shape), rh) <= tol_for(w.dtype)
 
 
-def test_host_api_rejects_small_buffer():
+@pytest.mark.parametrize("group_heads", [0, 2])
+def test_host_api_rejects_small_buffer(group_heads):
     w = CASES[0][0]
     hx = _host_inputs(w, W.prefill_inputs(w))
     need = kda.kda_chunk_fwd_host_buffer_size(w.B, w.H, w.T, w.dk, w.dv, w.C, kda.KDA_BF16,
-                                              kda.KDA_ALPHA_CHANNEL, 2)
+                                              kda.KDA_ALPHA_CHANNEL, group_heads)
     small = torch.empty(need - 256, dtype=torch.uint8, device=DEV)
     o = torch.empty((w.B, w.H, w.T, w.dv), dtype=torch.bfloat16)
     with pytest.raises(kda.KdaError) as e:
         kda.kda_chunk_fwd_host(hx["q"], hx["k"], hx["v"], hx["beta"], hx["log_alpha"], hx["h0"],
-                               o, None, w.C, small, 2)
+                               o, None, w.C, small, group_heads)
     assert e.value.status == kda.KDA_ERR_INVALID_ARG
