@@ -27,6 +27,7 @@ import os
 import platform
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -116,8 +117,11 @@ class ClockSampler:
 
     def __enter__(self):
         try:
-            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+            # raw samples: KDA_CLOCKS_DIR if set, else the system temp directory
+            # (the JSON line carries their summary)
+            out_dir = os.environ.get("KDA_CLOCKS_DIR") or tempfile.gettempdir()
+            os.makedirs(out_dir, exist_ok=True)
+            self.path = os.path.join(out_dir, f"kda_clocks_{os.getpid()}.csv")
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
