@@ -1,6 +1,7 @@
 """kda_attn_res (AttnRes depth mixing) on the GPU against the float64 oracle:
-float32 and bf16 stacks, block counts from 1 to the maximum, widths that are
-not a multiple of the CTA's 256 x 16-byte sweep, and the argument checks."""
+float32 and bf16 stacks, block counts from 1 to the maximum, widths from 8 to
+8192 (some not a multiple of the CTA's 256 x 16-byte sweep), more rows than
+the grid holds at once, and the argument checks."""
 import numpy as np
 import pytest
 import torch
@@ -24,7 +25,8 @@ def _case(nb, rows, D, dtype, seed, scale=1.0):
 
 @pytest.mark.parametrize("nb,rows,D,dtype", [
     (1, 5, 64, "f32"), (9, 33, 1024, "f32"), (9, 40, 7168, "bf16"), (32, 7, 520, "bf16"),
-    (13, 300, 2056, "bf16"), (8, 1, 8, "f32")])
+    (13, 300, 2056, "bf16"), (8, 1, 8, "f32"), (1, 3, 1024, "bf16"), (10, 17, 4096, "bf16"),
+    (9, 400, 2048, "bf16"), (3, 2, 8192, "bf16"), (11, 6, 7168, "bf16"), (4, 5, 1536, "bf16")])
 def test_attn_res_matches_oracle(nb, rows, D, dtype):
     V, w = _case(nb, rows, D, dtype, seed=nb * 7 + D)
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
