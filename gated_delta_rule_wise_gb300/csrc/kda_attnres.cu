@@ -165,8 +165,15 @@ attn_res_kernel(const T *__restrict__ V, int nb, const float *__restrict__ w, T 
 
 // The same with the block count fixed at compile time (1..16): every piece's
 // loads for all blocks are issued together and the sums live in registers.
+// Four CTAs per SM where a thread's pieces fit in 64 registers (bf16 up to
+// 11 blocks, float32 up to 7), three otherwise: more rows in flight per SM
+// hide more of each row's reduction than deeper unrolling within a row does.
 template <typename T, int NB>
-__global__ void __launch_bounds__(kAttnThreads)
+constexpr int attn_min_blocks() {
+  return (sizeof(T) == 2 ? NB <= 11 : NB <= 7) ? 4 : 3;
+}
+template <typename T, int NB>
+__global__ void __launch_bounds__(kAttnThreads, attn_min_blocks<T, NB>())
 attn_res_fixed_kernel(const T *__restrict__ V, const float *__restrict__ w, T *__restrict__ h,
                       long long rows, int D, float eps) {
   using P = Piece<T>;
@@ -182,7 +189,7 @@ attn_res_fixed_kernel(const T *__restrict__ V, const float *__restrict__ w, T *_
     float dot[NB], ss[NB];
 #pragma unroll
     for (int n = 0; n < NB; ++n) dot[n] = ss[n] = 0.f;
-#pragma unroll 2
+#pragma unroll 1
     for (int pc = tid; pc < npieces; pc += kAttnThreads) {
       float x[NB][E];
 #pragma unroll
@@ -241,7 +248,7 @@ attn_res_fixed_kernel(const T *__restrict__ V, const float *__restrict__ w, T *_
 #pragma unroll
     for (int n = 0; n < NB; ++n) al[n] = alpha[n];
     T *hr = h + (size_t)row * D;
-#pragma unroll 2
+#pragma unroll 1
     for (int pc = tid; pc < npieces; pc += kAttnThreads) {
       float x[NB][E];
 #pragma unroll
