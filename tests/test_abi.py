@@ -77,6 +77,29 @@ def test_workspace_size(lib):
     assert ws(1, 1, 64, 16, 16, 16, kda.KDA_F32, kda.KDA_ALPHA_NONE, 5) == 0   # bad path
 
 
+def test_host_buffer_size(lib):
+    """kda_chunk_fwd_host_buffer_size: segments of the sequence (group_heads = 0)
+    or head groups; both hold the workspace of one step and two staging slots
+    of its inputs and outputs, so each is at least that step's workspace plus
+    twice its input bytes; invalid arguments give 0."""
+    import gated_delta_rule_wise_gb300 as kda
+    hb, ws = kda.kda_chunk_fwd_host_buffer_size, kda.kda_chunk_fwd_workspace_size
+    B, H, T, d, C = 1, 32, 131072, 128, 64
+    bf, ch = kda.KDA_BF16, kda.KDA_ALPHA_CHANNEL
+    per_tok_in = 2 * (2 * d + d) + 4 + 4 * d            # q, k, v bf16, beta, channel log_alpha
+    seg_T = -(-T // 16)
+    seg_T = -(-seg_T // C) * C                           # a chunk-aligned sixteenth of T
+    seg = hb(B, H, T, d, d, C, bf, ch, 0)
+    assert seg >= ws(1, B * H, seg_T, d, d, C, bf, ch) + 2 * B * H * seg_T * per_tok_in
+    grp = hb(B, H, T, d, d, C, bf, ch, 4)
+    assert grp >= ws(1, 4, T, d, d, C, bf, ch) + 2 * 4 * T * per_tok_in
+    # a sequence shorter than one chunk still gets one segment of a chunk
+    assert hb(1, 2, 40, d, d, C, bf, ch, 0) >= ws(1, 2, C, d, d, C, bf, ch)
+    assert hb(-1, H, T, d, d, C, bf, ch, 0) == 0
+    assert hb(B, H, T, d, d, C, bf, ch, -1) == 0
+    assert hb(B, H, T, 24, 24, C, bf, ch, 0) == 0       # unsupported head size
+
+
 FAKE = 0x7f0000000000  # 256-byte aligned, never dereferenced by these cases
 
 
