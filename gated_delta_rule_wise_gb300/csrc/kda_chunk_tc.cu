@@ -606,8 +606,9 @@ __device__ __forceinline__ void prep_d64(const __nv_bfloat16 *__restrict__ q,
 // (10) Qp = Q*gamma - M W and O = M U to the record.
 // Each warp assembles its contiguous pieces of the record tiles in staging
 // slots of consumed shared memory and stores them with coalesced writes.
-// The next chunk's log_alpha, k and v rows are bulk-copied as soon as the last
-// product has read A's space and blocks 2-3 (after (9)), its q rows after (10).
+// The next chunk's input rows are prefetched into L2 during (5); its log_alpha,
+// k and v rows are bulk-copied as soon as the last product has read A's space
+// and blocks 2-3 (after (9)), its q rows after (10).
 struct PrepSmem128 {
   using R = Rec<128>;
   static constexpr int D = 128;
@@ -713,6 +714,16 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
     const uint32_t bytes = (uint32_t)valid * D * 2;
     ptx::mbar_arrive_expect_tx(qbar, bytes);
     ptx::bulk_g2s(sm + L::RAWQ, q + row0 * D, bytes, qbar);
+  };
+  auto prefetch_rows = [&](int idx) {  // a chunk's input rows into L2 ahead of its copies
+    int valid;
+    size_t row0;
+    rows_of(idx, valid, row0);
+    const uint32_t bytes = (uint32_t)valid * D * 2;
+    if (la_bulk) ptx::prefetch_l2(log_alpha + row0 * D, 2 * bytes);
+    ptx::prefetch_l2(k + row0 * D, bytes);
+    ptx::prefetch_l2(v + row0 * D, bytes);
+    ptx::prefetch_l2(q + row0 * D, bytes);
   };
 
   if (tid == 0) {
@@ -953,6 +964,7 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
                          umma::idesc_bf16_bmn(64, 256), ks > 0);
       ptx::mma_commit(bar);
     }
+    if (tid == 32 && has_next) prefetch_rows(idx_next);
     wait_mma(0x102u);
 
     // ---- (6) [W | U] rows -> natural tile over K_beta and beta V (both consumed).

@@ -96,6 +96,11 @@ __device__ __forceinline__ void bulk_s2g(void *dst_gmem, const void *src_smem, u
                "r"(smem_u32(src_smem)), "r"(bytes)
                : "memory");
 }
+// Bulk prefetch of global memory into L2 (no destination, no completion):
+// address 16-byte aligned, size a multiple of 16 bytes.
+__device__ __forceinline__ void prefetch_l2(const void *src_gmem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src_gmem), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
