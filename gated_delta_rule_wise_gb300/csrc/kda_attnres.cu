@@ -10,7 +10,8 @@
 // 16; above that, eight blocks at a time under a predicate) and accumulates
 // w . V_n and V_n . V_n; a block reduction and one warp's softmax give the
 // weights.  Pass 2 reads the same pieces again (from L2: the row was just
-// read) and writes the weighted sum.
+// read) and writes the weighted sum; both as streaming accesses, so that they
+// do not evict rows that other CTAs have read once and will read again.
 #include <utility>
 
 #include "kda_launch.cuh"
@@ -24,24 +25,35 @@ constexpr int kMaxBlocks = 32;
 constexpr int kGroup = 8;  // blocks whose loads are in flight together (general kernel)
 constexpr int kFixedMax = 16;  // block counts with a kernel of their own
 
+// A row is read twice.  The first read caches it in L2 only (`first`); the
+// second is its last use and reads it as streaming (`last`: evict-first), and
+// the output row is stored as streaming too, so neither pushes rows that are
+// still between their two reads out of L2.
+enum class Use { first, last };
+__device__ __forceinline__ uint4 ld16(const void *p, Use u) {
+  const uint4 *q = reinterpret_cast<const uint4 *>(p);
+  return u == Use::first ? __ldcg(q) : __ldcs(q);
+}
+
 template <typename T>
 struct Piece;  // 16 bytes of a row
 template <>
 struct Piece<float> {
   static constexpr int E = 4;
-  __device__ static void load(const float *p, float *x) {
-    const float4 u = __ldcg(reinterpret_cast<const float4 *>(p));
-    x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
+  __device__ static void load(const float *p, float *x, Use use) {
+    const uint4 u = ld16(p, use);
+    x[0] = __uint_as_float(u.x); x[1] = __uint_as_float(u.y);
+    x[2] = __uint_as_float(u.z); x[3] = __uint_as_float(u.w);
   }
   __device__ static void store(float *p, const float *x) {
-    *reinterpret_cast<float4 *>(p) = make_float4(x[0], x[1], x[2], x[3]);
+    __stcs(reinterpret_cast<float4 *>(p), make_float4(x[0], x[1], x[2], x[3]));
   }
 };
 template <>
 struct Piece<__nv_bfloat16> {
   static constexpr int E = 8;
-  __device__ static void load(const __nv_bfloat16 *p, float *x) {
-    const uint4 u = __ldcg(reinterpret_cast<const uint4 *>(p));
+  __device__ static void load(const __nv_bfloat16 *p, float *x, Use use) {
+    const uint4 u = ld16(p, use);
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -57,7 +69,7 @@ struct Piece<__nv_bfloat16> {
       const __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
       w[i] = *reinterpret_cast<const uint32_t *>(&h);
     }
-    *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+    __stcs(reinterpret_cast<uint4 *>(p), make_uint4(w[0], w[1], w[2], w[3]));
   }
 };
 
@@ -94,7 +106,7 @@ attn_res_kernel(const T *__restrict__ V, int nb, const float *__restrict__ w, T 
         for (int j = 0; j < kGroup; ++j) {
           if (g + j < nb) {
             float x[E];
-            P::load(vr + (size_t)(g + j) * stride + (size_t)pc * E, x);
+            P::load(vr + (size_t)(g + j) * stride + (size_t)pc * E, x, Use::first);
 #pragma unroll
             for (int e = 0; e < E; ++e) {
               dot[j] += wv[e] * x[e];
@@ -150,7 +162,7 @@ attn_res_kernel(const T *__restrict__ V, int nb, const float *__restrict__ w, T 
         for (int j = 0; j < kGroup; ++j) {
           if (g + j < nb) {
             float x[E];
-            P::load(vr + (size_t)(g + j) * stride + (size_t)pc * E, x);
+            P::load(vr + (size_t)(g + j) * stride + (size_t)pc * E, x, Use::last);
             const float an = alpha[g + j];
 #pragma unroll
             for (int e = 0; e < E; ++e) acc[e] += an * x[e];
@@ -193,7 +205,7 @@ attn_res_fixed_kernel(const T *__restrict__ V, const float *__restrict__ w, T *_
     for (int pc = tid; pc < npieces; pc += kAttnThreads) {
       float x[NB][E];
 #pragma unroll
-      for (int n = 0; n < NB; ++n) P::load(vr + (size_t)n * stride + (size_t)pc * E, x[n]);
+      for (int n = 0; n < NB; ++n) P::load(vr + (size_t)n * stride + (size_t)pc * E, x[n], Use::first);
       float wv[E];
       const float4 *wp = reinterpret_cast<const float4 *>(w + (size_t)pc * E);
 #pragma unroll
@@ -252,7 +264,7 @@ attn_res_fixed_kernel(const T *__restrict__ V, const float *__restrict__ w, T *_
     for (int pc = tid; pc < npieces; pc += kAttnThreads) {
       float x[NB][E];
 #pragma unroll
-      for (int n = 0; n < NB; ++n) P::load(vr + (size_t)n * stride + (size_t)pc * E, x[n]);
+      for (int n = 0; n < NB; ++n) P::load(vr + (size_t)n * stride + (size_t)pc * E, x[n], Use::last);
       float acc[E];
 #pragma unroll
       for (int e = 0; e < E; ++e) acc[e] = 0.f;
