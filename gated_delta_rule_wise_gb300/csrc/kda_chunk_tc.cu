@@ -1287,24 +1287,16 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
       const uint64_t dAP = umma::sdesc(ptx::smem_u32(st + R::AP));
       const uint64_t dQP = umma::sdesc(ptx::smem_u32(st + R::QP));
       const uint64_t dSB = umma::sdesc_mn(ptx::smem_u32(sb_of(i)), 128, 0);
-      ptx::named_barrier(1, kSyncThreads);  // bf16 S_i written, P_{i-1} read by every state thread
+      // bf16 S_i written and P_{i-1} read by every state thread, which have
+      // also seen record i land and accumulator b freed by the output warps
+      ptx::named_barrier(1, kSyncThreads);
       if (lane == 0) {
         ptx::tc_fence_after();
-        if (ok && !ptx::mbar_wait_fast(&full[s], (i / kStages) & 1, kWaitLimit)) {
-          ok = false;
-          report_error(hdr, KDA_ERR_TIMEOUT, 0x202u);
-        }
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)  // P = Ap S   (S read MN-major)
           ptx::mma_bf16_ss(tmem, dAP + (uint64_t)(((ks >> 2) * D * 128 + (ks & 3) * 32) >> 4),
                            dSB + (uint64_t)(ks * 2048 >> 4), umma::idesc_bf16_bmn(128, NB), ks > 0);
         ptx::mma_commit(mS);
-        if (i > 0) ptx::mbar_arrive(&empty[(i - 1) % kStages]);  // state side done with chunk i-1
-        if (i >= kOutBufs && ok &&
-            !ptx::mbar_wait_fast(&ofree[b], ((i / kOutBufs) - 1) & 1, kWaitLimit)) {
-          ok = false;  // the output warps have read accumulator b (chunk i - kOutBufs)
-          report_error(hdr, KDA_ERR_TIMEOUT, 0x222u);
-        }
         const uint32_t tOc = tmem + NB * (1 + b);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)  // o = Qp S
@@ -1385,11 +1377,25 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
       for (int c8 = 0; c8 < NB / 8; ++c8) st_chunk(sb, r, c8, 128, sr + 8 * c8);
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
-      ptx::named_arrive(1, kSyncThreads);
+      // the checks the issuer's products need, made here where they are off
+      // its serial path: record i landed (every state thread reads its B and
+      // gamma_C below anyway), accumulator (i mod 3) read by the output warps
+      // (chunk i - 3); and stage i-1 released for the state side (its products
+      // completed before P_{i-1} was read, its B was read before that)
       if (ok && !ptx::mbar_wait_fast(&full[s], (i / kStages) & 1, kWaitLimit)) {
         ok = false;
         report_error(hdr, KDA_ERR_TIMEOUT, 0x204u);
       }
+      if (r == 0) {
+        if (i >= kOutBufs && ok &&
+            !ptx::mbar_wait_fast(&ofree[i % kOutBufs], ((i / kOutBufs) - 1) & 1, kWaitLimit)) {
+          ok = false;
+          report_error(hdr, KDA_ERR_TIMEOUT, 0x222u);
+        }
+        if (i > 0) ptx::mbar_arrive(&empty[(i - 1) % kStages]);
+      }
+      __syncwarp();
+      ptx::named_arrive(1, kSyncThreads);
       {  // gamma_C S + B while the product runs
         const float gam = reinterpret_cast<const float *>(st + L::GC_S)[r];
 #pragma unroll
