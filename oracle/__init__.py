@@ -21,6 +21,9 @@ Contents
                        agree for every chunk size.
 ``forward_substitution`` the row recursion that inverts a unit lower-triangular
                        matrix, as stated for the chunked DeltaNet form.
+``linear``, ``linear_norm`` linear attention without and with the normaliser
+                       (plain C, float64); ``input_maps`` the maps applied to
+                       the projections (silu + normalise, sigmoid, ELU + 1).
 
 Pins (``tests/test_oracle_pins.py``) tie every function to facts the pages and
 the mathematics fix: a hand-worked 2x2 example, closed forms for pure decay,
@@ -43,7 +46,7 @@ _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "libkda_oracle.so")
 
 ALPHA_NONE, ALPHA_SCALAR, ALPHA_CHANNEL = 0, 1, 2
-_VERSION = 2
+_VERSION = 3
 
 _lib = None
 _lock = threading.Lock()
@@ -83,6 +86,10 @@ def open_library(path):
     f.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int, ctypes.c_void_p,
                                          ctypes.c_long, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_void_p, ctypes.c_void_p]
+    f = lib.kda_oracle_linear_norm
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int, ctypes.c_long, ctypes.c_int,
+                                         ctypes.c_int] + [ctypes.c_void_p] * 3
     return lib
 
 
@@ -167,6 +174,42 @@ def linear(q, k, v, log_alpha=None, h0=None, lib=None):
     return o, hT
 
 
+def linear_norm(q, k, v, log_alpha=None, lib=None):
+    """Token-by-token normalised linear attention for one head from a zero
+    state, in float64: S = Diag(a_t) S + k_t v_t^T, z = a_t z + k_t,
+    o_t = S^T q_t / (q_t . z) (see kda_oracle_linear_norm).  q and k are the
+    feature-mapped values (``input_maps(..., qk_map="elu1")``).
+
+    Returns (o [T, dv], hT [dk, dv], zT [dk]) as float64.
+    """
+    lib = lib or _load()
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    T, dk = q.shape
+    dv = v.shape[1]
+    if k.shape != (T, dk) or v.shape != (T, dv):
+        raise ValueError("shape mismatch")
+    mode = alpha_mode_of(log_alpha, T, dk)
+    la = _f32(log_alpha)
+    o = np.empty((T, dv), dtype=np.float64)
+    hT = np.empty((dk, dv), dtype=np.float64)
+    zT = np.empty(dk, dtype=np.float64)
+    rc = lib.kda_oracle_linear_norm(_ptr(q), _ptr(k), _ptr(v), _ptr(la), mode, T, dk, dv,
+                                    _ptr(o), _ptr(hT), _ptr(zT))
+    if rc != 0:
+        raise RuntimeError(f"kda_oracle_linear_norm failed with {rc}")
+    return o, hT, zT
+
+
+def linear_norm_heads(q, k, v, log_alpha=None):
+    """``linear_norm`` for every (b, h) of ``[B, H, T, d]`` inputs; o as [B*H, T, dv]."""
+    B, H, T, dk = q.shape
+    mode = ALPHA_NONE if log_alpha is None else (ALPHA_SCALAR if np.ndim(log_alpha) == 3
+                                                 else ALPHA_CHANNEL)
+    return np.stack([linear_norm(q[b, h], k[b, h], v[b, h],
+                                 _alpha_slice(log_alpha, mode, b, h))[0]
+                     for b in range(B) for h in range(H)])
+
+
 def linear_heads(q, k, v, log_alpha=None, h0=None):
     """``linear`` for every (b, h) of ``[B, H, T, d]`` inputs; (o [B*H, T, dv], hT [B*H, dk, dv])."""
     B, H, T, dk = q.shape
@@ -182,7 +225,7 @@ def linear_heads(q, k, v, log_alpha=None, h0=None):
     return np.stack(os_), np.stack(hs)
 
 
-def input_maps(q=None, k=None, beta_logit=None):
+def input_maps(q=None, k=None, beta_logit=None, qk_map="silu_norm"):
     """The maps the pages apply to the projections before the delta rule
     ("22,580: From GPT-2 to Kimi K3" (yichencityu.github.io), section 5.2,
     the DeltaNet forward: q = normalize(silu(q)), k = normalize(silu(k)) along
@@ -190,17 +233,26 @@ def input_maps(q=None, k=None, beta_logit=None):
     values.
 
     silu(x) = x / (1 + exp(-x)); normalize(x) = x / max(||x||_2, 1e-12) over
-    the last axis; sigmoid(x) = 1 / (1 + exp(-x)).  Returns the mapped arrays
+    the last axis; sigmoid(x) = 1 / (1 + exp(-x)).  With ``qk_map="elu1"`` q
+    and k take instead the feature map of the same page's linear attention,
+    elu(x) + 1 = x + 1 for x > 0, exp(x) otherwise.  Returns the mapped arrays
     (None for an argument given as None).
     """
+    if qk_map not in ("silu_norm", "elu1"):
+        raise ValueError(qk_map)
     def silu_norm(x):
         x = np.asarray(x, dtype=np.float64)
         s = x / (1.0 + np.exp(-x))
         n = np.sqrt((s * s).sum(axis=-1, keepdims=True))
         return s / np.maximum(n, 1e-12)
 
-    out_q = None if q is None else silu_norm(q)
-    out_k = None if k is None else silu_norm(k)
+    def elu1(x):
+        x = np.asarray(x, dtype=np.float64)
+        return np.where(x > 0.0, x + 1.0, np.exp(np.minimum(x, 0.0)))
+
+    fmap = silu_norm if qk_map == "silu_norm" else elu1
+    out_q = None if q is None else fmap(q)
+    out_k = None if k is None else fmap(k)
     out_b = None if beta_logit is None else 1.0 / (1.0 + np.exp(-np.asarray(beta_logit, np.float64)))
     return out_q, out_k, out_b
 

@@ -159,5 +159,54 @@ int kda_oracle_linear(const float *q, const float *k, const float *v,
   return 0;
 }
 
+/*
+ * Normalised linear attention, one head, float64, token by token, from a
+ * zero state:
+ *
+ *   S   = Diag(a_t) S + k_t v_t^T      as kda_oracle_linear
+ *   z   = a_t * z + k_t                the normaliser accumulator (per key channel)
+ *   o_t = (S^T q_t) / (q_t . z)        read-out after the write, divided
+ *
+ * Source: "22,580: From GPT-2 to Kimi K3" (yichencityu.github.io), the linear
+ * attention of the interlude before section 6.2: the state gathers k v^T and a
+ * normaliser z gathers k, the read-out q S is divided by q z (with q and k
+ * passed through a positive feature map first, e.g. ELU + 1; the caller
+ * applies it).  The decayed form applies a_t to z exactly as to the rows of S
+ * (z is the state's column for a value of all ones); the pages print a_t = 1.
+ * A zero denominator is left to IEEE arithmetic.  Writes o [T][dv] and the
+ * final S to hT and the final z to zT.  Returns 0, or -1 on bad arguments.
+ */
+int kda_oracle_linear_norm(const float *q, const float *k, const float *v,
+                           const float *log_alpha, int alpha_mode, long T, int dk, int dv,
+                           double *o, double *hT, double *zT) {
+  if (T < 0 || dk <= 0 || dv <= 0 || !o || !hT || !zT) return -1;
+  if (alpha_mode < 0 || alpha_mode > 2) return -1;
+  if (alpha_mode != ORACLE_ALPHA_NONE && !log_alpha) return -1;
+  if (T > 0 && (!q || !k || !v)) return -1;
+  memset(hT, 0, sizeof(double) * (size_t)dk * (size_t)dv);
+  memset(zT, 0, sizeof(double) * (size_t)dk);
+  for (long t = 0; t < T; ++t) {
+    const float *qt = q + t * dk, *kt = k + t * dk, *vt = v + t * dv;
+    for (int i = 0; i < dk; ++i) {
+      double ai = 1.0;  /* a_t of key channel i */
+      if (alpha_mode == ORACLE_ALPHA_CHANNEL)
+        ai = exp(-exp((double)log_alpha[t * dk + i]));
+      else if (alpha_mode == ORACLE_ALPHA_SCALAR)
+        ai = exp(-exp((double)log_alpha[t]));
+      double *Si = hT + (size_t)i * dv;
+      for (int j = 0; j < dv; ++j) Si[j] = ai * Si[j] + (double)kt[i] * (double)vt[j];
+      zT[i] = ai * zT[i] + (double)kt[i];
+    }
+    double den = 0.0;
+    for (int i = 0; i < dk; ++i) den += (double)qt[i] * zT[i];
+    for (int j = 0; j < dv; ++j) {
+      double num = 0.0;
+      for (int i = 0; i < dk; ++i) num += (double)qt[i] * hT[(size_t)i * dv + j];
+      o[t * dv + j] = num / den;
+    }
+  }
+  return 0;
+}
+
 /* Interface version, so the Python side can refuse a stale build. */
-int kda_oracle_version(void) { return 2; }
+int kda_oracle_version(void) { return 3; }

@@ -176,3 +176,106 @@ def test_planted_linear_slip_is_caught(tmp_path, name):
     assert src.count(old) == 1, f"mutation anchor for {name!r} not found once"
     lib = _compile(src.replace(old, new), tmp_path, "mut")
     assert not all(_linear_pins_pass(lib)), f"no pin caught: {name}"
+
+
+# ---------------------------------------------------------------- normalised form
+#
+# The interlude's linear attention with its normaliser: z = a_t z + k_t,
+# o_t = S^T q_t / (q_t . z).  Pinned by the explicit causal ratio of kernel
+# sums, o_t = sum_{s<=t} w_ts v_s / sum_{s<=t} w_ts with
+# w_ts = sum_c q_tc k_sc e^{g_tc - g_sc} (the closed form above, evaluated for
+# v and for a value of all ones), by invariants that hold for any positive
+# weights, and by planted slips.
+
+
+def _mapped_head(rng, T=40, dk=6, dv=5, mode="channel"):
+    q, k, v, la, _ = _head(rng, T=T, dk=dk, dv=dv, mode=mode, h0=False)
+    mq, mk, _ = oracle.input_maps(q, k, qk_map="elu1")
+    return mq.astype(np.float32), mk.astype(np.float32), v, la
+
+
+def _kernel_ratio(q, k, v, la):
+    num, _ = _closed_form(q, k, v, la, None)
+    den, _ = _closed_form(q, k, np.ones((q.shape[0], 1)), la, None)
+    return num / den
+
+
+@pytest.mark.parametrize("mode", ["none", "scalar", "channel"])
+def test_linear_norm_matches_kernel_ratio(mode):
+    rng = np.random.default_rng(31 + len(mode))
+    q, k, v, la = _mapped_head(rng, mode=mode)
+    o, _, _ = oracle.linear_norm(q, k, v, la)
+    assert _close(o, _kernel_ratio(q, k, v, la))
+
+
+def test_linear_norm_state_and_normaliser_closed_forms():
+    rng = np.random.default_rng(37)
+    q, k, v, la = _mapped_head(rng, mode="channel")
+    _, hT, zT = oracle.linear_norm(q, k, v, la)
+    _, h_c = _closed_form(q, k, v, la, None)
+    _, z_c = _closed_form(q, k, np.ones((q.shape[0], 1)), la, None)
+    assert _close(hT, h_c) and _close(zT, z_c[:, 0])
+
+
+def test_linear_norm_constant_values_are_returned():
+    rng = np.random.default_rng(41)
+    q, k, _, la = _mapped_head(rng, mode="channel")
+    c = np.array([0.5, -2.0, 3.0], np.float32)
+    o, _, _ = oracle.linear_norm(q, k, np.tile(c, (q.shape[0], 1)), la)
+    assert np.abs(o - c).max() <= 1e-12 * np.abs(c).max()
+
+
+def test_linear_norm_first_token_reads_its_own_value():
+    rng = np.random.default_rng(43)
+    q, k, v, la = _mapped_head(rng, T=1, mode="channel")
+    o, _, _ = oracle.linear_norm(q, k, v, la)
+    assert np.abs(o[0] - v[0]).max() <= 1e-13 * np.abs(v[0]).max()
+
+
+def test_elu1_map_matches_torch():
+    rng = np.random.default_rng(47)
+    x = 3.0 * rng.standard_normal((3, 11, 16))
+    x[0, 0, :4] = 0.0
+    mq, mk, _ = oracle.input_maps(x, -x, qk_map="elu1")
+    tx = torch.from_numpy(x)
+    # torch forms elu(x) + 1 as expm1(x) + 1: about 1e-16 absolute below zero
+    assert np.allclose(mq, (torch.nn.functional.elu(tx) + 1).numpy(), rtol=1e-14, atol=1e-15)
+    assert np.allclose(mk, (torch.nn.functional.elu(-tx) + 1).numpy(), rtol=1e-14, atol=1e-15)
+    assert np.all(mq > 0) and np.all(mq[0, 0, :4] == 1.0)
+
+
+LINEAR_NORM_MUTANTS = {
+    "normaliser not decayed": ("zT[i] = ai * zT[i] + (double)kt[i];",
+                               "zT[i] = zT[i] + (double)kt[i];"),
+    "normaliser read with the key": ("den += (double)qt[i] * zT[i];",
+                                     "den += (double)kt[i] * zT[i];"),
+    "normaliser decays the new key": ("zT[i] = ai * zT[i] + (double)kt[i];",
+                                      "zT[i] = ai * (zT[i] + (double)kt[i]);"),
+    "no division": ("o[t * dv + j] = num / den;", "o[t * dv + j] = num;"),
+    "state decays the new write": ("Si[j] = ai * Si[j] + (double)kt[i] * (double)vt[j];",
+                                   "Si[j] = ai * (Si[j] + (double)kt[i] * (double)vt[j]);"),
+}
+
+
+def _linear_norm_pins_pass(lib):
+    ok = []
+    for mode in ("none", "channel", "scalar"):
+        rng = np.random.default_rng(51 + len(mode))
+        q, k, v, la = _mapped_head(rng, mode=mode)
+        o, _, zT = oracle.linear_norm(q, k, v, la, lib=lib)
+        _, z_c = _closed_form(q, k, np.ones((q.shape[0], 1)), la, None)
+        ok.append(_close(o, _kernel_ratio(q, k, v, la)) and _close(zT, z_c[:, 0]))
+    return ok
+
+
+def test_unmodified_linear_norm_oracle_passes(tmp_path):
+    assert all(_linear_norm_pins_pass(_compile(open(SRC).read(), tmp_path, "orig_n")))
+
+
+@pytest.mark.parametrize("name", sorted(LINEAR_NORM_MUTANTS))
+def test_planted_linear_norm_slip_is_caught(tmp_path, name):
+    old, new = LINEAR_NORM_MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name!r} not found once"
+    lib = _compile(src.replace(old, new), tmp_path, "mut_n")
+    assert not all(_linear_norm_pins_pass(lib)), f"no pin caught: {name}"
