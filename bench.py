@@ -367,11 +367,13 @@ def run_ours(args, rank, world, local, dist):
 
     # ---- the other update rule and the fused input maps, same workload
     def time_variant(rule, maps):
-        beta_arg = None if rule == kda.KDA_RULE_LINEAR else d["beta"]
+        beta_arg = None if rule != kda.KDA_RULE_DELTA else d["beta"]
+        state = rule != kda.KDA_RULE_LINEAR_NORM   # the normalised rule keeps (S, z) internal
 
         def call():
-            kda.kda_chunk_fwd_rule(d["q"], d["k"], d["v"], beta_arg, d["log_alpha"], d["h0"], o,
-                                   hT, w.C, ws, rule, maps, stream)
+            kda.kda_chunk_fwd_rule(d["q"], d["k"], d["v"], beta_arg, d["log_alpha"],
+                                   d["h0"] if state else None, o, hT if state else None, w.C, ws,
+                                   rule, maps, stream)
 
         for _ in range(args.warmup):
             call()
@@ -394,6 +396,10 @@ def run_ours(args, rank, world, local, dist):
         "fused_input_maps": dict(
             time_variant(kda.KDA_RULE_DELTA, kda.KDA_MAP_QK_SILU_NORM | kda.KDA_MAP_BETA_SIGMOID),
             maps="q, k <- normalize(silu(.)), beta <- sigmoid(.) inside the prep kernel"),
+        "normalised_linear_attention": dict(
+            time_variant(kda.KDA_RULE_LINEAR_NORM, kda.KDA_MAP_QK_ELU1),
+            rule="q, k <- elu(.) + 1; S = Diag(a) S + k v^T, z = a z + k, o = S^T q / q.z "
+                 "(kda_chunk_fwd_rule, KDA_RULE_LINEAR_NORM, KDA_MAP_QK_ELU1)"),
     }
 
     # ---- end to end through the public API with host buffers

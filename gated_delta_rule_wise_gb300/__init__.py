@@ -25,8 +25,8 @@ __all__ = [
     "kda_chunk_fwd_status", "kda_decode_step", "kda_selftest_wait_timeout",
     "kda_chunk_fwd_launches", "kda_chunk_fwd_kernel_names", "kernel_sources",
     "kda_chunk_fwd_host", "kda_chunk_fwd_host_buffer_size", "host_buffer_for",
-    "kda_chunk_fwd_rule", "KDA_RULE_DELTA", "KDA_RULE_LINEAR", "KDA_MAP_QK_SILU_NORM",
-    "KDA_MAP_BETA_SIGMOID", "kda_attn_res", "attn_res",
+    "kda_chunk_fwd_rule", "KDA_RULE_DELTA", "KDA_RULE_LINEAR", "KDA_RULE_LINEAR_NORM",
+    "KDA_MAP_QK_SILU_NORM", "KDA_MAP_BETA_SIGMOID", "KDA_MAP_QK_ELU1", "kda_attn_res", "attn_res",
     "chunk_fwd", "decode_step", "workspace_for",
     "KDA_F32", "KDA_BF16", "KDA_ALPHA_NONE", "KDA_ALPHA_SCALAR", "KDA_ALPHA_CHANNEL",
     "KDA_PATH_AUTO", "KDA_PATH_CUDA_CORE", "KDA_PATH_TENSOR",
@@ -187,8 +187,8 @@ def kda_chunk_fwd(q, k, v, beta, log_alpha, h0, o, hT, C, workspace, stream=None
     kda_chunk_fwd_ex(q, k, v, beta, log_alpha, h0, o, hT, C, workspace, stream, KDA_PATH_AUTO)
 
 
-KDA_RULE_DELTA, KDA_RULE_LINEAR = 0, 1
-KDA_MAP_QK_SILU_NORM, KDA_MAP_BETA_SIGMOID = 1, 2
+KDA_RULE_DELTA, KDA_RULE_LINEAR, KDA_RULE_LINEAR_NORM = 0, 1, 2
+KDA_MAP_QK_SILU_NORM, KDA_MAP_BETA_SIGMOID, KDA_MAP_QK_ELU1 = 1, 2, 4
 
 
 def kda_chunk_fwd_rule(q, k, v, beta, log_alpha, h0, o, hT, C, workspace, rule=KDA_RULE_DELTA,

@@ -136,10 +136,13 @@ kda_status kda_chunk_fwd_rule(const void *q, const void *k, const void *v, const
                               int H, int T, int dk, int dv, int C, kda_dtype dt,
                               kda_alpha_mode am, kda_rule rule, unsigned maps, void *workspace,
                               size_t ws_bytes, kda_stream_t stream) {
-  const unsigned known = KDA_MAP_QK_SILU_NORM | KDA_MAP_BETA_SIGMOID;
-  if (rule != KDA_RULE_DELTA && rule != KDA_RULE_LINEAR) return KDA_ERR_INVALID_ARG;
+  const unsigned known = KDA_MAP_QK_SILU_NORM | KDA_MAP_BETA_SIGMOID | KDA_MAP_QK_ELU1;
+  if (rule != KDA_RULE_DELTA && rule != KDA_RULE_LINEAR && rule != KDA_RULE_LINEAR_NORM)
+    return KDA_ERR_INVALID_ARG;
   if ((maps & ~known) != 0u) return KDA_ERR_INVALID_ARG;
-  if (rule == KDA_RULE_LINEAR && (maps & KDA_MAP_BETA_SIGMOID)) return KDA_ERR_INVALID_ARG;
+  if (rule != KDA_RULE_DELTA && (maps & KDA_MAP_BETA_SIGMOID)) return KDA_ERR_INVALID_ARG;
+  if ((maps & KDA_MAP_QK_SILU_NORM) && (maps & KDA_MAP_QK_ELU1)) return KDA_ERR_INVALID_ARG;
+  if (rule == KDA_RULE_LINEAR_NORM && (h0 || hT)) return KDA_ERR_UNSUPPORTED;
   if (rule == KDA_RULE_DELTA && maps == 0u)
     return kda_chunk_fwd_ex(q, k, v, beta, log_alpha, h0, o, hT, B, H, T, dk, dv, C, dt, am,
                             workspace, ws_bytes, stream, KDA_PATH_AUTO, nullptr, 0);

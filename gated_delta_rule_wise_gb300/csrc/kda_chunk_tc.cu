@@ -609,6 +609,17 @@ __device__ __forceinline__ void prep_d64(const __nv_bfloat16 *__restrict__ q,
 // The next chunk's input rows are prefetched into L2 during (5); its log_alpha,
 // k and v rows are bulk-copied as soon as the last product has read A's space
 // and blocks 2-3 (after (9)), its q rows after (10).
+// Normalised linear attention: per (head, chunk) two vectors the scan needs
+// besides the record, in a region that follows all records of the workspace:
+// the row sums of the chunk's M (the intra-chunk part of each denominator) and
+// sum_s Kbar_s (the chunk's contribution to the normaliser z).
+struct NormRec {
+  static constexpr uint32_t MR = 0;            // float [C]
+  static constexpr uint32_t KS = kC * 4;       // float [128]
+  static constexpr uint32_t BYTES = KS + 128 * 4;
+};
+static_assert(NormRec::BYTES % 16 == 0, "bulk-copied");
+
 struct PrepSmem128 {
   using R = Rec<128>;
   static constexpr int D = 128;
@@ -629,7 +640,9 @@ struct PrepSmem128 {
   static constexpr uint32_t GMID = GCS + D * 4;      // gamma_mid float [D]
   static constexpr uint32_t BETA = GMID + D * 4;     // float [C]
   static constexpr uint32_t PART = BETA + kC * 4;    // float [2][D]
-  static constexpr uint32_t BAR = PART + 2 * D * 4;
+  static constexpr uint32_t KSS = PART + 2 * D * 4;  // float [D] column sums of K/gamma (norm.)
+  static constexpr uint32_t MRS = KSS + D * 4;       // float [2][C] half-row sums of M (norm.)
+  static constexpr uint32_t BAR = MRS + 2 * kC * 4;
   static constexpr uint32_t LBAR = BAR + 8;   // log_alpha, k, v rows landed
   static constexpr uint32_t QBAR = LBAR + 8;  // q rows landed
   static constexpr uint32_t TMEMP = QBAR + 8;
@@ -657,9 +670,12 @@ __device__ __forceinline__ uint4 pack8(const float *x) {
                     pack_bf16x2(x[6], x[7]));
 }
 
-// kGeneral = false compiles the plain gated delta rule (rule and maps fixed
-// at 0, their code folded away); true reads them at run time.
-template <bool kGeneral>
+// kMode 0 compiles the plain gated delta rule (rule and maps fixed at 0, their
+// code folded away); 1 reads the rule and the silu / sigmoid maps at run time;
+// 2 adds the ELU + 1 map and the normalised linear-attention rule's sums.  The
+// modes are separate instantiations because the prep runs at the register
+// limit: code that only one mode needs would cost the others spills.
+template <int kMode>
 __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
                                           const __nv_bfloat16 *__restrict__ k,
                                           const __nv_bfloat16 *__restrict__ v,
@@ -668,6 +684,7 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
                                           int T, int NC, int total, uint8_t *__restrict__ ws,
                                           uint8_t *sm, int rule, unsigned maps) {
   constexpr int D = 128;
+  constexpr bool kGeneral = kMode != 0, kExt = kMode == 2;
   using Rr = Rec<128>;
   using L = PrepSmem128;
   constexpr int R = 32;                // rows per thread in the decay phase
@@ -680,6 +697,8 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
   float *gmid = reinterpret_cast<float *>(sm + L::GMID);
   float *betas = reinterpret_cast<float *>(sm + L::BETA);
   float *part = reinterpret_cast<float *>(sm + L::PART);
+  float *kss = reinterpret_cast<float *>(sm + L::KSS);
+  float *mrs = reinterpret_cast<float *>(sm + L::MRS);
   uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::BAR);
   uint64_t *lbar = reinterpret_cast<uint64_t *>(sm + L::LBAR);
   uint64_t *qbar = reinterpret_cast<uint64_t *>(sm + L::QBAR);
@@ -752,7 +771,9 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
     rule = KDA_RULE_DELTA;
     maps = 0u;
   }
-  const bool linear = rule == KDA_RULE_LINEAR;  // W = 0, U = V: no beta, no solve
+  const bool linear = rule != KDA_RULE_DELTA;   // W = 0, U = V: no beta, no solve
+  const bool norm = kExt && rule == KDA_RULE_LINEAR_NORM;  // also the normaliser's sums
+  uint8_t *const nrm0 = ws + sizeof(WorkspaceHeader) + (size_t)total * Rr::BYTES;
   auto beta_of = [&](int idx) -> float {        // beta of row tid of a chunk (tid < C)
     int vn;
     size_t rn;
@@ -827,6 +848,7 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
         EG[((c >> 2) & 1) * (L::EG_PLANE / 4) + (r0 + i) * (D / 2) + (c >> 3) * 4 + (c & 3)] =
             __expf(g);
       }
+      if (norm && half == 0) kss[c] = 0.f;
       if (half == 0) {
         gcs[c] = __expf(p1);   // gamma_C / gamma_mid: scales (K/gamma)^T into Kbar^T
         gmid[c] = __expf(p0);  // gamma_mid: turns Q*gamma (mid-referenced) into Q*gamma
@@ -861,6 +883,13 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
       unpack8(rk[m], kf);
       unpack8(rq[m], qf);
       unpack8(rv[m], vf);
+      if (kExt && (maps & KDA_MAP_QK_ELU1)) {  // q, k <- elu(x) + 1; rows past the end stay zero
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          qf[e] = r < valid ? (qf[e] > 0.f ? qf[e] + 1.f : __expf(qf[e])) : 0.f;
+          kf[e] = r < valid ? (kf[e] > 0.f ? kf[e] + 1.f : __expf(kf[e])) : 0.f;
+        }
+      }
       if (maps & KDA_MAP_QK_SILU_NORM) {  // q, k <- silu / ||silu||, the row's 16 lanes reduce
         float sq = 0.f, sk = 0.f;
 #pragma unroll
@@ -924,11 +953,36 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
         for (int j = 0; j < 32; ++j) x[j] = (cb + j <= r) ? x[j] : 0.f;
 #pragma unroll
         for (int j8 = 0; j8 < 4; ++j8) st_chunk(MM, r, (cb >> 3) + j8, kC, x + 8 * j8);
+        if (norm) {
+          float sum = 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) sum += x[j];
+          mrs[colhalf * kC + r] = sum;
+        }
       }
     };
     if (linear) {  // [W | U] = [0 | V] already sits in rows 0-63 of the tile area
       read_m();
+      if (norm && quarter < 2) {  // the other four warps: column sums of the K/gamma tile,
+        // thread = (8-channel chunk, 8 rows); the 8 row groups meet in kss
+        const int t4 = (colhalf * 2 + quarter) * 32 + lane, q8 = t4 & 15, g8 = t4 >> 4;
+        float cs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int rr = 0; rr < 8; ++rr) {
+          float kv[8];
+          ld_chunk(X1 + 32768, kC + g8 * 8 + rr, q8, 128, kv);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) cs[e] += kv[e];
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) atomicAdd(&kss[q8 * 8 + e], cs[e]);
+      }
       sync_for_mma();
+      if (norm) {  // the chunk's normaliser sums (both complete after the sync above)
+        float *nr = reinterpret_cast<float *>(nrm0 + (size_t)idx * NormRec::BYTES);
+        if (tid < kC) nr[tid] = mrs[tid] + mrs[kC + tid];
+        else if (tid < kC + D) nr[kC + (tid - kC)] = kss[tid - kC] * gcs[tid - kC];
+      }
     } else {
 
     // ---- (3) lanes 0..63: A (strict lower) as float, 32 columns per warp
@@ -1148,7 +1202,7 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
   }
 }
 
-template <int D, bool kGeneral>
+template <int D, int kMode>
 __global__ void __launch_bounds__(256, D == 128 ? 2 : 1)
 kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                 const __nv_bfloat16 *__restrict__ v, const float *__restrict__ beta,
@@ -1158,7 +1212,7 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));
   if constexpr (D == 128)
-    prep_d128<kGeneral>(q, k, v, beta, log_alpha, alpha_mode, T, NC, total, ws, sm, rule, maps);
+    prep_d128<kMode>(q, k, v, beta, log_alpha, alpha_mode, T, NC, total, ws, sm, rule, maps);
   else
     prep_d64(q, k, v, beta, log_alpha, alpha_mode, T, NC, total, ws, sm);
 }
@@ -1203,10 +1257,12 @@ struct ScanSmem128 {
   static constexpr uint32_t OI_S = BI_S + 128 * NB * 2;      // O block [C][NB]
   static constexpr uint32_t GC_S = OI_S + kC * NB * 2;       // gamma_C [128]
   static constexpr uint32_t STAGE_BYTES = GC_S + 128 * 4;
-  static constexpr uint32_t STAGE = align1k(STAGE_BYTES);
+  static constexpr uint32_t NRM_S = STAGE_BYTES;             // NormRec (normalised rule only)
+  static constexpr uint32_t STAGE = align1k(NRM_S + NormRec::BYTES);
   static constexpr uint32_t SB = kStages * STAGE;            // 2 x bf16 S [128 rows][64 cols]
+  static constexpr uint32_t ZS = SB + 2 * 128 * 64 * 2;      // float [128]: z at the chunk start
   // full[kStages], empty[kStages], mS, mO[kOutBufs], ofree[kOutBufs]
-  static constexpr uint32_t BAR = SB + 2 * 128 * 64 * 2;
+  static constexpr uint32_t BAR = ZS + 128 * 4;
   static constexpr uint32_t TMEMP = BAR + (2 * kStages + 1 + 2 * kOutBufs) * 8;
   static constexpr uint32_t BYTES = TMEMP + 8;
   static constexpr uint32_t TMEM_COLS = 128;                 // P | o[0] | o[1] | o[2]
@@ -1214,10 +1270,14 @@ struct ScanSmem128 {
   static_assert(BYTES + 1024 <= 232448, "scan shared memory");
 };
 
-template <int NB>
+// kNorm: the normalised linear-attention rule (the output warps also carry
+// the normaliser and divide); a separate instantiation, so that the other
+// rules' scan is compiled without it.
+template <int NB, bool kNorm>
 __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfloat16 *__restrict__ o,
                                           float *__restrict__ hT, int T, int NC,
                                           uint8_t *__restrict__ ws, uint8_t *sm) {
+  constexpr bool norm = kNorm;
   constexpr int D = 128;
   constexpr uint32_t kSyncThreads = 128 + 32;  // state warps + issuer warp
   using R = Rec<128>;
@@ -1233,6 +1293,8 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.y, blk = blockIdx.x, j0 = blk * NB;
   const uint8_t *rec0 = ws + sizeof(WorkspaceHeader) + (size_t)bh * NC * R::BYTES;
+  const uint8_t *nrm0 = ws + sizeof(WorkspaceHeader) + (size_t)gridDim.y * NC * R::BYTES +
+                        (size_t)bh * NC * NormRec::BYTES;
   bool ok = true;
 
   if (tid == 0) {
@@ -1270,7 +1332,9 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
         uint8_t *st = sm + s * L::STAGE;
         const uint8_t *rec = rec0 + (size_t)j * R::BYTES;
         ptx::fence_proxy_async_smem();
-        ptx::mbar_arrive_expect_tx(&full[s], L::STAGE_BYTES);
+        ptx::mbar_arrive_expect_tx(&full[s], L::STAGE_BYTES + (norm ? NormRec::BYTES : 0u));
+        if (norm)
+          ptx::bulk_g2s(st + L::NRM_S, nrm0 + (size_t)j * NormRec::BYTES, NormRec::BYTES, &full[s]);
         ptx::bulk_g2s(st, rec, R::PRE, &full[s]);
         ptx::bulk_g2s(st + L::BI_S, rec + R::BI + (size_t)blk * (128 * NB * 2), 128 * NB * 2, &full[s]);
         ptx::bulk_g2s(st + L::OI_S, rec + R::OI + (size_t)blk * (kC * NB * 2), kC * NB * 2, &full[s]);
@@ -1313,6 +1377,11 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
   } else if (warp >= 4) {
     // ---------------------------------------------------------- output warps
     const int orow = (warp - 4) * 16 + lane;  // output row (M = 64 layout: lanes 32w + 0..15)
+    // normalised rule: thread c = tid - 128 carries z_c (key channel c); each
+    // chunk publishes z at its start to ZS, and the row's denominator is
+    // (Q gamma)_t . z_start (the record's Qp, as W = 0) + the row sum of M
+    float zc = 0.f;
+    float *zs = reinterpret_cast<float *>(sm + L::ZS);
     for (int j = 0; j < NC; ++j) {
       const int b = j % kOutBufs, s = j % kStages;
       if (ok && !ptx::mbar_wait(&mO[b], (j / kOutBufs) & 1, kWaitLimit)) {
@@ -1327,6 +1396,34 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
       const uint32_t tO = t_lane + NB * (1 + b);
       const uint8_t *oi = sm + s * L::STAGE + L::OI_S;
       const int t = j * kC + orow;
+      float inv_den = 1.f;
+      if (norm) {
+        const uint8_t *st = sm + s * L::STAGE;
+        const float *nr = reinterpret_cast<const float *>(st + L::NRM_S);
+        const int c = tid - 128;
+        zs[c] = zc;
+        zc = reinterpret_cast<const float *>(st + L::GC_S)[c] * zc + nr[NormRec::KS / 4 + c];
+        ptx::named_barrier(2, 128);  // z_start complete
+        // row (warp - 4) * 16 + (lane & 15); lanes 0-15 take channels 0-63, 16-31 64-127
+        const int drow = (warp - 4) * 16 + (lane & 15), atom = lane >> 4;
+        const uint8_t *qrow = st + R::QP + atom * (kC * 128) + drow * 128;
+        float acc = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          const uint4 u = *reinterpret_cast<const uint4 *>(qrow + ((cc ^ (drow & 7)) << 4));
+          const float4 z0 = *reinterpret_cast<const float4 *>(zs + atom * 64 + cc * 8);
+          const float4 z1 = *reinterpret_cast<const float4 *>(zs + atom * 64 + cc * 8 + 4);
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+          const float zz[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 p2 = *reinterpret_cast<const __nv_bfloat162 *>(&w[e]);
+            acc += __low2float(p2) * zz[2 * e] + __high2float(p2) * zz[2 * e + 1];
+          }
+        }
+        acc += __shfl_xor_sync(0xffffffffu, acc, 16);
+        inv_den = 1.f / (acc + nr[NormRec::MR / 4 + drow]);
+      }
 #pragma unroll
       for (int cb = 0; cb < NB; cb += 16) {
         float x[16];
@@ -1340,7 +1437,8 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const __nv_bfloat162 p2 = *reinterpret_cast<const __nv_bfloat162 *>(&w[e]);
-            pk[e] = pack_bf16x2(x[2 * e] + __low2float(p2), x[2 * e + 1] + __high2float(p2));
+            pk[e] = pack_bf16x2((x[2 * e] + __low2float(p2)) * inv_den,
+                                (x[2 * e + 1] + __high2float(p2)) * inv_den);
           }
           uint4 *dst = reinterpret_cast<uint4 *>(o + ((size_t)bh * T + t) * D + j0 + cb);
           dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -1639,7 +1737,7 @@ __device__ __forceinline__ void scan_d64(const float *__restrict__ h0, __nv_bflo
 }
 
 
-template <int D, int NB>
+template <int D, int NB, bool kNorm>
 __global__ void __launch_bounds__(kScan128Threads, 1)
 kda_scan_kernel(const float *__restrict__ h0, __nv_bfloat16 *__restrict__ o,
                 float *__restrict__ hT, int T, int NC, uint8_t *__restrict__ ws) {
@@ -1647,7 +1745,7 @@ kda_scan_kernel(const float *__restrict__ h0, __nv_bfloat16 *__restrict__ o,
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));
   if constexpr (D == 128)
-    scan_d128<NB>(h0, o, hT, T, NC, ws, sm);
+    scan_d128<NB, kNorm>(h0, o, hT, T, NC, ws, sm);
   else
     scan_d64<NB>(h0, o, hT, T, NC, ws, sm);
 }
@@ -1667,13 +1765,20 @@ kda_status launch_d(const void *q, const void *k, const void *v, const float *be
   const uint32_t prep_smem = (D == 128 ? PrepSmem128::BYTES : PrepSmem64::BYTES) + 1024;
   const uint32_t scan_smem =
       (D == 128 ? ScanSmem128<NB>::BYTES : ScanSmem64<NB>::BYTES) + 1024;
-  auto prep = kda_prep_kernel<D, false>;
+  auto prep = kda_prep_kernel<D, 0>;
   if constexpr (D == 128) {
-    if (rule != 0 || maps != 0u) prep = kda_prep_kernel<D, true>;
+    if (rule == KDA_RULE_LINEAR_NORM || (maps & KDA_MAP_QK_ELU1))
+      prep = kda_prep_kernel<D, 2>;
+    else if (rule != 0 || maps != 0u)
+      prep = kda_prep_kernel<D, 1>;
+  }
+  auto scan = kda_scan_kernel<D, NB, false>;
+  if constexpr (D == 128) {
+    if (rule == KDA_RULE_LINEAR_NORM) scan = kda_scan_kernel<D, NB, true>;
   }
   if (cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)prep_smem) != cudaSuccess ||
-      cudaFuncSetAttribute(kda_scan_kernel<D, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaFuncSetAttribute(scan, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)scan_smem) != cudaSuccess)
     return KDA_ERR_CUDA;
   if (NC > 0) {
@@ -1692,7 +1797,7 @@ kda_status launch_d(const void *q, const void *k, const void *v, const float *be
         rule, maps);
   }
   timer.mark();
-  kda_scan_kernel<D, NB><<<dim3(D / NB, BH), D == 128 ? kScan128Threads : 128, scan_smem, st>>>(
+  scan<<<dim3(D / NB, BH), D == 128 ? kScan128Threads : 128, scan_smem, st>>>(
       h0, static_cast<__nv_bfloat16 *>(o), hT, T, NC, ws);
   timer.mark();
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
@@ -1707,7 +1812,9 @@ bool chunk_tc_supported(int dk, int dv, int C, kda_dtype dt) {
 size_t chunk_tc_workspace_bytes(int B, int H, int T, int dk, int dv, int C) {
   if (dk != dv || C != kC) return 0;
   const size_t NC = (size_t)(T + kC - 1) / kC;
-  const size_t rec = dk == 128 ? Rec<128>::BYTES : Rec<64>::BYTES;
+  // d = 128: each chunk record is followed, after all of them, by its
+  // normaliser sums (read only by the normalised linear-attention rule)
+  const size_t rec = dk == 128 ? Rec<128>::BYTES + NormRec::BYTES : Rec<64>::BYTES;
   return (size_t)B * H * NC * rec;
 }
 

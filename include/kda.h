@@ -211,20 +211,32 @@ kda_status kda_chunk_fwd_status(void *workspace, kda_stream_t stream);
  *                    masked scores), with the same optional decay applied
  *                    first:  S = Diag(a_t) S + k_t v_t^T,  o_t = S^T q_t.
  *                    No normaliser; beta is not read (may be NULL).
+ *   KDA_RULE_LINEAR_NORM  the same page's linear attention with its
+ *                    normaliser (the interlude before section 6.2): a second
+ *                    accumulator z = Diag(a_t) z + k_t (the state's column for
+ *                    a value of all ones) and o_t = S^T q_t / (q_t . z).  Meant
+ *                    with KDA_MAP_QK_ELU1, which keeps q . z positive.  From
+ *                    a zero state only: h0 and hT must be NULL
+ *                    (KDA_ERR_UNSUPPORTED otherwise); beta is not read.
  * input_maps (bit set), the maps the same page's section 5.2 applies to the
  * projections before the delta rule:
  *   KDA_MAP_QK_SILU_NORM  q, k <- silu(x) / max(||silu(x)||_2, 1e-12) per
  *                         (token, head), silu(x) = x / (1 + exp(-x))
- *   KDA_MAP_BETA_SIGMOID  beta <- 1 / (1 + exp(-beta))   (not with LINEAR)
+ *   KDA_MAP_BETA_SIGMOID  beta <- 1 / (1 + exp(-beta))   (DELTA only)
+ *   KDA_MAP_QK_ELU1       q, k <- elu(x) + 1 = (x > 0 ? x + 1 : exp(x)), the
+ *                         feature map of the page's linear attention
+ *                         (not with QK_SILU_NORM)
  *
  * Other arguments as kda_chunk_fwd (same workspace size).  rule DELTA with
  * no maps is kda_chunk_fwd (every shape); anything else runs on the tensor
  * path only: bf16, C = 64, dk = dv = 128, else KDA_ERR_UNSUPPORTED.  An
- * unknown rule or map bit, or BETA_SIGMOID with LINEAR: KDA_ERR_INVALID_ARG.
+ * unknown rule or map bit, BETA_SIGMOID with a linear rule, or both q, k
+ * maps: KDA_ERR_INVALID_ARG.
  */
-typedef enum { KDA_RULE_DELTA = 0, KDA_RULE_LINEAR = 1 } kda_rule;
+typedef enum { KDA_RULE_DELTA = 0, KDA_RULE_LINEAR = 1, KDA_RULE_LINEAR_NORM = 2 } kda_rule;
 #define KDA_MAP_QK_SILU_NORM 1u
 #define KDA_MAP_BETA_SIGMOID 2u
+#define KDA_MAP_QK_ELU1 4u
 kda_status kda_chunk_fwd_rule(const void *q, const void *k, const void *v,
                               const float *beta, const float *log_alpha,
                               const float *h0, void *o, float *hT,

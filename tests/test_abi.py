@@ -172,10 +172,26 @@ def test_tensor_path_is_what_auto_picks_for_bf16_c64(lib):
     assert kda.kda_chunk_fwd_kernel_names(1, 1, 0, 128, 128, 64, kda.KDA_BF16, 2) == ["kda_scan_kernel"]
     assert kda.kda_chunk_fwd_kernel_names(1, 1, 64, 16, 16, 16, kda.KDA_F32, 2) == ["chunk_ffma_kernel"]
     big = kda.kda_chunk_fwd_workspace_size(1, 32, 131072, 128, 128, 64, kda.KDA_BF16, 2)
-    assert big == 256 + 32 * 2048 * 98816     # one 98816-byte record per (head, chunk)
+    # one 98816-byte record per (head, chunk), then its 768 bytes of normaliser sums
+    assert big == 256 + 32 * 2048 * (98816 + 768)
 
 
 def test_status_and_selftest_validation(lib):
     assert lib.kda_chunk_fwd_status(None, None) == 1
     assert lib.kda_selftest_wait_timeout(FAKE, 256, 0, None) == 1
     assert lib.kda_selftest_wait_timeout(FAKE, 16, 10, None) == 1
+
+
+def test_rule_argument_checks_before_any_launch(lib):
+    """kda_chunk_fwd_rule rejects bad rule / map combinations synchronously,
+    before it touches the device (fake pointers, no GPU needed)."""
+    def call(rule, maps, h0=None, hT=FAKE):
+        return lib.kda_chunk_fwd_rule(FAKE, FAKE, FAKE, None, None, h0, FAKE, hT,
+                                      1, 1, 64, 128, 128, 64, 1, 0, rule, maps, FAKE, 1 << 30,
+                                      None)
+    assert call(3, 0) == 1                      # unknown rule
+    assert call(1, 8) == 1                      # unknown map bit
+    assert call(2, 2) == 1                      # beta map with a linear rule
+    assert call(0, 1 | 4) == 1                  # two maps for q, k
+    assert call(2, 4, h0=FAKE, hT=None) == 2    # the normalised rule starts from zero ...
+    assert call(2, 4, h0=None, hT=FAKE) == 2    # ... and keeps its state (S, z) internal

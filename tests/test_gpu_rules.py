@@ -5,6 +5,9 @@
 - input maps: q, k = normalize(silu(.)) and beta = sigmoid(.) applied inside
   the prep kernel to raw projections; the oracle applies the same maps in
   float64 to the same stored values, then runs its token loop.
+- KDA_RULE_LINEAR_NORM with KDA_MAP_QK_ELU1: the same linear attention with
+  the ELU + 1 feature map on q, k and the normaliser (o = S^T q / q.z),
+  against the oracle's normalised loop on the same stored values.
 - argument checks of the new entry point.
 """
 import numpy as np
@@ -111,6 +114,53 @@ def test_input_maps_with_linear_rule():
     assert rel_err(hT.cpu().numpy().reshape(rh.shape), rh) <= TOL_BF16
 
 
+def _norm_case(name, T, alpha, seed, H=2):
+    """Raw q, k (N(0, 1.5^2), bf16, both signs so that ELU + 1 takes both
+    branches), v and decay from the workload generator, zero initial state."""
+    w = _prefill(name, T, alpha, 0.0, seed=seed, H=H)
+    x = W.prefill_inputs(w)
+    rng = np.random.default_rng(seed + 1000)
+    shp = (w.B, w.H, w.T, w.dk)
+    x["q"] = W.round_bf16((1.5 * rng.standard_normal(shp)).astype(np.float32))
+    x["k"] = W.round_bf16((1.5 * rng.standard_normal(shp)).astype(np.float32))
+    d = device_inputs(w, x)
+    d["beta"] = None
+    d["h0"] = None
+    return w, x, d
+
+
+def _norm_reference(x):
+    mq, mk, _ = oracle.input_maps(x["q"], x["k"], qk_map="elu1")
+    return oracle.linear_norm_heads(mq, mk, x["v"], x["log_alpha"])
+
+
+@pytest.mark.parametrize("alpha", ["none", "scalar", "channel"])
+def test_normalised_linear_attention_matches_oracle(alpha):
+    w, x, d = _norm_case("linn", 3 * 64 + 33, alpha, seed=101 + len(alpha))
+    o, _ = _run_rule(d, w.C, kda.KDA_RULE_LINEAR_NORM, kda.KDA_MAP_QK_ELU1, with_hT=False)
+    ro = _norm_reference(x)
+    eo = rel_err(o.float().cpu().numpy().reshape(ro.shape), ro)
+    assert eo <= TOL_BF16, eo
+
+
+def test_normalised_linear_attention_long_sequence():
+    """Many chunks: the normaliser and the state grow together chunk by chunk."""
+    w, x, d = _norm_case("linn_long", 4096, "channel", seed=121, H=3)
+    o, _ = _run_rule(d, w.C, kda.KDA_RULE_LINEAR_NORM, kda.KDA_MAP_QK_ELU1, with_hT=False)
+    ro = _norm_reference(x)
+    assert rel_err(o.float().cpu().numpy().reshape(ro.shape), ro) <= TOL_BF16
+
+
+def test_normalised_linear_attention_constant_values():
+    """v the same vector for every token: every output row is that vector."""
+    w, x, d = _norm_case("linn_const", 2 * 64 + 9, "channel", seed=131)
+    c = W.round_bf16(np.linspace(-2.0, 2.0, w.dv).astype(np.float32))
+    d["v"] = put(np.broadcast_to(c, d["v"].shape).copy()).to(d["v"].dtype)
+    o, _ = _run_rule(d, w.C, kda.KDA_RULE_LINEAR_NORM, kda.KDA_MAP_QK_ELU1, with_hT=False)
+    got = o.float().cpu().numpy()
+    assert np.abs(got - c).max() <= TOL_BF16 * np.abs(c).max()
+
+
 def test_default_rule_equals_kda_chunk_fwd():
     w = _prefill("rule0", 2 * 64 + 5, "channel", 0.05, seed=81)
     d = device_inputs(w, W.prefill_inputs(w))
@@ -124,8 +174,12 @@ def test_rule_argument_checks():
     w = _prefill("args", 64, "none", 0.0, seed=91)
     d = device_inputs(w, W.prefill_inputs(w))
     bad = [(kda.KDA_RULE_LINEAR, kda.KDA_MAP_BETA_SIGMOID, kda.KDA_ERR_INVALID_ARG),
-           (2, 0, kda.KDA_ERR_INVALID_ARG),
-           (kda.KDA_RULE_DELTA, 4, kda.KDA_ERR_INVALID_ARG)]
+           (kda.KDA_RULE_LINEAR_NORM, kda.KDA_MAP_BETA_SIGMOID, kda.KDA_ERR_INVALID_ARG),
+           (kda.KDA_RULE_DELTA, kda.KDA_MAP_QK_SILU_NORM | kda.KDA_MAP_QK_ELU1,
+            kda.KDA_ERR_INVALID_ARG),
+           (3, 0, kda.KDA_ERR_INVALID_ARG),
+           (kda.KDA_RULE_DELTA, 8, kda.KDA_ERR_INVALID_ARG),
+           (kda.KDA_RULE_LINEAR_NORM, kda.KDA_MAP_QK_ELU1, kda.KDA_ERR_UNSUPPORTED)]  # hT given
     for rule, maps, code in bad:
         with pytest.raises(kda.KdaError) as e:
             _run_rule(d, w.C, rule, maps)
