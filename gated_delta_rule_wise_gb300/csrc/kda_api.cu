@@ -142,6 +142,7 @@ kda_status kda_chunk_fwd_rule(const void *q, const void *k, const void *v, const
   if ((maps & ~known) != 0u) return KDA_ERR_INVALID_ARG;
   if (rule != KDA_RULE_DELTA && (maps & KDA_MAP_BETA_SIGMOID)) return KDA_ERR_INVALID_ARG;
   if ((maps & KDA_MAP_QK_SILU_NORM) && (maps & KDA_MAP_QK_ELU1)) return KDA_ERR_INVALID_ARG;
+  if (rule == KDA_RULE_DELTA && (maps & KDA_MAP_QK_ELU1)) return KDA_ERR_INVALID_ARG;
   if (rule == KDA_RULE_LINEAR_NORM && (h0 || hT)) return KDA_ERR_UNSUPPORTED;
   if (rule == KDA_RULE_DELTA && maps == 0u)
     return kda_chunk_fwd_ex(q, k, v, beta, log_alpha, h0, o, hT, B, H, T, dk, dv, C, dt, am,

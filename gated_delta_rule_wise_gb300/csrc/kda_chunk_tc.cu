@@ -672,9 +672,10 @@ __device__ __forceinline__ uint4 pack8(const float *x) {
 
 // kMode 0 compiles the plain gated delta rule (rule and maps fixed at 0, their
 // code folded away); 1 reads the rule and the silu / sigmoid maps at run time;
-// 2 adds the ELU + 1 map and the normalised linear-attention rule's sums.  The
-// modes are separate instantiations because the prep runs at the register
-// limit: code that only one mode needs would cost the others spills.
+// 2 is for the linear rules only (no solve compiled in) and adds the ELU + 1
+// map and the normalised rule's sums.  The modes are separate instantiations
+// because the prep runs at the register limit: code that only one mode needs
+// would cost the others spills.
 template <int kMode>
 __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
                                           const __nv_bfloat16 *__restrict__ k,
@@ -771,7 +772,7 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
     rule = KDA_RULE_DELTA;
     maps = 0u;
   }
-  const bool linear = rule != KDA_RULE_DELTA;   // W = 0, U = V: no beta, no solve
+  const bool linear = kExt || rule != KDA_RULE_DELTA;  // W = 0, U = V: no beta, no solve
   const bool norm = kExt && rule == KDA_RULE_LINEAR_NORM;  // also the normaliser's sums
   uint8_t *const nrm0 = ws + sizeof(WorkspaceHeader) + (size_t)total * Rr::BYTES;
   auto beta_of = [&](int idx) -> float {        // beta of row tid of a chunk (tid < C)
@@ -1260,9 +1261,8 @@ struct ScanSmem128 {
   static constexpr uint32_t NRM_S = STAGE_BYTES;             // NormRec (normalised rule only)
   static constexpr uint32_t STAGE = align1k(NRM_S + NormRec::BYTES);
   static constexpr uint32_t SB = kStages * STAGE;            // 2 x bf16 S [128 rows][64 cols]
-  static constexpr uint32_t ZS = SB + 2 * 128 * 64 * 2;      // float [128]: z at the chunk start
   // full[kStages], empty[kStages], mS, mO[kOutBufs], ofree[kOutBufs]
-  static constexpr uint32_t BAR = ZS + 128 * 4;
+  static constexpr uint32_t BAR = SB + 2 * 128 * 64 * 2;
   static constexpr uint32_t TMEMP = BAR + (2 * kStages + 1 + 2 * kOutBufs) * 8;
   static constexpr uint32_t BYTES = TMEMP + 8;
   static constexpr uint32_t TMEM_COLS = 128;                 // P | o[0] | o[1] | o[2]
@@ -1270,18 +1270,25 @@ struct ScanSmem128 {
   static_assert(BYTES + 1024 <= 232448, "scan shared memory");
 };
 
-// kNorm: the normalised linear-attention rule (the output warps also carry
-// the normaliser and divide); a separate instantiation, so that the other
-// rules' scan is compiled without it.
+// kNorm: the normalised linear-attention rule.  Its normaliser z is the
+// state's column for a value of all ones (with W = 0 its update is
+// z <- gamma_C z + sum_s Kbar_s): the state warps carry z_r beside row r and
+// write it as column NB of the bf16 S copy, the output product runs with
+// N = NB + 8, and its column NB is Qp z, to which the output warps add the
+// row sum of M for the denominator.  A separate instantiation, so that the
+// other rules' scan is compiled without it.
 template <int NB, bool kNorm>
 __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfloat16 *__restrict__ o,
                                           float *__restrict__ hT, int T, int NC,
                                           uint8_t *__restrict__ ws, uint8_t *sm) {
-  constexpr bool norm = kNorm;
   constexpr int D = 128;
   constexpr uint32_t kSyncThreads = 128 + 32;  // state warps + issuer warp
   using R = Rec<128>;
   using L = ScanSmem128<NB>;
+  constexpr bool norm = kNorm;
+  constexpr int kOW = kNorm ? NB + 8 : NB;                     // output accumulator width
+  constexpr uint32_t kTmemCols = kNorm ? 256 : L::TMEM_COLS;  // P | o[0] | o[1] | o[2]
+  static_assert(NB + kOutBufs * kOW <= (int)kTmemCols, "TMEM columns");
   uint64_t *full = reinterpret_cast<uint64_t *>(sm + L::BAR);
   uint64_t *empty = full + kStages;
   uint64_t *mS = empty + kStages;
@@ -1310,7 +1317,7 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
     ptx::fence_mbar_init();
   }
   if (warp == 0) {
-    ptx::tmem_alloc(tmem_ptr, L::TMEM_COLS);
+    ptx::tmem_alloc(tmem_ptr, kTmemCols);
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
@@ -1361,11 +1368,11 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
           ptx::mma_bf16_ss(tmem, dAP + (uint64_t)(((ks >> 2) * D * 128 + (ks & 3) * 32) >> 4),
                            dSB + (uint64_t)(ks * 2048 >> 4), umma::idesc_bf16_bmn(128, NB), ks > 0);
         ptx::mma_commit(mS);
-        const uint32_t tOc = tmem + NB * (1 + b);
+        const uint32_t tOc = tmem + NB + kOW * b;
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)  // o = Qp S
+        for (int ks = 0; ks < D / 16; ++ks)  // o = Qp S  (and Qp z in column NB)
           ptx::mma_bf16_ss(tOc, dQP + (uint64_t)(((ks >> 2) * kC * 128 + (ks & 3) * 32) >> 4),
-                           dSB + (uint64_t)(ks * 2048 >> 4), umma::idesc_bf16_bmn(64, NB), ks > 0);
+                           dSB + (uint64_t)(ks * 2048 >> 4), umma::idesc_bf16_bmn(64, kOW), ks > 0);
         ptx::mma_commit(&mO[b]);
       }
       __syncwarp();
@@ -1377,11 +1384,6 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
   } else if (warp >= 4) {
     // ---------------------------------------------------------- output warps
     const int orow = (warp - 4) * 16 + lane;  // output row (M = 64 layout: lanes 32w + 0..15)
-    // normalised rule: thread c = tid - 128 carries z_c (key channel c); each
-    // chunk publishes z at its start to ZS, and the row's denominator is
-    // (Q gamma)_t . z_start (the record's Qp, as W = 0) + the row sum of M
-    float zc = 0.f;
-    float *zs = reinterpret_cast<float *>(sm + L::ZS);
     for (int j = 0; j < NC; ++j) {
       const int b = j % kOutBufs, s = j % kStages;
       if (ok && !ptx::mbar_wait(&mO[b], (j / kOutBufs) & 1, kWaitLimit)) {
@@ -1393,36 +1395,16 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
         report_error(hdr, KDA_ERR_TIMEOUT, 0x223u);
       }
       ptx::tc_fence_after();
-      const uint32_t tO = t_lane + NB * (1 + b);
+      const uint32_t tO = t_lane + NB + kOW * b;
       const uint8_t *oi = sm + s * L::STAGE + L::OI_S;
       const int t = j * kC + orow;
       float inv_den = 1.f;
-      if (norm) {
-        const uint8_t *st = sm + s * L::STAGE;
-        const float *nr = reinterpret_cast<const float *>(st + L::NRM_S);
-        const int c = tid - 128;
-        zs[c] = zc;
-        zc = reinterpret_cast<const float *>(st + L::GC_S)[c] * zc + nr[NormRec::KS / 4 + c];
-        ptx::named_barrier(2, 128);  // z_start complete
-        // row (warp - 4) * 16 + (lane & 15); lanes 0-15 take channels 0-63, 16-31 64-127
-        const int drow = (warp - 4) * 16 + (lane & 15), atom = lane >> 4;
-        const uint8_t *qrow = st + R::QP + atom * (kC * 128) + drow * 128;
-        float acc = 0.f;
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          const uint4 u = *reinterpret_cast<const uint4 *>(qrow + ((cc ^ (drow & 7)) << 4));
-          const float4 z0 = *reinterpret_cast<const float4 *>(zs + atom * 64 + cc * 8);
-          const float4 z1 = *reinterpret_cast<const float4 *>(zs + atom * 64 + cc * 8 + 4);
-          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-          const float zz[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const __nv_bfloat162 p2 = *reinterpret_cast<const __nv_bfloat162 *>(&w[e]);
-            acc += __low2float(p2) * zz[2 * e] + __high2float(p2) * zz[2 * e + 1];
-          }
-        }
-        acc += __shfl_xor_sync(0xffffffffu, acc, 16);
-        inv_den = 1.f / (acc + nr[NormRec::MR / 4 + drow]);
+      if (norm) {  // denominator: (Qp z)_t from column NB plus the row sum of M
+        float qz;
+        ptx::tmem_ld1(tO + NB, qz);
+        ptx::tmem_ld_wait();
+        const float *nr = reinterpret_cast<const float *>(sm + s * L::STAGE + L::NRM_S);
+        inv_den = 1.f / (qz + nr[NormRec::MR / 4 + (orow & (kC - 1))]);
       }
 #pragma unroll
       for (int cb = 0; cb < NB; cb += 16) {
@@ -1461,6 +1443,7 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
     // gamma_C S + B while the product runs, then S <- that + P.
     const int r = tid;  // key channel = TMEM lane
     const uint32_t tP = t_lane;
+    float zr = 0.f;     // normalised rule: z_r (zero initial state)
     float sr[NB];
     {
       const size_t s0 = (size_t)bh * D * D + (size_t)r * D + j0;
@@ -1473,6 +1456,10 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
       uint8_t *sb = sb_of(i);
 #pragma unroll
       for (int c8 = 0; c8 < NB / 8; ++c8) st_chunk(sb, r, c8, 128, sr + 8 * c8);
+      if (norm) {
+        const float zc[8] = {zr, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        st_chunk(sb, r, NB / 8, 128, zc);
+      }
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       // the checks the issuer's products need, made here where they are off
@@ -1496,6 +1483,8 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
       ptx::named_arrive(1, kSyncThreads);
       {  // gamma_C S + B while the product runs
         const float gam = reinterpret_cast<const float *>(st + L::GC_S)[r];
+        if (norm)
+          zr = gam * zr + reinterpret_cast<const float *>(st + L::NRM_S)[NormRec::KS / 4 + r];
 #pragma unroll
         for (int q4 = 0; q4 < NB / 8; ++q4) {
           const uint4 a = *reinterpret_cast<const uint4 *>(st + L::BI_S + rotated_chunk(r, q4));
@@ -1532,7 +1521,7 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
   __syncthreads();
   if (warp == 0) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, L::TMEM_COLS);
+    ptx::tmem_dealloc(tmem, kTmemCols);
   }
 }
 

@@ -162,6 +162,12 @@ __device__ __forceinline__ void tmem_st_wait() {
 
 // 32 lanes x 32 bits, 16 consecutive columns: thread t of the warp gets lane
 // (base lane + t), columns [col, col + 16).
+// One column of this warp's 32 lanes (one value per thread).
+__device__ __forceinline__ void tmem_ld1(uint32_t taddr, float &r) {
+  uint32_t u;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(u) : "r"(taddr) : "memory");
+  r = __uint_as_float(u);
+}
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&r)[16]) {
   uint32_t x[16];
   asm volatile(

@@ -225,13 +225,13 @@ kda_status kda_chunk_fwd_status(void *workspace, kda_stream_t stream);
  *   KDA_MAP_BETA_SIGMOID  beta <- 1 / (1 + exp(-beta))   (DELTA only)
  *   KDA_MAP_QK_ELU1       q, k <- elu(x) + 1 = (x > 0 ? x + 1 : exp(x)), the
  *                         feature map of the page's linear attention
- *                         (not with QK_SILU_NORM)
+ *                         (linear rules only; not with QK_SILU_NORM)
  *
  * Other arguments as kda_chunk_fwd (same workspace size).  rule DELTA with
  * no maps is kda_chunk_fwd (every shape); anything else runs on the tensor
  * path only: bf16, C = 64, dk = dv = 128, else KDA_ERR_UNSUPPORTED.  An
- * unknown rule or map bit, BETA_SIGMOID with a linear rule, or both q, k
- * maps: KDA_ERR_INVALID_ARG.
+ * unknown rule or map bit, BETA_SIGMOID with a linear rule, QK_ELU1 with the
+ * delta rule, or both q, k maps: KDA_ERR_INVALID_ARG.
  */
 typedef enum { KDA_RULE_DELTA = 0, KDA_RULE_LINEAR = 1, KDA_RULE_LINEAR_NORM = 2 } kda_rule;
 #define KDA_MAP_QK_SILU_NORM 1u

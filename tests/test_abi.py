@@ -193,5 +193,6 @@ def test_rule_argument_checks_before_any_launch(lib):
     assert call(1, 8) == 1                      # unknown map bit
     assert call(2, 2) == 1                      # beta map with a linear rule
     assert call(0, 1 | 4) == 1                  # two maps for q, k
+    assert call(0, 4) == 1                      # the feature map belongs to the linear rules
     assert call(2, 4, h0=FAKE, hT=None) == 2    # the normalised rule starts from zero ...
     assert call(2, 4, h0=None, hT=FAKE) == 2    # ... and keeps its state (S, z) internal

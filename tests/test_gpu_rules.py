@@ -179,6 +179,7 @@ def test_rule_argument_checks():
             kda.KDA_ERR_INVALID_ARG),
            (3, 0, kda.KDA_ERR_INVALID_ARG),
            (kda.KDA_RULE_DELTA, 8, kda.KDA_ERR_INVALID_ARG),
+           (kda.KDA_RULE_DELTA, kda.KDA_MAP_QK_ELU1, kda.KDA_ERR_INVALID_ARG),
            (kda.KDA_RULE_LINEAR_NORM, kda.KDA_MAP_QK_ELU1, kda.KDA_ERR_UNSUPPORTED)]  # hT given
     for rule, maps, code in bad:
         with pytest.raises(kda.KdaError) as e:
