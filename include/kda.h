@@ -212,7 +212,8 @@ kda_status kda_chunk_fwd_status(void *workspace, kda_stream_t stream);
  *                    first:  S = Diag(a_t) S + k_t v_t^T,  o_t = S^T q_t.
  *                    No normaliser; beta is not read (may be NULL).
  *   KDA_RULE_LINEAR_NORM  the same page's linear attention with its
- *                    normaliser (the interlude before section 6.2): a second
+ *                    normaliser (section 04, "Linear Attention: Bring Back
+ *                    the RNN"): a second
  *                    accumulator z = Diag(a_t) z + k_t (the state's column for
  *                    a value of all ones) and o_t = S^T q_t / (q_t . z).  Meant
  *                    with KDA_MAP_QK_ELU1, which keeps q . z positive.  From

@@ -124,7 +124,8 @@ int kda_oracle_recurrent(const float *q, const float *k, const float *v,
  * its own chunk, i.e. the token loop above with a_t = 1.  The decayed form
  * (a_t as in kda_oracle_recurrent) is the same decay applied before each
  * write; the pages print only a_t = 1.  No normaliser (the pages' section 6.2
- * form, not the feature-map-with-denominator variant of the interlude).
+ * form, not the feature-map-with-denominator variant of section 04; that one
+ * is kda_oracle_linear_norm).
  * Same layouts and return codes as kda_oracle_recurrent; there is no beta.
  */
 int kda_oracle_linear(const float *q, const float *k, const float *v,
@@ -167,8 +168,8 @@ int kda_oracle_linear(const float *q, const float *k, const float *v,
  *   z   = a_t * z + k_t                the normaliser accumulator (per key channel)
  *   o_t = (S^T q_t) / (q_t . z)        read-out after the write, divided
  *
- * Source: "22,580: From GPT-2 to Kimi K3" (yichencityu.github.io), the linear
- * attention of the interlude before section 6.2: the state gathers k v^T and a
+ * Source: "22,580: From GPT-2 to Kimi K3" (yichencityu.github.io), section 04
+ * ("Linear Attention: Bring Back the RNN"): the state gathers k v^T and a
  * normaliser z gathers k, the read-out q S is divided by q z (with q and k
  * passed through a positive feature map first, e.g. ELU + 1; the caller
  * applies it).  The decayed form applies a_t to z exactly as to the rows of S

@@ -180,7 +180,7 @@ def test_planted_linear_slip_is_caught(tmp_path, name):
 
 # ---------------------------------------------------------------- normalised form
 #
-# The interlude's linear attention with its normaliser: z = a_t z + k_t,
+# The linear attention of the same page's section 04 with its normaliser: z = a_t z + k_t,
 # o_t = S^T q_t / (q_t . z).  Pinned by the explicit causal ratio of kernel
 # sums, o_t = sum_{s<=t} w_ts v_s / sum_{s<=t} w_ts with
 # w_ts = sum_c q_tc k_sc e^{g_tc - g_sc} (the closed form above, evaluated for
