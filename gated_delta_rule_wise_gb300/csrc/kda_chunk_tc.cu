@@ -640,9 +640,7 @@ struct PrepSmem128 {
   static constexpr uint32_t GMID = GCS + D * 4;      // gamma_mid float [D]
   static constexpr uint32_t BETA = GMID + D * 4;     // float [C]
   static constexpr uint32_t PART = BETA + kC * 4;    // float [2][D]
-  static constexpr uint32_t KSS = PART + 2 * D * 4;  // float [D] column sums of K/gamma (norm.)
-  static constexpr uint32_t MRS = KSS + D * 4;       // float [2][C] half-row sums of M (norm.)
-  static constexpr uint32_t BAR = MRS + 2 * kC * 4;
+  static constexpr uint32_t BAR = PART + 2 * D * 4;
   static constexpr uint32_t LBAR = BAR + 8;   // log_alpha, k, v rows landed
   static constexpr uint32_t QBAR = LBAR + 8;  // q rows landed
   static constexpr uint32_t TMEMP = QBAR + 8;
@@ -698,8 +696,6 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
   float *gmid = reinterpret_cast<float *>(sm + L::GMID);
   float *betas = reinterpret_cast<float *>(sm + L::BETA);
   float *part = reinterpret_cast<float *>(sm + L::PART);
-  float *kss = reinterpret_cast<float *>(sm + L::KSS);
-  float *mrs = reinterpret_cast<float *>(sm + L::MRS);
   uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::BAR);
   uint64_t *lbar = reinterpret_cast<uint64_t *>(sm + L::LBAR);
   uint64_t *qbar = reinterpret_cast<uint64_t *>(sm + L::QBAR);
@@ -849,7 +845,6 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
         EG[((c >> 2) & 1) * (L::EG_PLANE / 4) + (r0 + i) * (D / 2) + (c >> 3) * 4 + (c & 3)] =
             __expf(g);
       }
-      if (norm && half == 0) kss[c] = 0.f;
       if (half == 0) {
         gcs[c] = __expf(p1);   // gamma_C / gamma_mid: scales (K/gamma)^T into Kbar^T
         gmid[c] = __expf(p0);  // gamma_mid: turns Q*gamma (mid-referenced) into Q*gamma
@@ -884,11 +879,12 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
       unpack8(rk[m], kf);
       unpack8(rq[m], qf);
       unpack8(rv[m], vf);
-      if (kExt && (maps & KDA_MAP_QK_ELU1)) {  // q, k <- elu(x) + 1; rows past the end stay zero
+      if (kExt && (maps & KDA_MAP_QK_ELU1)) {  // q, k <- elu(x) + 1 = max(x, 0) + exp(min(x, 0));
+        const float in = r < valid ? 1.f : 0.f;  // rows past the end stay zero
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          qf[e] = r < valid ? (qf[e] > 0.f ? qf[e] + 1.f : __expf(qf[e])) : 0.f;
-          kf[e] = r < valid ? (kf[e] > 0.f ? kf[e] + 1.f : __expf(kf[e])) : 0.f;
+          qf[e] = in * (fmaxf(qf[e], 0.f) + __expf(fminf(qf[e], 0.f)));
+          kf[e] = in * (fmaxf(kf[e], 0.f) + __expf(fminf(kf[e], 0.f)));
         }
       }
       if (maps & KDA_MAP_QK_SILU_NORM) {  // q, k <- silu / ||silu||, the row's 16 lanes reduce
@@ -921,7 +917,11 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
       float kb[8], qg[8], vb[8], kh[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        kb[e] = linear ? 0.f : bt * kf[e] * eg[e];
+        // linear rules: W = 0, except that the normalised rule puts a ones
+        // column (channel 0, valid rows) there: the products (K/gamma)^T W and
+        // M W then leave the chunk's key sums and M's row sums in column 0
+        kb[e] = linear ? ((norm && c8 == 0 && e == 0 && r < valid) ? 1.f : 0.f)
+                       : bt * kf[e] * eg[e];
         qg[e] = qf[e] * eg[e];
         vb[e] = bt * vf[e];
         kh[e] = kf[e] * __fdividef(1.f, eg[e]);
@@ -954,36 +954,11 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
         for (int j = 0; j < 32; ++j) x[j] = (cb + j <= r) ? x[j] : 0.f;
 #pragma unroll
         for (int j8 = 0; j8 < 4; ++j8) st_chunk(MM, r, (cb >> 3) + j8, kC, x + 8 * j8);
-        if (norm) {
-          float sum = 0.f;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) sum += x[j];
-          mrs[colhalf * kC + r] = sum;
-        }
       }
     };
     if (linear) {  // [W | U] = [0 | V] already sits in rows 0-63 of the tile area
       read_m();
-      if (norm && quarter < 2) {  // the other four warps: column sums of the K/gamma tile,
-        // thread = (8-channel chunk, 8 rows); the 8 row groups meet in kss
-        const int t4 = (colhalf * 2 + quarter) * 32 + lane, q8 = t4 & 15, g8 = t4 >> 4;
-        float cs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int rr = 0; rr < 8; ++rr) {
-          float kv[8];
-          ld_chunk(X1 + 32768, kC + g8 * 8 + rr, q8, 128, kv);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) cs[e] += kv[e];
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) atomicAdd(&kss[q8 * 8 + e], cs[e]);
-      }
       sync_for_mma();
-      if (norm) {  // the chunk's normaliser sums (both complete after the sync above)
-        float *nr = reinterpret_cast<float *>(nrm0 + (size_t)idx * NormRec::BYTES);
-        if (tid < kC) nr[tid] = mrs[tid] + mrs[kC + tid];
-        else if (tid < kC + D) nr[kC + (tid - kC)] = kss[tid - kC] * gcs[tid - kC];
-      }
     } else {
 
     // ---- (3) lanes 0..63: A (strict lower) as float, 32 columns per warp
@@ -1075,6 +1050,11 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
           ptx::tmem_ld32(t_lane + a * 64, *reinterpret_cast<float(*)[32]>(x));
           ptx::tmem_ld32(t_lane + a * 64 + 32, *reinterpret_cast<float(*)[32]>(x + 32));
           ptx::tmem_ld_wait();
+          if (norm && a == 0) {  // sum_s Kbar_s = gamma_C/gamma_mid * sum_s (K/gamma)_s
+            reinterpret_cast<float *>(nrm0 + (size_t)idx * NormRec::BYTES + NormRec::KS)[key] =
+                gcs[key] * x[0];
+            x[0] = 0.f;
+          }
 #pragma unroll
           for (int j = 0; j < 64; ++j) x[j] *= gk;
 #pragma unroll
@@ -1147,6 +1127,10 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
                                 *reinterpret_cast<float(*)[32]>(x + 32));
       ptx::tmem_ld_wait();
       if (colhalf == 0) {
+        if (norm && side == 0) {  // (M W)_t0 = sum_s M_ts; Qp keeps Q*gamma there
+          reinterpret_cast<float *>(nrm0 + (size_t)idx * NormRec::BYTES + NormRec::MR)[rr] = x[0];
+          x[0] = 0.f;
+        }
         uint8_t *stg = X1 + (quarter >> 1) * 16384 + (quarter & 1) * 4096;  // 4 KB
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {  // this thread's K atom is `side`
