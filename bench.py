@@ -421,15 +421,18 @@ def run_ours(args, rank, world, local, dist):
         e2e_step()
     e2e_steps = max(1, min(args.steps, 5))
     barrier(dist, torch)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
+    # an event after every step as well: the host link is shared with other
+    # tenants of the machine, and the per-step times show a slow stretch
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps + 1)]
+    evs[0].record(stream)
+    for i in range(e2e_steps):
         e2e_step()
-    e1.record(stream)
+        evs[i + 1].record(stream)
     barrier(dist, torch)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, dev)
+    e2e_ms = max_over_ranks(evs[0].elapsed_time(evs[-1]) / e2e_steps, dist, dev)
     e2e = {"value": world * tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+           "step_ms": [round(evs[i].elapsed_time(evs[i + 1]), 3) for i in range(e2e_steps)],
            "api": "kda_chunk_fwd_host from pinned host memory, 16 segments of T (all heads), "
                   "copy-in / prefill / copy-out of neighbouring segments overlapped",
            "steps": e2e_steps}
