@@ -92,7 +92,9 @@ const char *kda_status_string(kda_status s);
  * Returns 0 if the arguments are invalid or unsupported.  The workspace holds
  * a device error word (first 256 bytes) and, on the tensor-core path, the
  * per-chunk intermediates of the prep kernel (corrected keys and values,
- * decayed queries, the intra-chunk mask and decay factors).
+ * decayed queries, the intra-chunk mask and decay factors: 98,816 bytes per
+ * (head, chunk) at d = 128, followed at d = 128 by 768 bytes per (head,
+ * chunk) that only the normalised linear-attention rule fills).
  */
 size_t kda_chunk_fwd_workspace_size(int B, int H, int T, int dk, int dv, int C,
                                     kda_dtype dt, kda_alpha_mode am);
