@@ -1334,14 +1334,27 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
     }
   } else if (warp == 9) {
     // ---------------------------------------------------------- issuer
-    for (int i = 0; i < NC; ++i) {
-      const int s = i % kStages, b = i % kOutBufs;
-      // descriptors of the K-slices are the tile's descriptor plus a constant
-      // (shared memory addresses stay below 2^18): form them before the wait
-      const uint8_t *st = sm + s * L::STAGE;
-      const uint64_t dAP = umma::sdesc(ptx::smem_u32(st + R::AP));
-      const uint64_t dQP = umma::sdesc(ptx::smem_u32(st + R::QP));
-      const uint64_t dSB = umma::sdesc_mn(ptx::smem_u32(sb_of(i)), 128, 0);
+    // The descriptors of every ring slot, formed once (a K-slice's descriptor
+    // is its tile's plus a constant: shared memory addresses stay below
+    // 2^18), and the loop unrolled over six chunks, the period of the 3-stage
+    // record ring, the 3 output accumulators and the 2 S copies, so that
+    // nothing but the MMAs sits between the hand-off and the first product.
+    static_assert(kStages == 3 && kOutBufs == 3, "six-chunk issuer period");
+    uint64_t dAPs[kStages], dQPs[kStages], dSBs[2];
+#pragma unroll
+    for (int q = 0; q < kStages; ++q) {
+      dAPs[q] = umma::sdesc(ptx::smem_u32(sm + q * L::STAGE + R::AP));
+      dQPs[q] = umma::sdesc(ptx::smem_u32(sm + q * L::STAGE + R::QP));
+    }
+#pragma unroll
+    for (int q = 0; q < 2; ++q) dSBs[q] = umma::sdesc_mn(ptx::smem_u32(sb_of(q)), 128, 0);
+    for (int i0 = 0; i0 < NC; i0 += 6)
+#pragma unroll
+    for (int u = 0; u < 6; ++u) {
+      const int i = i0 + u;
+      if (i >= NC) break;
+      const int b = u % kOutBufs;
+      const uint64_t dAP = dAPs[u % kStages], dQP = dQPs[u % kStages], dSB = dSBs[u & 1];
       // bf16 S_i written and P_{i-1} read by every state thread, which have
       // also seen record i land and accumulator b freed by the output warps
       ptx::named_barrier(1, kSyncThreads);
