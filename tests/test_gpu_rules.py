@@ -143,6 +143,25 @@ def test_normalised_linear_attention_matches_oracle(alpha):
     assert eo <= TOL_BF16, eo
 
 
+@pytest.mark.parametrize("B,H,T", [(1, 1, 1), (1, 2, 33), (2, 2, 64), (2, 3, 2 * 64 + 5)])
+def test_normalised_linear_attention_edges(B, H, T):
+    """One token, a single partial chunk, exactly one chunk, and batches > 1."""
+    w = W.Prefill("linn_edge", B=B, H=H, T=T, dk=128, dv=128, C=64, dtype="bf16",
+                  alpha="channel", la_mu=-3.5, h0_sd=0.0, seed=141 + T)
+    x = W.prefill_inputs(w)
+    rng = np.random.default_rng(151 + T)
+    shp = (B, H, T, 128)
+    x["q"] = W.round_bf16((1.5 * rng.standard_normal(shp)).astype(np.float32))
+    x["k"] = W.round_bf16((1.5 * rng.standard_normal(shp)).astype(np.float32))
+    d = device_inputs(w, x)
+    d["beta"] = None
+    d["h0"] = None
+    o, _ = _run_rule(d, w.C, kda.KDA_RULE_LINEAR_NORM, kda.KDA_MAP_QK_ELU1, with_hT=False)
+    ro = _norm_reference(x)
+    eo = rel_err(o.float().cpu().numpy().reshape(ro.shape), ro)
+    assert eo <= TOL_BF16, eo
+
+
 def test_normalised_linear_attention_long_sequence():
     """Many chunks: the normaliser and the state grow together chunk by chunk."""
     w, x, d = _norm_case("linn_long", 4096, "channel", seed=121, H=3)
