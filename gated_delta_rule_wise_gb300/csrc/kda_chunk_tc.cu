@@ -1232,6 +1232,7 @@ struct ScanSmem64 {
 // their own arithmetic.  Four output warps (same TMEM lane quarters) wait
 // for an output product, add M U and store o.
 constexpr int kStages = 3;
+constexpr int kPrefetchAhead = 3;  // scan: records prefetched into L2 this many chunks ahead of their copy
 constexpr int kOutBufs = 3;
 constexpr int kScan128Threads = 320;  // 4 state warps, 4 output warps, producer, issuer
 template <int NB>
@@ -1322,6 +1323,17 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
         }
         uint8_t *st = sm + s * L::STAGE;
         const uint8_t *rec = rec0 + (size_t)j * R::BYTES;
+        // a later record into L2 ahead of its copy, so that the copy meets L2
+        // rather than DRAM latency; the Ap | Qp tile the four CTAs of a head
+        // share is prefetched by one of them (all four made the scan slower)
+        if (j + kPrefetchAhead < NC) {
+          const uint8_t *rp = rec0 + (size_t)(j + kPrefetchAhead) * R::BYTES;
+          if (blk == 0) ptx::prefetch_l2(rp, R::PRE);  // the head's shared Ap | Qp tile, once
+          ptx::prefetch_l2(rp + R::BI + (size_t)blk * (128 * NB * 2), 128 * NB * 2);
+          ptx::prefetch_l2(rp + R::OI + (size_t)blk * (kC * NB * 2), kC * NB * 2);
+          ptx::prefetch_l2(rp + R::GC, 128 * 4);
+          if (norm) ptx::prefetch_l2(nrm0 + (size_t)(j + kPrefetchAhead) * NormRec::BYTES, NormRec::BYTES);
+        }
         ptx::fence_proxy_async_smem();
         ptx::mbar_arrive_expect_tx(&full[s], L::STAGE_BYTES + (norm ? NormRec::BYTES : 0u));
         if (norm)
