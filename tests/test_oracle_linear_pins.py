@@ -279,3 +279,20 @@ def test_planted_linear_norm_slip_is_caught(tmp_path, name):
     assert src.count(old) == 1, f"mutation anchor for {name!r} not found once"
     lib = _compile(src.replace(old, new), tmp_path, "mut_n")
     assert not all(_linear_norm_pins_pass(lib)), f"no pin caught: {name}"
+
+
+def test_linear_norm_hand_worked_golden():
+    """Exact rational example (golden/hand_linear_norm_2tok.json): the
+    normaliser's accumulation, its decay and the division after the write."""
+    import json
+    with open(os.path.join(ROOT, "tests", "golden", "hand_linear_norm_2tok.json")) as f:
+        g = json.load(f)
+    inp = g["inputs"]
+    q, k, v = (np.array(inp[n], np.float32) for n in ("q", "k", "v"))
+    num = lambda x: float("-inf") if x == "-inf" else float(x)
+    la = np.array([[num(x) for x in row] for row in inp["log_alpha_channel"]], np.float32)
+    for case, log_alpha in (("no_decay", None), ("channel_decay", la)):
+        o, hT, zT = oracle.linear_norm(q, k, v, log_alpha)
+        np.testing.assert_allclose(o, g[case]["o"], rtol=0, atol=1e-6)
+        np.testing.assert_allclose(hT, g[case]["hT"], rtol=0, atol=1e-6)
+        np.testing.assert_allclose(zT, g[case]["zT"], rtol=0, atol=1e-6)
