@@ -38,6 +38,23 @@ def test_attn_res_matches_oracle(nb, rows, D, dtype):
     assert rel_err(h.float().cpu().numpy(), ref) <= tol
 
 
+def test_attn_res_bench_size_sampled_rows():
+    """The bench's case, 9 blocks x 4096 rows x 7168 (bf16), in the bench's
+    launch: more rows than the grid (16 CTAs per SM), so CTAs take a second
+    row (and prefetch it).  Checked on a seeded sample of rows, among them the
+    first rows past the grid."""
+    nb, rows, D = 9, 4096, 7168
+    V, w = _case(nb, rows, D, "bf16", seed=97)
+    h = kda.attn_res(torch.from_numpy(V).to(DEV).to(torch.bfloat16), torch.from_numpy(w).to(DEV))
+    torch.cuda.synchronize()
+    grid = torch.cuda.get_device_properties(0).multi_processor_count * 16
+    rng = np.random.default_rng(3)
+    sample = np.unique(np.concatenate([rng.choice(rows, 48, replace=False),
+                                       [0, grid - 1, grid, grid + 1, rows - 1]]))
+    ref = oracle.attn_res(V[:, sample], w)
+    assert rel_err(h.float().cpu().numpy()[sample], ref) <= 1e-2
+
+
 def test_attn_res_weights_follow_the_scores():
     """Block 3 of every row made dominant: h is (nearly) that block."""
     V, w = _case(6, 64, 256, "f32", seed=5)
