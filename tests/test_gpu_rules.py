@@ -54,8 +54,9 @@ def test_linear_attention_matches_oracle(alpha):
 
 
 def test_linear_attention_long_sequence():
-    """Many chunks: the state keeps growing without the delta correction."""
-    w = _prefill("lin_long", 4096, "channel", 0.0, seed=41, H=3)
+    """Many chunks: the state keeps growing without the delta correction; 512
+    chunk-heads, more than the prep's persistent grid, so CTAs take several."""
+    w = _prefill("lin_long", 4096, "channel", 0.0, seed=41, H=8)
     x = W.prefill_inputs(w)
     d = device_inputs(w, x)
     d["beta"] = None
@@ -100,6 +101,20 @@ def test_input_maps_match_oracle(maps):
     eo = rel_err(o.float().cpu().numpy().reshape(ro.shape), ro)
     eh = rel_err(hT.cpu().numpy().reshape(rh.shape), rh)
     assert eo <= TOL_BF16 and eh <= TOL_BF16, (eo, eh)
+
+
+def test_input_maps_many_chunks():
+    """Fused maps on the delta rule over 512 chunk-heads (more than the prep's
+    persistent grid): the general prep's multi-chunk path."""
+    maps = kda.KDA_MAP_QK_SILU_NORM | kda.KDA_MAP_BETA_SIGMOID
+    w = _prefill("maps_long", 4096, "channel", 0.0, seed=161, H=8)
+    x = _raw_projections(w, seed=162)
+    d = device_inputs(w, x)
+    o, hT = _run_rule(d, w.C, kda.KDA_RULE_DELTA, maps)
+    mq, mk, mb = oracle.input_maps(x["q"], x["k"], x["beta"])
+    ro, rh = oracle.recurrent_heads(mq, mk, x["v"], mb, x["log_alpha"], x["h0"])
+    assert rel_err(o.float().cpu().numpy().reshape(ro.shape), ro) <= TOL_BF16
+    assert rel_err(hT.cpu().numpy().reshape(rh.shape), rh) <= TOL_BF16
 
 
 def test_input_maps_with_linear_rule():
@@ -163,8 +178,9 @@ def test_normalised_linear_attention_edges(B, H, T):
 
 
 def test_normalised_linear_attention_long_sequence():
-    """Many chunks: the normaliser and the state grow together chunk by chunk."""
-    w, x, d = _norm_case("linn_long", 4096, "channel", seed=121, H=3)
+    """Many chunks: the normaliser and the state grow together chunk by chunk;
+    512 chunk-heads, so the prep's CTAs take several chunks each."""
+    w, x, d = _norm_case("linn_long", 4096, "channel", seed=121, H=8)
     o, _ = _run_rule(d, w.C, kda.KDA_RULE_LINEAR_NORM, kda.KDA_MAP_QK_ELU1, with_hT=False)
     ro = _norm_reference(x)
     assert rel_err(o.float().cpu().numpy().reshape(ro.shape), ro) <= TOL_BF16
