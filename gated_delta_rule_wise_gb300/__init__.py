@@ -193,9 +193,10 @@ KDA_MAP_QK_SILU_NORM, KDA_MAP_BETA_SIGMOID, KDA_MAP_QK_ELU1 = 1, 2, 4
 
 def kda_chunk_fwd_rule(q, k, v, beta, log_alpha, h0, o, hT, C, workspace, rule=KDA_RULE_DELTA,
                        maps=0, stream=None):
-    """``kda_chunk_fwd`` with an update rule (KDA_RULE_DELTA / KDA_RULE_LINEAR)
-    and input maps (KDA_MAP_* bits) applied on the fly; beta may be None for
-    the linear rule."""
+    """``kda_chunk_fwd`` with an update rule (KDA_RULE_DELTA, KDA_RULE_LINEAR,
+    KDA_RULE_LINEAR_NORM) and input maps (KDA_MAP_* bits) applied on the fly;
+    beta may be None for the linear rules, and KDA_RULE_LINEAR_NORM takes
+    h0 = hT = None (its state stays inside the call)."""
     B, H, T, dk = q.shape
     dv = v.shape[-1]
     st = load_library().kda_chunk_fwd_rule(
