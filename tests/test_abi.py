@@ -9,6 +9,7 @@ import ctypes
 import os
 import re
 import subprocess
+import sys
 
 import pytest
 
@@ -196,3 +197,26 @@ def test_rule_argument_checks_before_any_launch(lib):
     assert call(0, 4) == 1                      # the feature map belongs to the linear rules
     assert call(2, 4, h0=FAKE, hT=None) == 2    # the normalised rule starts from zero ...
     assert call(2, 4, h0=None, hT=FAKE) == 2    # ... and keeps its state (S, z) internal
+
+
+def test_ops_fail_loudly_without_the_library(monkeypatch):
+    """No fallback: with libkda.so absent every entry point raises."""
+    import gated_delta_rule_wise_gb300 as kda
+    monkeypatch.setattr(kda, "_lib", None)
+    monkeypatch.setattr(kda, "library_path", lambda: "/nonexistent/libkda.so")
+    with pytest.raises(RuntimeError, match="missing"):
+        kda.kda_chunk_fwd_workspace_size(1, 1, 64, 16, 16, 16, kda.KDA_F32, 2)
+    with pytest.raises(RuntimeError, match="missing"):
+        kda.load_library()
+
+
+def test_package_does_not_import_the_oracle():
+    """The library path and the oracle share nothing: importing and loading
+    the package leaves the oracle unimported."""
+    code = ("import sys, gated_delta_rule_wise_gb300 as kda; kda.load_library(); "
+            "print('oracle' in sys.modules, 'workloads' in sys.modules)")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    p = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True,
+                       timeout=300)
+    assert p.returncode == 0, p.stderr[-2000:]
+    assert p.stdout.split()[:2] == ["False", "False"], p.stdout
