@@ -280,12 +280,13 @@ def kda_chunk_fwd_kernel_names(B, H, T, dk, dv, C, dtype, alpha_mode, path=KDA_P
 
 # Source files behind each kernel (their hash tells whether a recorded ncu
 # measurement still describes the kernel that runs).
+_TC_HEADERS = ["kda_internal.cuh", "kda_ptx.cuh", "kda_umma.cuh"]
 KERNEL_SOURCES = {
-    "chunk_ffma_kernel": ["kda_chunk_ffma.cu"],
-    "decode_step_kernel": ["kda_decode.cu"],
-    "kda_prep_kernel": ["kda_chunk_tc.cu"],
-    "kda_scan_kernel": ["kda_chunk_tc.cu"],
-    "attn_res_kernel": ["kda_attnres.cu"],
+    "chunk_ffma_kernel": ["kda_chunk_ffma.cu", "kda_internal.cuh"],
+    "decode_step_kernel": ["kda_decode.cu", "kda_internal.cuh"],
+    "kda_prep_kernel": ["kda_chunk_tc.cu"] + _TC_HEADERS,
+    "kda_scan_kernel": ["kda_chunk_tc.cu"] + _TC_HEADERS,
+    "attn_res_kernel": ["kda_attnres.cu", "kda_internal.cuh"],
 }
 
 

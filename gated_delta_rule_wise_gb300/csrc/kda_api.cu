@@ -44,6 +44,31 @@ size_t workspace_bytes(int B, int H, int T, int dk, int dv, int C, kda_dtype dt,
 }
 
 }  // namespace
+
+kda_status validate_chunk_fwd(const void *q, const void *k, const void *v, const float *beta,
+                              const float *log_alpha, const float *h0, const void *o,
+                              const float *hT, int B, int H, int T, int dk, int dv, int C,
+                              kda_dtype dt, kda_alpha_mode am, const void *workspace,
+                              size_t ws_bytes, kda_path path) {
+  kda_status st = check_chunk_shape(B, H, T, dk, dv, C, dt, am, path);
+  if (st != KDA_OK) return st;
+  const bool has_tokens = (long long)B * H * T > 0;
+  if (has_tokens) {
+    if (!q || !k || !v || !beta || !o) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(beta) || !aligned16(o))
+      return KDA_ERR_INVALID_ARG;
+  }
+  if (am == KDA_ALPHA_NONE) {
+    if (log_alpha) return KDA_ERR_INVALID_ARG;
+  } else if (has_tokens && (!log_alpha || !aligned16(log_alpha))) {
+    return KDA_ERR_INVALID_ARG;
+  }
+  if ((h0 && !aligned16(h0)) || (hT && !aligned16(hT))) return KDA_ERR_INVALID_ARG;
+  if (!workspace || !aligned256(workspace)) return KDA_ERR_INVALID_ARG;
+  if (ws_bytes < workspace_bytes(B, H, T, dk, dv, C, dt, am, path)) return KDA_ERR_INVALID_ARG;
+  return KDA_OK;
+}
+
 }  // namespace kda
 
 using namespace kda;
@@ -95,27 +120,14 @@ kda_status kda_chunk_fwd_ex(const void *q, const void *k, const void *v, const f
                             kda_alpha_mode am, void *workspace, size_t ws_bytes,
                             kda_stream_t stream, kda_path path, void *const *events,
                             int n_events) {
-  kda_status st = check_chunk_shape(B, H, T, dk, dv, C, dt, am, path);
+  kda_status st = validate_chunk_fwd(q, k, v, beta, log_alpha, h0, o, hT, B, H, T, dk, dv, C, dt,
+                                     am, workspace, ws_bytes, path);
   if (st != KDA_OK) return st;
   if (n_events < 0 || (n_events > 0 && !events)) return KDA_ERR_INVALID_ARG;
   const bool tensor = use_tensor(dk, dv, C, dt, path);
   const int launches = tensor ? chunk_tc_launches(B * H, T, hT != nullptr)
                               : chunk_ffma_launches(B * H, T, hT != nullptr);
   if (n_events > 0 && n_events < launches + 1) return KDA_ERR_INVALID_ARG;
-  const bool has_tokens = (long long)B * H * T > 0;
-  if (has_tokens) {
-    if (!q || !k || !v || !beta || !o) return KDA_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(beta) || !aligned16(o))
-      return KDA_ERR_INVALID_ARG;
-  }
-  if (am == KDA_ALPHA_NONE) {
-    if (log_alpha) return KDA_ERR_INVALID_ARG;
-  } else if (has_tokens && (!log_alpha || !aligned16(log_alpha))) {
-    return KDA_ERR_INVALID_ARG;
-  }
-  if ((h0 && !aligned16(h0)) || (hT && !aligned16(hT))) return KDA_ERR_INVALID_ARG;
-  if (!workspace || !aligned256(workspace)) return KDA_ERR_INVALID_ARG;
-  if (ws_bytes < workspace_bytes(B, H, T, dk, dv, C, dt, am, path)) return KDA_ERR_INVALID_ARG;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   WorkspaceHeader *hdr = static_cast<WorkspaceHeader *>(workspace);

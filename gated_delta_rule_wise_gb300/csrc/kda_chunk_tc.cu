@@ -289,7 +289,13 @@ __device__ __forceinline__ void prep_d64(const __nv_bfloat16 *__restrict__ q,
 
   const int tid = threadIdx.x, warp = tid >> 5;
   const int c = tid % D, qtr = tid / D, r0 = qtr * R;
+  // every thread waits on the same barriers; the chunk's last barrier ORs
+  // the outcome of its waits so that the CTA leaves together after one gave up
   bool ok = true;
+  auto fail = [&](unsigned where) {
+    ok = false;
+    report_error(hdr, KDA_ERR_TIMEOUT, where);
+  };
 
   auto issue_raw = [&](int idx) {  // bulk copies of one chunk's q, k, v rows
     const int bh = idx / NC, t0 = (idx % NC) * kC;
@@ -364,10 +370,7 @@ __device__ __forceinline__ void prep_d64(const __nv_bfloat16 *__restrict__ q,
     for (int i = 0; i < R; ++i) psum += ld[i];
     part[qtr * D + c] = psum;
     if (tid == 0) ptx::bulk_wait_read_all();  // the previous record has left shared memory
-    if (ok && !ptx::mbar_wait(lbar, it & 1, kWaitLimit)) {
-      ok = false;
-      report_error(hdr, KDA_ERR_TIMEOUT, 0x100u);
-    }
+    if (ok && !ptx::mbar_wait(lbar, it & 1, kWaitLimit)) fail(0x100u);
     for (int idx2 = valid * D + tid; idx2 < kC * D; idx2 += 256) {  // zero the padded rows
       reinterpret_cast<__nv_bfloat16 *>(rawq)[idx2] = __float2bfloat16_rn(0.f);
       reinterpret_cast<__nv_bfloat16 *>(rawk)[idx2] = __float2bfloat16_rn(0.f);
@@ -426,10 +429,7 @@ __device__ __forceinline__ void prep_d64(const __nv_bfloat16 *__restrict__ q,
       ptx::mma_commit(bar);
     }
     if (has_next) load_la(idx_next, I_0{}, I_1{});
-    if (ok && !ptx::mbar_wait(bar, mma_phase & 1, kWaitLimit)) {
-      ok = false;
-      report_error(hdr, KDA_ERR_TIMEOUT, 0x101u);
-    }
+    if (ok && !ptx::mbar_wait(bar, mma_phase & 1, kWaitLimit)) fail(0x101u);
     ++mma_phase;
     ptx::tc_fence_after();
 
@@ -484,10 +484,7 @@ __device__ __forceinline__ void prep_d64(const __nv_bfloat16 *__restrict__ q,
       ptx::mma_commit(bar);
     }
     if (has_next) load_la(idx_next, I_1{}, I_2{});
-    if (ok && !ptx::mbar_wait(bar, mma_phase & 1, kWaitLimit)) {
-      ok = false;
-      report_error(hdr, KDA_ERR_TIMEOUT, 0x102u);
-    }
+    if (ok && !ptx::mbar_wait(bar, mma_phase & 1, kWaitLimit)) fail(0x102u);
     ++mma_phase;
     ptx::tc_fence_after();
 
@@ -528,10 +525,7 @@ __device__ __forceinline__ void prep_d64(const __nv_bfloat16 *__restrict__ q,
       ptx::mma_commit(bar);
     }
     if (has_next) load_la(idx_next, I_2{}, I_3{});
-    if (ok && !ptx::mbar_wait(bar, mma_phase & 1, kWaitLimit)) {
-      ok = false;
-      report_error(hdr, KDA_ERR_TIMEOUT, 0x103u);
-    }
+    if (ok && !ptx::mbar_wait(bar, mma_phase & 1, kWaitLimit)) fail(0x103u);
     ++mma_phase;
     ptx::tc_fence_after();
 
@@ -565,8 +559,17 @@ __device__ __forceinline__ void prep_d64(const __nv_bfloat16 *__restrict__ q,
     }
     ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
-    __syncthreads();
+    const int stop = __syncthreads_or(!ok);  // a wait of this CTA gave up
     ptx::tc_fence_after();
+    if (stop) {
+      // drain (bounded) what thread 0 started: the latest row copy, the products
+      if (tid == 0) {
+        ptx::mbar_wait(lbar, (it + (has_next ? 1 : 0)) & 1, kWaitLimit);
+        ptx::mma_commit(bar);
+        ptx::mbar_wait(bar, mma_phase & 1, kWaitLimit);
+      }
+      break;
+    }
 
     // ---- (9) record -> workspace (one bulk copy; its read is awaited before
     // the record region is written again)
@@ -705,7 +708,14 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, colhalf = warp >> 2;  // TMEM lane quarter, column half
   const int c = tid & (D - 1), half = tid >> 7, r0 = half * R;   // decay phase mapping
+  // Every thread waits on the same barriers, so a wait that gives up gives
+  // up in every thread; the chunk's last barrier ORs the outcome and the
+  // whole CTA leaves together (after draining what thread 0 started).
   bool ok = true;
+  auto fail = [&](unsigned where) {
+    ok = false;
+    report_error(hdr, KDA_ERR_TIMEOUT, where);
+  };
 
   const bool la_bulk = alpha_mode == KDA_ALPHA_CHANNEL;  // per-channel rows: 512 B each
   auto rows_of = [&](int idx, int &valid, size_t &row0) {
@@ -785,10 +795,7 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
   uint32_t mma_phase = 0;
 
   auto wait_mma = [&](unsigned code) {
-    if (ok && !ptx::mbar_wait(bar, mma_phase & 1, kWaitLimit)) {
-      ok = false;
-      report_error(hdr, KDA_ERR_TIMEOUT, code);
-    }
+    if (ok && !ptx::mbar_wait(bar, mma_phase & 1, kWaitLimit)) fail(code);
     ++mma_phase;
     ptx::tc_fence_after();
   };
@@ -811,10 +818,7 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
 
     // ---- (0) decay
     if (tid < kC) betas[tid] = b_next;
-    if (ok && !ptx::mbar_wait(lbar, it & 1, kWaitLimit)) {
-      ok = false;
-      report_error(hdr, KDA_ERR_TIMEOUT, 0x100u);
-    }
+    if (ok && !ptx::mbar_wait(lbar, it & 1, kWaitLimit)) fail(0x100u);
     float ld[R];
     if (la_bulk) {  // one straight run of shared loads
 #pragma unroll
@@ -851,10 +855,7 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
         reinterpret_cast<float *>(recg + Rr::GC)[c] = __expf(p0 + p1);
       }
     }
-    if (ok && !ptx::mbar_wait(qbar, it & 1, kWaitLimit)) {
-      ok = false;
-      report_error(hdr, KDA_ERR_TIMEOUT, 0x105u);
-    }
+    if (ok && !ptx::mbar_wait(qbar, it & 1, kWaitLimit)) fail(0x105u);
     __syncthreads();
 
     // ---- (1) decayed tiles, one thread per (row, 8 channels): raw rows to
@@ -1172,11 +1173,24 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
         }
       }
     }
-    // block 0 and the TMEM columns are free again: fetch the next chunk's q rows
+    // block 0 and the TMEM columns are free again: fetch the next chunk's q
+    // rows, unless a wait of this CTA gave up (then every thread leaves here)
     ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
-    __syncthreads();
+    const int stop = __syncthreads_or(!ok);
     ptx::tc_fence_after();
+    if (stop) {
+      // drain (bounded) what thread 0 started: the latest row copies (the
+      // next chunk's log_alpha, k, v if issued; this chunk's q), then the
+      // products, before shared memory and TMEM are released
+      if (tid == 0) {
+        ptx::mbar_wait(lbar, (it + (has_next ? 1 : 0)) & 1, kWaitLimit);
+        ptx::mbar_wait(qbar, it & 1, kWaitLimit);
+        ptx::mma_commit(bar);
+        ptx::mbar_wait(bar, mma_phase & 1, kWaitLimit);
+      }
+      break;
+    }
     if (tid == 0 && has_next) issue_q(idx_next);
   }
   ptx::tc_fence_before();
@@ -1249,6 +1263,7 @@ struct ScanSmem128 {
   // full[kStages], empty[kStages], mS, mO[kOutBufs], ofree[kOutBufs]
   static constexpr uint32_t BAR = SB + 2 * 128 * 64 * 2;
   static constexpr uint32_t TMEMP = BAR + (2 * kStages + 1 + 2 * kOutBufs) * 8;
+  static constexpr uint32_t ABORT = TMEMP + 4;               // CTA-wide abort word
   static constexpr uint32_t BYTES = TMEMP + 8;
   static constexpr uint32_t TMEM_COLS = 128;                 // P | o[0] | o[1] | o[2]
   static_assert(NB * (1 + kOutBufs) <= TMEM_COLS, "TMEM columns");
@@ -1262,9 +1277,12 @@ struct ScanSmem128 {
 // N = NB + 8, and its column NB is Qp z, to which the output warps add the
 // row sum of M for the denominator.  A separate instantiation, so that the
 // other rules' scan is compiled without it.
+// h0 and hT may be one buffer (in-place resume): each state thread reads its
+// own elements of h0 before the first chunk and writes the same elements of
+// hT after the last, so neither pointer is declared __restrict__.
 template <int NB, bool kNorm>
-__device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfloat16 *__restrict__ o,
-                                          float *__restrict__ hT, int T, int NC,
+__device__ __forceinline__ void scan_d128(const float *h0, __nv_bfloat16 *__restrict__ o,
+                                          float *hT, int T, int NC,
                                           uint8_t *__restrict__ ws, uint8_t *sm) {
   constexpr int D = 128;
   constexpr uint32_t kSyncThreads = 128 + 32;  // state warps + issuer warp
@@ -1280,6 +1298,7 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
   uint64_t *mO = mS + 1;
   uint64_t *ofree = mO + kOutBufs;
   uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(sm + L::TMEMP);
+  uint32_t *abort_f = reinterpret_cast<uint32_t *>(sm + L::ABORT);
   WorkspaceHeader *hdr = reinterpret_cast<WorkspaceHeader *>(ws);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1287,7 +1306,16 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
   const uint8_t *rec0 = ws + sizeof(WorkspaceHeader) + (size_t)bh * NC * R::BYTES;
   const uint8_t *nrm0 = ws + sizeof(WorkspaceHeader) + (size_t)gridDim.y * NC * R::BYTES +
                         (size_t)bh * NC * NormRec::BYTES;
+  // After a wait gives up, every role of the CTA stops waiting (the abort
+  // word), the producer stops copying and waits (bounded) for the copies it
+  // started, and the issuer for its products, before TMEM and shared memory
+  // are released.  The other roles run out their loops without waiting.
   bool ok = true;
+  auto fail = [&](unsigned where) {
+    ok = false;
+    ptx::set_abort(abort_f);
+    report_error(hdr, KDA_ERR_TIMEOUT, where);
+  };
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -1299,6 +1327,7 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
       ptx::mbar_init(&mO[b], 1);
       ptx::mbar_init(&ofree[b], 1);
     }
+    *abort_f = 0u;
     ptx::fence_mbar_init();
   }
   if (warp == 0) {
@@ -1315,12 +1344,13 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
   if (warp == 8) {
     // ---------------------------------------------------------- producer
     if (lane == 0) {
+      int issued = 0;
       for (int j = 0; j < NC; ++j) {
         const int s = j % kStages;
-        if (j >= kStages && ok && !ptx::mbar_wait_fast(&empty[s], ((j / kStages) - 1) & 1, kWaitLimit)) {
-          ok = false;
-          report_error(hdr, KDA_ERR_TIMEOUT, 0x210u);
-        }
+        if (j >= kStages && ok &&
+            !ptx::mbar_wait_fast(&empty[s], ((j / kStages) - 1) & 1, kWaitLimit, abort_f))
+          fail(0x210u);
+        if (!ok || ptx::aborted(abort_f)) break;
         uint8_t *st = sm + s * L::STAGE;
         const uint8_t *rec = rec0 + (size_t)j * R::BYTES;
         // a later record into L2 ahead of its copy, so that the copy meets L2
@@ -1342,7 +1372,11 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
         ptx::bulk_g2s(st + L::BI_S, rec + R::BI + (size_t)blk * (128 * NB * 2), 128 * NB * 2, &full[s]);
         ptx::bulk_g2s(st + L::OI_S, rec + R::OI + (size_t)blk * (kC * NB * 2), kC * NB * 2, &full[s]);
         ptx::bulk_g2s(st + L::GC_S, rec + R::GC, 128 * 4, &full[s]);
+        issued = j + 1;
       }
+      if (ptx::aborted(abort_f))  // drain (bounded): the copies still in flight
+        for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
+          if (!ptx::mbar_wait(&full[j % kStages], (j / kStages) & 1, kWaitLimit)) break;
     }
   } else if (warp == 9) {
     // ---------------------------------------------------------- issuer
@@ -1386,7 +1420,7 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
       }
       __syncwarp();
     }
-    if (lane == 0 && !ok) {  // after a timeout: let this thread's MMAs finish before TMEM is freed
+    if (lane == 0 && ptx::aborted(abort_f)) {  // let this thread's MMAs finish before TMEM is freed
       ptx::mma_commit(mS);
       ptx::mbar_wait(mS, NC & 1, kWaitLimit);
     }
@@ -1395,14 +1429,10 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
     const int orow = (warp - 4) * 16 + lane;  // output row (M = 64 layout: lanes 32w + 0..15)
     for (int j = 0; j < NC; ++j) {
       const int b = j % kOutBufs, s = j % kStages;
-      if (ok && !ptx::mbar_wait(&mO[b], (j / kOutBufs) & 1, kWaitLimit)) {
-        ok = false;
-        report_error(hdr, KDA_ERR_TIMEOUT, 0x221u);
-      }
-      if (ok && !ptx::mbar_wait_fast(&full[s], (j / kStages) & 1, kWaitLimit)) {
-        ok = false;  // already complete: orders the record's bulk copy before the reads below
-        report_error(hdr, KDA_ERR_TIMEOUT, 0x223u);
-      }
+      if (ok && !ptx::mbar_wait(&mO[b], (j / kOutBufs) & 1, kWaitLimit, abort_f)) fail(0x221u);
+      // already complete: orders the record's bulk copy before the reads below
+      if (ok && !ptx::mbar_wait_fast(&full[s], (j / kStages) & 1, kWaitLimit, abort_f))
+        fail(0x223u);
       ptx::tc_fence_after();
       const uint32_t tO = t_lane + NB + kOW * b;
       const uint8_t *oi = sm + s * L::STAGE + L::OI_S;
@@ -1476,16 +1506,13 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
       // gamma_C below anyway), accumulator (i mod 3) read by the output warps
       // (chunk i - 3); and stage i-1 released for the state side (its products
       // completed before P_{i-1} was read, its B was read before that)
-      if (ok && !ptx::mbar_wait_fast(&full[s], (i / kStages) & 1, kWaitLimit)) {
-        ok = false;
-        report_error(hdr, KDA_ERR_TIMEOUT, 0x204u);
-      }
+      if (ok && !ptx::mbar_wait_fast(&full[s], (i / kStages) & 1, kWaitLimit, abort_f))
+        fail(0x204u);
       if (r == 0) {
         if (i >= kOutBufs && ok &&
-            !ptx::mbar_wait_fast(&ofree[i % kOutBufs], ((i / kOutBufs) - 1) & 1, kWaitLimit)) {
-          ok = false;
-          report_error(hdr, KDA_ERR_TIMEOUT, 0x222u);
-        }
+            !ptx::mbar_wait_fast(&ofree[i % kOutBufs], ((i / kOutBufs) - 1) & 1, kWaitLimit,
+                                 abort_f))
+          fail(0x222u);
         if (i > 0) ptx::mbar_arrive(&empty[(i - 1) % kStages]);
       }
       __syncwarp();
@@ -1506,10 +1533,7 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
           }
         }
       }
-      if (ok && !ptx::mbar_wait(mS, i & 1, kWaitLimit)) {
-        ok = false;
-        report_error(hdr, KDA_ERR_TIMEOUT, 0x201u);
-      }
+      if (ok && !ptx::mbar_wait(mS, i & 1, kWaitLimit, abort_f)) fail(0x201u);
       ptx::tc_fence_after();
       {
         float x[NB];
@@ -1535,8 +1559,8 @@ __device__ __forceinline__ void scan_d128(const float *__restrict__ h0, __nv_bfl
 }
 
 template <int NB>
-__device__ __forceinline__ void scan_d64(const float *__restrict__ h0, __nv_bfloat16 *__restrict__ o,
-                                         float *__restrict__ hT, int T, int NC,
+__device__ __forceinline__ void scan_d64(const float *h0, __nv_bfloat16 *__restrict__ o,
+                                         float *hT, int T, int NC,
                                          uint8_t *__restrict__ ws, uint8_t *sm) {
   constexpr int D = 64;
   using B = Rec<64>;
@@ -1552,7 +1576,15 @@ __device__ __forceinline__ void scan_d64(const float *__restrict__ h0, __nv_bflo
   const int bh = blockIdx.y, j0 = blockIdx.x * NB;
   const int dv = D;
   const uint8_t *rec0 = ws + sizeof(WorkspaceHeader) + (size_t)bh * NC * B::BYTES;
+  // Every thread waits on the same barriers; the chunk's hand-off barrier
+  // ORs the outcome of the waits so that all leave together after one gave
+  // up, and thread 0 then drains its last record copy and its products.
   bool ok = true;
+  int loads_issued = 0, commits = 0;  // thread 0's record copies and MMA commits
+  auto fail = [&](unsigned where) {
+    ok = false;
+    report_error(hdr, KDA_ERR_TIMEOUT, where);
+  };
 
   if (tid == 0) {
     ptx::mbar_init(&full[0], 1);
@@ -1597,7 +1629,10 @@ __device__ __forceinline__ void scan_d64(const float *__restrict__ h0, __nv_bflo
     }
     ptx::tmem_st_wait();
   }
-  if (tid == 0 && NC > 0) issue_loads(0, 0);
+  if (tid == 0 && NC > 0) {
+    issue_loads(0, 0);
+    loads_issued = 1;
+  }
   ptx::tc_fence_before();
   ptx::named_barrier(1, 128);
 
@@ -1627,16 +1662,13 @@ __device__ __forceinline__ void scan_d64(const float *__restrict__ h0, __nv_bflo
   for (int i = 0; i < NC; ++i) {
     const int s = i & 1;
     uint8_t *st = sm + s * L::STAGE;
-    if (i > 0 && ok && !ptx::mbar_wait(mbar, (i - 1) & 1, kWaitLimit)) {
-      ok = false;
-      report_error(hdr, KDA_ERR_TIMEOUT, 0x201u);
-    }
+    if (i > 0 && ok && !ptx::mbar_wait(mbar, (i - 1) & 1, kWaitLimit)) fail(0x201u);
     ptx::tc_fence_after();
-    if (tid == 0 && i + 1 < NC) issue_loads(i + 1, (i + 1) & 1);
-    if (ok && !ptx::mbar_wait(&full[s], (i >> 1) & 1, kWaitLimit)) {
-      ok = false;
-      report_error(hdr, KDA_ERR_TIMEOUT, 0x202u);
+    if (tid == 0 && i + 1 < NC) {
+      issue_loads(i + 1, (i + 1) & 1);
+      loads_issued = i + 2;
     }
+    if (ok && !ptx::mbar_wait(&full[s], (i >> 1) & 1, kWaitLimit)) fail(0x202u);
     // state row: bf16 copy as the MMA operand, then scale by gamma_C in place
     if (state_row) {
       const float gam = reinterpret_cast<const float *>(st + B::PRE + NB * 128)[srow];
@@ -1664,7 +1696,7 @@ __device__ __forceinline__ void scan_d64(const float *__restrict__ h0, __nv_bflo
     ptx::tmem_st_wait();
     ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
-    ptx::named_barrier(1, 128);
+    if (ptx::named_barrier_or(1, 128, !ok)) break;  // a wait gave up
     if (tid == 0) {
       ptx::tc_fence_after();
       const uint32_t sAP = ptx::smem_u32(st + B::AP), sQP = ptx::smem_u32(st + B::QP);
@@ -1699,15 +1731,13 @@ __device__ __forceinline__ void scan_d64(const float *__restrict__ h0, __nv_bflo
                            umma::idesc_bf16(128, NB), 1);
       }
       ptx::mma_commit(mbar);
+      ++commits;
     }
   }
 
   // epilogue: last chunk's output, final state
   if (NC > 0) {
-    if (ok && !ptx::mbar_wait(mbar, (NC - 1) & 1, kWaitLimit)) {
-      ok = false;
-      report_error(hdr, KDA_ERR_TIMEOUT, 0x203u);
-    }
+    if (ok && !ptx::mbar_wait(mbar, (NC - 1) & 1, kWaitLimit)) fail(0x203u);
     ptx::tc_fence_after();
     store_o_rows(NC - 1);
   }
@@ -1726,6 +1756,14 @@ __device__ __forceinline__ void scan_d64(const float *__restrict__ h0, __nv_bflo
       }
     }
   }
+  if (tid == 0 && !ok) {  // drain (bounded): the last copy, the products
+    if (loads_issued > 0) {
+      const int j = loads_issued - 1;
+      ptx::mbar_wait(&full[j & 1], (j >> 1) & 1, kWaitLimit);
+    }
+    ptx::mma_commit(mbar);
+    ptx::mbar_wait(mbar, commits & 1, kWaitLimit);
+  }
   ptx::tc_fence_before();
   ptx::named_barrier(1, 128);
   if (warp == 0) {
@@ -1737,8 +1775,8 @@ __device__ __forceinline__ void scan_d64(const float *__restrict__ h0, __nv_bflo
 
 template <int D, int NB, bool kNorm>
 __global__ void __launch_bounds__(kScan128Threads, 1)
-kda_scan_kernel(const float *__restrict__ h0, __nv_bfloat16 *__restrict__ o,
-                float *__restrict__ hT, int T, int NC, uint8_t *__restrict__ ws) {
+kda_scan_kernel(const float *h0, __nv_bfloat16 *__restrict__ o, float *hT, int T, int NC,
+                uint8_t *__restrict__ ws) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));

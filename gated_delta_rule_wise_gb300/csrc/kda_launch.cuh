@@ -48,4 +48,12 @@ kda_status launch_chunk_tc(const void *q, const void *k, const void *v, const fl
                            LaunchTimer &timer, int rule = 0, unsigned maps = 0);
 kda_status launch_selftest_wait(WorkspaceHeader *hdr, unsigned spin_limit,
                                 cudaStream_t stream);
+// Every check kda_chunk_fwd_ex makes before it launches anything (shapes,
+// enums, pointers, alignment, workspace size); KDA_OK if a call with these
+// arguments would launch.
+kda_status validate_chunk_fwd(const void *q, const void *k, const void *v, const float *beta,
+                              const float *log_alpha, const float *h0, const void *o,
+                              const float *hT, int B, int H, int T, int dk, int dv, int C,
+                              kda_dtype dt, kda_alpha_mode am, const void *workspace,
+                              size_t ws_bytes, kda_path path);
 }  // namespace kda

@@ -51,6 +51,13 @@ extern "C" kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const 
     return kda_chunk_fwd(q, k, v, beta, log_alpha, h0, o, hT, B, H, T, dk, dv, C, dt, am,
                          reinterpret_cast<void *>(256), 0, stream);
   if (need > kNoallocScratchBytes) return KDA_ERR_UNSUPPORTED;
+  // every argument check of kda_chunk_fwd, made before anything is enqueued
+  // (the scratch address stands in for the workspace: its only requirement,
+  // 256-byte alignment, holds by declaration)
+  const kda_status valid =
+      kda::validate_chunk_fwd(q, k, v, beta, log_alpha, h0, o, hT, B, H, T, dk, dv, C, dt, am,
+                              reinterpret_cast<void *>(256), kNoallocScratchBytes, KDA_PATH_AUTO);
+  if (valid != KDA_OK) return valid;
   void *scratch = nullptr;
   const kda_status st = scratch_on_current_device(&scratch);
   if (st != KDA_OK) return st;

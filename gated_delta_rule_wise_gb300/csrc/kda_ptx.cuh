@@ -69,9 +69,45 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_wait_fast(uint64_t *bar, uint32_t parity, uint32_t limit) {
   return mbar_test(bar, parity) || mbar_wait(bar, parity, limit);
 }
+
+// CTA-wide abort: a word in shared memory that any thread of the CTA sets
+// when one of its waits gives up.  The waits below poll it every 256 tries,
+// so every other role of the CTA stops waiting soon after, instead of each
+// running out its own limit on work that will never arrive.
+__device__ __forceinline__ bool aborted(const uint32_t *flag) {
+  return *reinterpret_cast<const volatile uint32_t *>(flag) != 0u;
+}
+__device__ __forceinline__ void set_abort(uint32_t *flag) {
+  *reinterpret_cast<volatile uint32_t *>(flag) = 1u;
+}
+// Bounded wait that also gives up once `flag` is set.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t limit,
+                                          const uint32_t *flag) {
+  for (uint32_t i = 0; i < limit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 255u && aborted(flag)) return false;
+  }
+  return false;
+}
+__device__ __forceinline__ bool mbar_wait_fast(uint64_t *bar, uint32_t parity, uint32_t limit,
+                                               const uint32_t *flag) {
+  return mbar_test(bar, parity) || mbar_wait(bar, parity, limit, flag);
+}
 // Barrier among `count` threads (a multiple of 32) under id `id` (1..15).
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// Named barrier that also ORs a predicate over its `count` threads: every
+// participant gets true if any of them passed true.
+__device__ __forceinline__ bool named_barrier_or(uint32_t id, uint32_t count, bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred ps, pd;\n\tsetp.ne.u32 ps, %1, 0;\n\t"
+      "bar.red.or.pred pd, %2, %3, ps;\n\tselp.u32 %0, 1, 0, pd;\n\t}"
+      : "=r"(out)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return out != 0;
 }
 // Arrive at named barrier `id` without waiting (producer side of a barrier
 // whose consumers call named_barrier with the same id and count).

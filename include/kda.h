@@ -117,6 +117,13 @@ size_t kda_chunk_fwd_workspace_size_ex(int B, int H, int T, int dk, int dv, int 
  *   dk, dv in {16, 32, 64, 128}; C in {16, 32, 64} (chunk length);
  *   workspace: >= kda_chunk_fwd_workspace_size(...) bytes of device memory,
  *   256-byte aligned, owned by the caller, not shared with a concurrent call.
+ *   Its first 256 bytes are the device error word: they must be zero before
+ *   the first call that uses the workspace (cudaMemset them once after
+ *   allocating it); the library never clears them itself except through
+ *   kda_chunk_fwd_status, which reads and clears them.  A workspace whose
+ *   first bytes hold leftover data makes the next kda_chunk_fwd_status
+ *   report an error that no call made (and clear it); the rest of the
+ *   workspace needs no initialisation.
  *
  * No scaling is applied to q.k (the caller normalises q and k).  o_t includes
  * token t's own write.  Precision: the CUDA-core path computes in float32;
@@ -284,7 +291,9 @@ kda_status kda_attn_res(const void *V, int n_blocks, const float *w, void *h,
  *                                  kda_chunk_fwd_host_buffer_size(...) bytes,
  *                                  owned by the caller; it holds the shared
  *                                  workspace (its start: read device errors
- *                                  with kda_chunk_fwd_status(dev_buffer, ...))
+ *                                  with kda_chunk_fwd_status(dev_buffer, ...);
+ *                                  its first 256 bytes must be zero before
+ *                                  the first call, as for kda_chunk_fwd)
  *                                  (segments: also the carried state) and two
  *                                  staging slots of one pipeline step
  *

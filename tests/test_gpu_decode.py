@@ -12,6 +12,7 @@ import gated_delta_rule_wise_gb300 as kda
 import oracle
 import workloads as W
 from _gpu_helpers import DEV, put, rel_err, tdtype, tol_for
+from _margins import record
 
 pytestmark = pytest.mark.gpu
 
@@ -41,8 +42,10 @@ def test_decode_shapes(dk, dv, alpha, dtype):
         S_ref = S_ref.reshape(S0.shape)
         torch.cuda.synchronize()
         tol = tol_for(dtype)
-        assert rel_err(o.float().cpu().numpy().reshape(o_ref.shape), o_ref) <= tol
-        assert rel_err(S.cpu().numpy(), S_ref) <= tol
+        case = f"decode N=5 H=3 dk={dk} dv={dv} {dtype} {alpha}"
+        eo = record(case, "o", rel_err(o.float().cpu().numpy().reshape(o_ref.shape), o_ref), tol)
+        es = record(case, "S", rel_err(S.cpu().numpy(), S_ref), tol)
+        assert eo <= tol and es <= tol, (step, eo, es)
 
 
 def test_decode_full_workload_1000_steps_sampled_states():
@@ -75,6 +78,10 @@ def test_decode_full_workload_1000_steps_sampled_states():
             o_ref_last.append(o_ref)
     Sg = np.stack([S[n, h].cpu().numpy() for n, h in states])
     tol = tol_for(w.dtype)
-    assert rel_err(Sg, Sref[:, 0]) <= tol
+    case = f"{w.name} N={w.N} H={w.H} d={w.dk}, {w.steps} steps, 64 sampled states"
+    es = record(case, "S", rel_err(Sg, Sref[:, 0]), tol)
+    assert es <= tol, es
     for og, orf in zip(o_last, o_ref_last):
-        assert rel_err(np.stack([og[n, h].float().cpu().numpy() for n, h in states]), orf) <= tol
+        got = np.stack([og[n, h].float().cpu().numpy() for n, h in states])
+        eo = record(case, "o (last 3 steps)", rel_err(got, orf), tol)
+        assert eo <= tol, eo

@@ -14,6 +14,7 @@ import gated_delta_rule_wise_gb300 as kda
 import oracle
 import workloads as W
 from _gpu_helpers import DEV, device_inputs, rel_err, tdtype, tol_for
+from _margins import case_name, record
 
 pytestmark = pytest.mark.gpu
 
@@ -86,8 +87,11 @@ def test_host_api_against_oracle(group_heads):
     x = W.prefill_inputs(w)
     o, hT = _run_host(w, _host_inputs(w, x), group_heads)
     ro, rh = oracle.recurrent_heads(x["q"], x["k"], x["v"], x["beta"], x["log_alpha"], x["h0"])
-    assert rel_err(o.float().numpy().reshape(ro.shape), ro) <= tol_for(w.dtype)
-    assert rel_err(hT.numpy().reshape(rh.shape), rh) <= tol_for(w.dtype)
+    tol = tol_for(w.dtype)
+    case = case_name(w, f"host memory, group_heads={group_heads}")
+    eo = record(case, "o", rel_err(o.float().numpy().reshape(ro.shape), ro), tol)
+    eh = record(case, "hT", rel_err(hT.numpy().reshape(rh.shape), rh), tol)
+    assert eo <= tol and eh <= tol, (eo, eh)
 
 
 @pytest.mark.parametrize("group_heads", [0, 2])

@@ -18,6 +18,7 @@ import gated_delta_rule_wise_gb300 as kda
 import oracle
 import workloads as W
 from _gpu_helpers import DEV, TOL_BF16, device_inputs, put, rel_err
+from _margins import case_name, record
 
 pytestmark = pytest.mark.gpu
 
@@ -35,6 +36,11 @@ def _run_rule(d, C, rule, maps, with_hT=True):
     return o, hT
 
 
+def _err(w, qty, got, ref):
+    """rel_err of got against the oracle's ref, recorded as a parity margin."""
+    return record(case_name(w), qty, rel_err(got, ref), TOL_BF16)
+
+
 def _prefill(name, T, alpha, h0_sd, seed, H=2, B=1):
     return W.Prefill(name, B=B, H=H, T=T, dk=128, dv=128, C=64, dtype="bf16", alpha=alpha,
                      la_mu=-3.5, h0_sd=h0_sd, seed=seed)
@@ -48,8 +54,8 @@ def test_linear_attention_matches_oracle(alpha):
     d["beta"] = None
     o, hT = _run_rule(d, w.C, kda.KDA_RULE_LINEAR, 0)
     ro, rh = oracle.linear_heads(x["q"], x["k"], x["v"], x["log_alpha"], x["h0"])
-    eo = rel_err(o.float().cpu().numpy().reshape(ro.shape), ro)
-    eh = rel_err(hT.cpu().numpy().reshape(rh.shape), rh)
+    eo = _err(w, "o", o.float().cpu().numpy().reshape(ro.shape), ro)
+    eh = _err(w, "hT", hT.cpu().numpy().reshape(rh.shape), rh)
     assert eo <= TOL_BF16 and eh <= TOL_BF16, (eo, eh)
 
 
@@ -62,8 +68,8 @@ def test_linear_attention_long_sequence():
     d["beta"] = None
     o, hT = _run_rule(d, w.C, kda.KDA_RULE_LINEAR, 0)
     ro, rh = oracle.linear_heads(x["q"], x["k"], x["v"], x["log_alpha"], x["h0"])
-    assert rel_err(o.float().cpu().numpy().reshape(ro.shape), ro) <= TOL_BF16
-    assert rel_err(hT.cpu().numpy().reshape(rh.shape), rh) <= TOL_BF16
+    assert _err(w, "o", o.float().cpu().numpy().reshape(ro.shape), ro) <= TOL_BF16
+    assert _err(w, "hT", hT.cpu().numpy().reshape(rh.shape), rh) <= TOL_BF16
 
 
 def _raw_projections(w, seed, raw_qk=True):
@@ -98,8 +104,8 @@ def test_input_maps_match_oracle(maps):
     k = mk if mk is not None else k
     b = mb if mb is not None else b
     ro, rh = oracle.recurrent_heads(q, k, x["v"], b, x["log_alpha"], x["h0"])
-    eo = rel_err(o.float().cpu().numpy().reshape(ro.shape), ro)
-    eh = rel_err(hT.cpu().numpy().reshape(rh.shape), rh)
+    eo = _err(w, "o", o.float().cpu().numpy().reshape(ro.shape), ro)
+    eh = _err(w, "hT", hT.cpu().numpy().reshape(rh.shape), rh)
     assert eo <= TOL_BF16 and eh <= TOL_BF16, (eo, eh)
 
 
@@ -113,8 +119,8 @@ def test_input_maps_many_chunks():
     o, hT = _run_rule(d, w.C, kda.KDA_RULE_DELTA, maps)
     mq, mk, mb = oracle.input_maps(x["q"], x["k"], x["beta"])
     ro, rh = oracle.recurrent_heads(mq, mk, x["v"], mb, x["log_alpha"], x["h0"])
-    assert rel_err(o.float().cpu().numpy().reshape(ro.shape), ro) <= TOL_BF16
-    assert rel_err(hT.cpu().numpy().reshape(rh.shape), rh) <= TOL_BF16
+    assert _err(w, "o", o.float().cpu().numpy().reshape(ro.shape), ro) <= TOL_BF16
+    assert _err(w, "hT", hT.cpu().numpy().reshape(rh.shape), rh) <= TOL_BF16
 
 
 def test_input_maps_with_linear_rule():
@@ -125,8 +131,8 @@ def test_input_maps_with_linear_rule():
     o, hT = _run_rule(d, w.C, kda.KDA_RULE_LINEAR, kda.KDA_MAP_QK_SILU_NORM)
     mq, mk, _ = oracle.input_maps(x["q"], x["k"], None)
     ro, rh = oracle.linear_heads(mq, mk, x["v"], x["log_alpha"], x["h0"])
-    assert rel_err(o.float().cpu().numpy().reshape(ro.shape), ro) <= TOL_BF16
-    assert rel_err(hT.cpu().numpy().reshape(rh.shape), rh) <= TOL_BF16
+    assert _err(w, "o", o.float().cpu().numpy().reshape(ro.shape), ro) <= TOL_BF16
+    assert _err(w, "hT", hT.cpu().numpy().reshape(rh.shape), rh) <= TOL_BF16
 
 
 def _norm_case(name, T, alpha, seed, H=2):
@@ -154,7 +160,7 @@ def test_normalised_linear_attention_matches_oracle(alpha):
     w, x, d = _norm_case("linn", 3 * 64 + 33, alpha, seed=101 + len(alpha))
     o, _ = _run_rule(d, w.C, kda.KDA_RULE_LINEAR_NORM, kda.KDA_MAP_QK_ELU1, with_hT=False)
     ro = _norm_reference(x)
-    eo = rel_err(o.float().cpu().numpy().reshape(ro.shape), ro)
+    eo = _err(w, "o", o.float().cpu().numpy().reshape(ro.shape), ro)
     assert eo <= TOL_BF16, eo
 
 
@@ -173,7 +179,7 @@ def test_normalised_linear_attention_edges(B, H, T):
     d["h0"] = None
     o, _ = _run_rule(d, w.C, kda.KDA_RULE_LINEAR_NORM, kda.KDA_MAP_QK_ELU1, with_hT=False)
     ro = _norm_reference(x)
-    eo = rel_err(o.float().cpu().numpy().reshape(ro.shape), ro)
+    eo = _err(w, "o", o.float().cpu().numpy().reshape(ro.shape), ro)
     assert eo <= TOL_BF16, eo
 
 
@@ -183,7 +189,7 @@ def test_normalised_linear_attention_long_sequence():
     w, x, d = _norm_case("linn_long", 4096, "channel", seed=121, H=8)
     o, _ = _run_rule(d, w.C, kda.KDA_RULE_LINEAR_NORM, kda.KDA_MAP_QK_ELU1, with_hT=False)
     ro = _norm_reference(x)
-    assert rel_err(o.float().cpu().numpy().reshape(ro.shape), ro) <= TOL_BF16
+    assert _err(w, "o", o.float().cpu().numpy().reshape(ro.shape), ro) <= TOL_BF16
 
 
 def test_normalised_linear_attention_constant_values():
