@@ -430,6 +430,9 @@ def time_prefill_config(kda, torch, w, dev, stream, steps, warmup, peaks, peak_s
     scratch = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev) if flush else None
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_launch + 1)]
           for _ in range(steps)]
+    for row in ev:           # create the CUDA events (torch creates them on first record)
+        for e in row:
+            e.record(stream)
 
     def call(events=None):
         kda.kda_chunk_fwd_ex(d["q"], d["k"], d["v"], d["beta"], d["log_alpha"], d["h0"], o, hT,

@@ -1306,16 +1306,15 @@ __device__ __forceinline__ void scan_d128(const float *h0, __nv_bfloat16 *__rest
   const uint8_t *rec0 = ws + sizeof(WorkspaceHeader) + (size_t)bh * NC * R::BYTES;
   const uint8_t *nrm0 = ws + sizeof(WorkspaceHeader) + (size_t)gridDim.y * NC * R::BYTES +
                         (size_t)bh * NC * NormRec::BYTES;
-  // After a wait gives up, every role of the CTA stops waiting (the abort
-  // word), the producer stops copying and waits (bounded) for the copies it
-  // started, and the issuer for its products, before TMEM and shared memory
-  // are released.  The other roles run out their loops without waiting.
+  // A wait that gives up records the error, sets the CTA's abort word and
+  // makes its thread skip its later waits.  The producer then stops copying
+  // and waits (bounded) for the copies it started; the issuer, which waits
+  // on nothing but the state warps' named barrier, reads the abort word at
+  // the end and waits (bounded) for its products before TMEM is released.
+  // The other roles run out their loops, each giving up at most one wait of
+  // its own: the waits on the serial path stay plain (polling the abort word
+  // there cost the scan about 4 %).
   bool ok = true;
-  auto fail = [&](unsigned where) {
-    ok = false;
-    ptx::set_abort(abort_f);
-    report_error(hdr, KDA_ERR_TIMEOUT, where);
-  };
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -1344,13 +1343,15 @@ __device__ __forceinline__ void scan_d128(const float *h0, __nv_bfloat16 *__rest
   if (warp == 8) {
     // ---------------------------------------------------------- producer
     if (lane == 0) {
-      int issued = 0;
-      for (int j = 0; j < NC; ++j) {
+      int j = 0;
+      for (; j < NC; ++j) {
         const int s = j % kStages;
-        if (j >= kStages && ok &&
-            !ptx::mbar_wait_fast(&empty[s], ((j / kStages) - 1) & 1, kWaitLimit, abort_f))
-          fail(0x210u);
-        if (!ok || ptx::aborted(abort_f)) break;
+        if (j >= kStages && ok && !ptx::mbar_wait_fast(&empty[s], ((j / kStages) - 1) & 1, kWaitLimit)) {
+          ok = false;
+          ptx::set_abort(abort_f);
+          report_error(hdr, KDA_ERR_TIMEOUT, 0x210u);
+        }
+        if (!ok) break;
         uint8_t *st = sm + s * L::STAGE;
         const uint8_t *rec = rec0 + (size_t)j * R::BYTES;
         // a later record into L2 ahead of its copy, so that the copy meets L2
@@ -1372,11 +1373,10 @@ __device__ __forceinline__ void scan_d128(const float *h0, __nv_bfloat16 *__rest
         ptx::bulk_g2s(st + L::BI_S, rec + R::BI + (size_t)blk * (128 * NB * 2), 128 * NB * 2, &full[s]);
         ptx::bulk_g2s(st + L::OI_S, rec + R::OI + (size_t)blk * (kC * NB * 2), kC * NB * 2, &full[s]);
         ptx::bulk_g2s(st + L::GC_S, rec + R::GC, 128 * 4, &full[s]);
-        issued = j + 1;
       }
-      if (ptx::aborted(abort_f))  // drain (bounded): the copies still in flight
-        for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
-          if (!ptx::mbar_wait(&full[j % kStages], (j / kStages) & 1, kWaitLimit)) break;
+      if (!ok)  // drain (bounded): the copies still in flight (j were issued)
+        for (int i = j > kStages ? j - kStages : 0; i < j; ++i)
+          if (!ptx::mbar_wait(&full[i % kStages], (i / kStages) & 1, kWaitLimit)) break;
     }
   } else if (warp == 9) {
     // ---------------------------------------------------------- issuer
@@ -1429,10 +1429,16 @@ __device__ __forceinline__ void scan_d128(const float *h0, __nv_bfloat16 *__rest
     const int orow = (warp - 4) * 16 + lane;  // output row (M = 64 layout: lanes 32w + 0..15)
     for (int j = 0; j < NC; ++j) {
       const int b = j % kOutBufs, s = j % kStages;
-      if (ok && !ptx::mbar_wait(&mO[b], (j / kOutBufs) & 1, kWaitLimit, abort_f)) fail(0x221u);
-      // already complete: orders the record's bulk copy before the reads below
-      if (ok && !ptx::mbar_wait_fast(&full[s], (j / kStages) & 1, kWaitLimit, abort_f))
-        fail(0x223u);
+      if (ok && !ptx::mbar_wait(&mO[b], (j / kOutBufs) & 1, kWaitLimit)) {
+        ok = false;
+        ptx::set_abort(abort_f);
+        report_error(hdr, KDA_ERR_TIMEOUT, 0x221u);
+      }
+      if (ok && !ptx::mbar_wait_fast(&full[s], (j / kStages) & 1, kWaitLimit)) {
+        ok = false;  // already complete: orders the record's bulk copy before the reads below
+        ptx::set_abort(abort_f);
+        report_error(hdr, KDA_ERR_TIMEOUT, 0x223u);
+      }
       ptx::tc_fence_after();
       const uint32_t tO = t_lane + NB + kOW * b;
       const uint8_t *oi = sm + s * L::STAGE + L::OI_S;
@@ -1506,13 +1512,18 @@ __device__ __forceinline__ void scan_d128(const float *h0, __nv_bfloat16 *__rest
       // gamma_C below anyway), accumulator (i mod 3) read by the output warps
       // (chunk i - 3); and stage i-1 released for the state side (its products
       // completed before P_{i-1} was read, its B was read before that)
-      if (ok && !ptx::mbar_wait_fast(&full[s], (i / kStages) & 1, kWaitLimit, abort_f))
-        fail(0x204u);
+      if (ok && !ptx::mbar_wait_fast(&full[s], (i / kStages) & 1, kWaitLimit)) {
+        ok = false;
+        ptx::set_abort(abort_f);
+        report_error(hdr, KDA_ERR_TIMEOUT, 0x204u);
+      }
       if (r == 0) {
         if (i >= kOutBufs && ok &&
-            !ptx::mbar_wait_fast(&ofree[i % kOutBufs], ((i / kOutBufs) - 1) & 1, kWaitLimit,
-                                 abort_f))
-          fail(0x222u);
+            !ptx::mbar_wait_fast(&ofree[i % kOutBufs], ((i / kOutBufs) - 1) & 1, kWaitLimit)) {
+          ok = false;
+          ptx::set_abort(abort_f);
+          report_error(hdr, KDA_ERR_TIMEOUT, 0x222u);
+        }
         if (i > 0) ptx::mbar_arrive(&empty[(i - 1) % kStages]);
       }
       __syncwarp();
@@ -1533,7 +1544,11 @@ __device__ __forceinline__ void scan_d128(const float *h0, __nv_bfloat16 *__rest
           }
         }
       }
-      if (ok && !ptx::mbar_wait(mS, i & 1, kWaitLimit, abort_f)) fail(0x201u);
+      if (ok && !ptx::mbar_wait(mS, i & 1, kWaitLimit)) {
+        ok = false;
+        ptx::set_abort(abort_f);
+        report_error(hdr, KDA_ERR_TIMEOUT, 0x201u);
+      }
       ptx::tc_fence_after();
       {
         float x[NB];

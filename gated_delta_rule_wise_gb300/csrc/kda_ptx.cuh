@@ -70,28 +70,14 @@ __device__ __forceinline__ bool mbar_wait_fast(uint64_t *bar, uint32_t parity, u
   return mbar_test(bar, parity) || mbar_wait(bar, parity, limit);
 }
 
-// CTA-wide abort: a word in shared memory that any thread of the CTA sets
-// when one of its waits gives up.  The waits below poll it every 256 tries,
-// so every other role of the CTA stops waiting soon after, instead of each
-// running out its own limit on work that will never arrive.
+// CTA-wide abort word: a word in shared memory that a thread of the CTA sets
+// when one of its waits gives up, read by roles that must clean up after it
+// (stop issuing copies, wait for their products before TMEM is released).
 __device__ __forceinline__ bool aborted(const uint32_t *flag) {
   return *reinterpret_cast<const volatile uint32_t *>(flag) != 0u;
 }
 __device__ __forceinline__ void set_abort(uint32_t *flag) {
   *reinterpret_cast<volatile uint32_t *>(flag) = 1u;
-}
-// Bounded wait that also gives up once `flag` is set.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t limit,
-                                          const uint32_t *flag) {
-  for (uint32_t i = 0; i < limit; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 255u && aborted(flag)) return false;
-  }
-  return false;
-}
-__device__ __forceinline__ bool mbar_wait_fast(uint64_t *bar, uint32_t parity, uint32_t limit,
-                                               const uint32_t *flag) {
-  return mbar_test(bar, parity) || mbar_wait(bar, parity, limit, flag);
 }
 // Barrier among `count` threads (a multiple of 32) under id `id` (1..15).
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
