@@ -29,7 +29,8 @@ __all__ = [
     "KDA_MAP_QK_SILU_NORM", "KDA_MAP_BETA_SIGMOID", "KDA_MAP_QK_ELU1", "kda_attn_res", "attn_res",
     "chunk_fwd", "decode_step", "workspace_for",
     "KDA_F32", "KDA_BF16", "KDA_ALPHA_NONE", "KDA_ALPHA_SCALAR", "KDA_ALPHA_CHANNEL",
-    "KDA_PATH_AUTO", "KDA_PATH_CUDA_CORE", "KDA_PATH_TENSOR",
+    "KDA_PATH_AUTO", "KDA_PATH_CUDA_CORE", "KDA_PATH_TENSOR", "KDA_PATH_TENSOR_SPLIT_SCAN",
+    "KDA_PATH_TENSOR_WIDE_SCAN",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -38,6 +39,7 @@ KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT 
 KDA_F32, KDA_BF16 = 0, 1
 KDA_ALPHA_NONE, KDA_ALPHA_SCALAR, KDA_ALPHA_CHANNEL = 0, 1, 2
 KDA_PATH_AUTO, KDA_PATH_CUDA_CORE, KDA_PATH_TENSOR = 0, 1, 2
+KDA_PATH_TENSOR_SPLIT_SCAN, KDA_PATH_TENSOR_WIDE_SCAN = 3, 4
 ABI_VERSION = 1
 
 _lib = None
@@ -286,6 +288,7 @@ KERNEL_SOURCES = {
     "decode_step_kernel": ["kda_decode.cu", "kda_internal.cuh"],
     "kda_prep_kernel": ["kda_chunk_tc.cu"] + _TC_HEADERS,
     "kda_scan_kernel": ["kda_chunk_tc.cu"] + _TC_HEADERS,
+    "kda_scan_wide_kernel": ["kda_chunk_tc.cu"] + _TC_HEADERS,
     "attn_res_kernel": ["kda_attnres.cu", "kda_internal.cuh"],
 }
 

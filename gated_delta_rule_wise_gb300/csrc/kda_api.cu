@@ -21,18 +21,27 @@ kda_status check_chunk_shape(int B, int H, int T, int dk, int dv, int C, kda_dty
                              kda_alpha_mode am, kda_path path) {
   if (B < 0 || H < 0 || T < 0) return KDA_ERR_INVALID_ARG;
   if (!valid_dtype(dt) || !valid_alpha(am)) return KDA_ERR_INVALID_ARG;
-  if (path != KDA_PATH_AUTO && path != KDA_PATH_CUDA_CORE && path != KDA_PATH_TENSOR)
+  if (path != KDA_PATH_AUTO && path != KDA_PATH_CUDA_CORE && path != KDA_PATH_TENSOR &&
+      path != KDA_PATH_TENSOR_SPLIT_SCAN && path != KDA_PATH_TENSOR_WIDE_SCAN)
     return KDA_ERR_INVALID_ARG;
   if (!is_pow2_dim(dk) || !is_pow2_dim(dv)) return KDA_ERR_UNSUPPORTED;
   if (C != 16 && C != 32 && C != 64) return KDA_ERR_UNSUPPORTED;
   if ((long long)B * H > 65535) return KDA_ERR_UNSUPPORTED;
-  if (path == KDA_PATH_TENSOR && !chunk_tc_supported(dk, dv, C, dt)) return KDA_ERR_UNSUPPORTED;
+  const bool tensor_only = path == KDA_PATH_TENSOR || path == KDA_PATH_TENSOR_SPLIT_SCAN ||
+                           path == KDA_PATH_TENSOR_WIDE_SCAN;
+  if (tensor_only && !chunk_tc_supported(dk, dv, C, dt)) return KDA_ERR_UNSUPPORTED;
+  if (path == KDA_PATH_TENSOR_WIDE_SCAN && dk != 128) return KDA_ERR_UNSUPPORTED;
   return KDA_OK;
 }
 
 bool use_tensor(int dk, int dv, int C, kda_dtype dt, kda_path path) {
   if (path == KDA_PATH_CUDA_CORE) return false;
   return chunk_tc_supported(dk, dv, C, dt);
+}
+
+// Scan choice handed to the tensor path: 0 automatic, 1 split, 2 wide.
+int scan_choice(kda_path path) {
+  return path == KDA_PATH_TENSOR_SPLIT_SCAN ? 1 : (path == KDA_PATH_TENSOR_WIDE_SCAN ? 2 : 0);
 }
 
 size_t workspace_bytes(int B, int H, int T, int dk, int dv, int C, kda_dtype dt,
@@ -111,7 +120,8 @@ const char *kda_chunk_fwd_kernel_name(int B, int H, int T, int dk, int dv, int C
                                       kda_alpha_mode am, kda_path path, int i) {
   if (check_chunk_shape(B, H, T, dk, dv, C, dt, am, path) != KDA_OK) return nullptr;
   if (i < 0 || i >= kda_chunk_fwd_launches(B, H, T, dk, dv, C, dt, am, path)) return nullptr;
-  return use_tensor(dk, dv, C, dt, path) ? chunk_tc_kernel_name(T, i) : chunk_ffma_kernel_name(i);
+  return use_tensor(dk, dv, C, dt, path) ? chunk_tc_kernel_name(B * H, T, dk, scan_choice(path), i)
+                                         : chunk_ffma_kernel_name(i);
 }
 
 kda_status kda_chunk_fwd_ex(const void *q, const void *k, const void *v, const float *beta,
@@ -138,7 +148,7 @@ kda_status kda_chunk_fwd_ex(const void *q, const void *k, const void *v, const f
   timer.s = s;
   if (tensor)
     return launch_chunk_tc(q, k, v, beta, log_alpha, h0, o, hT, B, H, T, dk, dv, C, am,
-                           workspace, ws_bytes, s, timer);
+                           workspace, ws_bytes, s, timer, 0, 0u, scan_choice(path));
   return launch_chunk_ffma(q, k, v, beta, log_alpha, h0, o, hT, B, H, T, dk, dv, C, dt, am,
                            hdr, s, timer);
 }

@@ -1788,6 +1788,309 @@ __device__ __forceinline__ void scan_d64(const float *h0, __nv_bfloat16 *__restr
 }
 
 
+// D = 128, one CTA per (batch, head) holding all 128 value columns ("wide"
+// scan).  The value-column split above gives a head four CTAs, each issuing
+// the same sixteen MMAs per chunk on a 32-column slice; when heads outnumber
+// a quarter of the SMs those CTAs run in several rounds, and one CTA per head
+// that issues the sixteen MMAs on N = 128 takes one round.  Roles:
+//  - eight state warps: warp w owns key rows 32 (w mod 4) .. +31 (its TMEM
+//    lane quarter) and value columns 64 (w / 4) .. +63, each thread one row
+//    of 64 columns in registers as float;
+//  - two output warps, each thread one token row x 128 columns (the output
+//    product is issued with M = 128: the 64 rows past the chunk's read the
+//    bytes that follow the Qp tile and land in TMEM lanes 64-127, which
+//    nothing reads; so two lane quarters hold the rows and two warps suffice);
+//  - a producer warp streaming the MMA operands Ap | Qp through a 3-stage
+//    ring with gamma_C beside them, and prefetching whole records into L2
+//    three chunks ahead;
+//  - an issuer warp: P = Ap S (8 MMAs, M = 128, N = 128), then o = Qp S
+//    (8 MMAs, M = 128 as above, N = 128) into one of two output accumulators.
+// The additive terms B = Kbar^T U (state warps) and O = M U (output warps)
+// are not staged: each thread loads its 128-byte slice from L2 at the start
+// of the chunk that adds it (the state warps before they hand S over, the
+// output warps before they wait for the product), which keeps the ring, the
+// two bf16 copies of S and 512 TMEM columns inside one SM.
+constexpr int kWStages = 3;
+constexpr int kWOutBufs = 2;
+constexpr int kWideThreads = 384;  // 8 state warps, 2 output warps, producer, issuer
+struct ScanWideSmem {
+  using R = Rec<128>;
+  static constexpr uint32_t STAGE = R::PRE;                    // Ap | Qp (48 KB)
+  static_assert((STAGE & 1023u) == 0, "stage alignment");
+  static constexpr uint32_t SB = kWStages * STAGE;             // 2 x bf16 S [128 keys][128 values]
+  static constexpr uint32_t SB_BYTES = 128 * 128 * 2;
+  static constexpr uint32_t GC = SB + 2 * SB_BYTES;            // gamma_C [kWStages][128] float
+  // full[kWStages], empty[kWStages], mS, mO[kWOutBufs], ofree[kWOutBufs]
+  static constexpr uint32_t BAR = GC + kWStages * 128 * 4;
+  static constexpr uint32_t TMEMP = BAR + (2 * kWStages + 1 + 2 * kWOutBufs) * 8;
+  static constexpr uint32_t ABORT = TMEMP + 4;                 // CTA-wide abort word
+  static constexpr uint32_t BYTES = TMEMP + 8;
+  static constexpr uint32_t TMEM_COLS = 512;                   // P | o[0] | o[1], 128 each
+  static_assert(128 * (1 + kWOutBufs) <= (int)TMEM_COLS, "TMEM columns");
+  static_assert(BYTES + 1024 <= 232448, "wide scan shared memory");
+};
+
+// 32 * n bf16 of row r of a [4][rows][32] rotated block array (B or O of a
+// record), blocks blk0 .. blk0 + n - 1 (columns 32 blk0 ..), as 16-byte loads
+// from L2.
+template <int n>
+__device__ __forceinline__ void load_row_blocks(const uint8_t *blocks, int rows, int r, int blk0,
+                                                uint4 (&u)[4 * n]) {
+#pragma unroll
+  for (int b2 = 0; b2 < n; ++b2)
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      u[4 * b2 + q] = __ldg(reinterpret_cast<const uint4 *>(
+          blocks + (size_t)(blk0 + b2) * rows * 64 + rotated_chunk(r, q)));
+}
+
+__device__ __forceinline__ void scan_wide_d128(const float *h0, __nv_bfloat16 *__restrict__ o,
+                                               float *hT, int T, int NC,
+                                               uint8_t *__restrict__ ws, uint8_t *sm) {
+  constexpr int D = 128;
+  constexpr uint32_t kSyncThreads = 256 + 32;  // state warps + issuer warp
+  using R = Rec<128>;
+  using L = ScanWideSmem;
+  uint64_t *full = reinterpret_cast<uint64_t *>(sm + L::BAR);
+  uint64_t *empty = full + kWStages;
+  uint64_t *mS = empty + kWStages;
+  uint64_t *mO = mS + 1;
+  uint64_t *ofree = mO + kWOutBufs;
+  uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(sm + L::TMEMP);
+  uint32_t *abort_f = reinterpret_cast<uint32_t *>(sm + L::ABORT);
+  const float *gcr = reinterpret_cast<const float *>(sm + L::GC);
+  WorkspaceHeader *hdr = reinterpret_cast<WorkspaceHeader *>(ws);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.x;
+  const uint8_t *rec0 = ws + sizeof(WorkspaceHeader) + (size_t)bh * NC * R::BYTES;
+  // After a failed wait: the abort word is set and the thread skips its later
+  // waits; the producer stops copying and drains its copies, the issuer
+  // drains its products before TMEM is released (as in the split scan).
+  bool ok = true;
+  auto fail = [&](unsigned where) {
+    ok = false;
+    ptx::set_abort(abort_f);
+    report_error(hdr, KDA_ERR_TIMEOUT, where);
+  };
+
+  if (tid == 0) {
+    for (int s = 0; s < kWStages; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 2);  // released by the state side and by the output warps
+    }
+    ptx::mbar_init(mS, 1);
+    for (int b = 0; b < kWOutBufs; ++b) {
+      ptx::mbar_init(&mO[b], 1);
+      ptx::mbar_init(&ofree[b], 1);
+    }
+    *abort_f = 0u;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc(tmem_ptr, L::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_ptr;
+  const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+  auto sb_of = [&](int chunk) { return sm + L::SB + (chunk & 1) * L::SB_BYTES; };
+
+  if (warp == 10) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      int j = 0;
+      for (; j < NC; ++j) {
+        const int s = j % kWStages;
+        if (j >= kWStages && ok &&
+            !ptx::mbar_wait_fast(&empty[s], ((j / kWStages) - 1) & 1, kWaitLimit))
+          fail(0x310u);
+        if (!ok) break;
+        // whole records into L2 three chunks ahead: the stage copies and the
+        // state and output warps' loads of B and O then meet L2, not DRAM
+        if (j + kPrefetchAhead < NC)
+          ptx::prefetch_l2(rec0 + (size_t)(j + kPrefetchAhead) * R::BYTES, R::BYTES);
+        const uint8_t *rec = rec0 + (size_t)j * R::BYTES;
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive_expect_tx(&full[s], R::PRE + 128 * 4);
+        ptx::bulk_g2s(sm + s * L::STAGE, rec, R::PRE, &full[s]);
+        ptx::bulk_g2s(sm + L::GC + s * 512, rec + R::GC, 128 * 4, &full[s]);
+      }
+      if (!ok)  // drain (bounded): the copies still in flight (j were issued)
+        for (int i = j > kWStages ? j - kWStages : 0; i < j; ++i)
+          if (!ptx::mbar_wait(&full[i % kWStages], (i / kWStages) & 1, kWaitLimit)) break;
+    }
+  } else if (warp == 11) {
+    // ---------------------------------------------------------- issuer
+    uint64_t dAPs[kWStages], dQPs[kWStages], dSBs[2];
+#pragma unroll
+    for (int q = 0; q < kWStages; ++q) {
+      dAPs[q] = umma::sdesc(ptx::smem_u32(sm + q * L::STAGE + R::AP));
+      dQPs[q] = umma::sdesc(ptx::smem_u32(sm + q * L::STAGE + R::QP));
+    }
+#pragma unroll
+    for (int q = 0; q < 2; ++q) dSBs[q] = umma::sdesc_mn(ptx::smem_u32(sb_of(q)), 128, 0);
+    static_assert(kWStages == 3 && kWOutBufs == 2, "six-chunk issuer period");
+    for (int i0 = 0; i0 < NC; i0 += 6)
+#pragma unroll
+    for (int u = 0; u < 6; ++u) {
+      const int i = i0 + u;
+      if (i >= NC) break;
+      const int b = u % kWOutBufs;
+      const uint64_t dAP = dAPs[u % kWStages], dQP = dQPs[u % kWStages], dSB = dSBs[u & 1];
+      ptx::named_barrier(1, kSyncThreads);  // S_i written, record i landed, o[b] free
+      if (lane == 0) {
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)  // P = Ap S   (S read MN-major, N = 128)
+          ptx::mma_bf16_ss(tmem, dAP + (uint64_t)(((ks >> 2) * D * 128 + (ks & 3) * 32) >> 4),
+                           dSB + (uint64_t)(ks * 2048 >> 4), umma::idesc_bf16_bmn(128, D), ks > 0);
+        ptx::mma_commit(mS);
+        const uint32_t tOc = tmem + D + D * b;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)  // o = Qp S  (M = 128: rows 64-127 unused)
+          ptx::mma_bf16_ss(tOc, dQP + (uint64_t)(((ks >> 2) * kC * 128 + (ks & 3) * 32) >> 4),
+                           dSB + (uint64_t)(ks * 2048 >> 4), umma::idesc_bf16_bmn(128, D), ks > 0);
+        ptx::mma_commit(&mO[b]);
+      }
+      __syncwarp();
+    }
+    if (lane == 0 && ptx::aborted(abort_f)) {  // let this thread's MMAs finish before TMEM is freed
+      ptx::mma_commit(mS);
+      ptx::mbar_wait(mS, NC & 1, kWaitLimit);
+    }
+  } else if (warp >= 8) {
+    // ---------------------------------------------------------- output warps
+    // warp 8 + w reads TMEM lane quarter w: token rows 32 w + lane
+    const int row = (warp - 8) * 32 + lane;
+    const uint8_t *orec = rec0 + R::OI;
+    for (int j = 0; j < NC; ++j, orec += R::BYTES) {
+      const int b = j % kWOutBufs, s = j % kWStages;
+      uint4 Oc[8];  // O of this row, columns 0-63, from L2, loaded while the product runs
+      load_row_blocks<2>(orec, kC, row, 0, Oc);
+      if (ok && !ptx::mbar_wait(&mO[b], (j / kWOutBufs) & 1, kWaitLimit)) fail(0x321u);
+      ptx::tc_fence_after();
+      const uint32_t tO = t_lane + D + D * b;
+      const int t = j * kC + row;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {  // 32-column block c of the row
+        if (c == 2) load_row_blocks<2>(orec, kC, row, 2, Oc);  // columns 64-127
+        float x[32];
+        ptx::tmem_ld32(tO + 32 * c, x);
+        ptx::tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 a = Oc[4 * (c & 1) + q];
+          const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 p2 = *reinterpret_cast<const __nv_bfloat162 *>(&w[e]);
+            pk[4 * q + e] = pack_bf16x2(x[8 * q + 2 * e] + __low2float(p2),
+                                        x[8 * q + 2 * e + 1] + __high2float(p2));
+          }
+        }
+        if (t < T) {
+          uint4 *dst = reinterpret_cast<uint4 *>(o + ((size_t)bh * T + t) * D + 32 * c);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::named_barrier(2, 64);  // all output rows of chunk j read from TMEM
+      if (tid == 256) {
+        ptx::mbar_arrive(&ofree[b]);
+        ptx::mbar_arrive(&empty[s]);  // Qp of stage s was read by the output product
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- state warps
+    const int r = (warp & 3) * 32 + lane, half = warp >> 2;  // key row, column half
+    const uint32_t tP = t_lane + 64 * half;
+    float sr[64];
+#pragma unroll
+    for (int j = 0; j < 64; ++j) sr[j] = 0.f;
+    if (h0) {
+      const float4 *src = reinterpret_cast<const float4 *>(h0 + (size_t)bh * D * D + (size_t)r * D +
+                                                           64 * half);
+#pragma unroll
+      for (int j4 = 0; j4 < 16; ++j4) {
+        const float4 a = src[j4];
+        sr[4 * j4] = a.x; sr[4 * j4 + 1] = a.y; sr[4 * j4 + 2] = a.z; sr[4 * j4 + 3] = a.w;
+      }
+    }
+    for (int i = 0; i < NC; ++i) {
+      const int s = i % kWStages;
+      uint8_t *sb = sb_of(i);
+      uint4 Bc[8];  // this chunk's B row slice, from L2 (used after the hand-off)
+      load_row_blocks<2>(rec0 + (size_t)i * R::BYTES + R::BI, 128, r, 2 * half, Bc);
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) st_chunk(sb, r, 8 * half + c8, 128, sr + 8 * c8);
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      // record i landed (gamma_C is read below), output accumulator (i mod 2)
+      // read by the output warps (chunk i - 2), stage i - 1 released for the
+      // state side (its product completed before P_{i-1} was read)
+      if (ok && !ptx::mbar_wait_fast(&full[s], (i / kWStages) & 1, kWaitLimit)) fail(0x304u);
+      if (tid == 0) {
+        if (i >= kWOutBufs && ok &&
+            !ptx::mbar_wait_fast(&ofree[i % kWOutBufs], ((i / kWOutBufs) - 1) & 1, kWaitLimit))
+          fail(0x322u);
+        if (i > 0) ptx::mbar_arrive(&empty[(i - 1) % kWStages]);
+      }
+      __syncwarp();
+      ptx::named_arrive(1, kSyncThreads);
+      {  // gamma_C S + B while the product runs
+        const float gam = gcr[s * 128 + r];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t w[4] = {Bc[q].x, Bc[q].y, Bc[q].z, Bc[q].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 p2 = *reinterpret_cast<const __nv_bfloat162 *>(&w[e]);
+            sr[8 * q + 2 * e] = gam * sr[8 * q + 2 * e] + __low2float(p2);
+            sr[8 * q + 2 * e + 1] = gam * sr[8 * q + 2 * e + 1] + __high2float(p2);
+          }
+        }
+      }
+      if (ok && !ptx::mbar_wait(mS, i & 1, kWaitLimit)) fail(0x301u);
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        float x[16];
+        ptx::tmem_ld16(tP + 16 * c4, x);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) sr[16 * c4 + j] += x[j];
+      }
+    }
+    if (hT) {
+      float4 *dst = reinterpret_cast<float4 *>(hT + (size_t)bh * D * D + (size_t)r * D + 64 * half);
+#pragma unroll
+      for (int j4 = 0; j4 < 16; ++j4)
+        dst[j4] = make_float4(sr[4 * j4], sr[4 * j4 + 1], sr[4 * j4 + 2], sr[4 * j4 + 3]);
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, L::TMEM_COLS);
+  }
+}
+
+__global__ void __launch_bounds__(kWideThreads, 1)
+kda_scan_wide_kernel(const float *h0, __nv_bfloat16 *__restrict__ o, float *hT, int T, int NC,
+                     uint8_t *__restrict__ ws) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                            ~static_cast<uintptr_t>(1023));
+  scan_wide_d128(h0, o, hT, T, NC, ws, sm);
+}
+
 template <int D, int NB, bool kNorm>
 __global__ void __launch_bounds__(kScan128Threads, 1)
 kda_scan_kernel(const float *h0, __nv_bfloat16 *__restrict__ o, float *hT, int T, int NC,
@@ -1806,11 +2109,19 @@ kda_scan_kernel(const float *h0, __nv_bfloat16 *__restrict__ o, float *hT, int T
 template <int D>
 constexpr int scan_nb() { return 32; }
 
+int sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return sms;
+}
+
 template <int D>
 kda_status launch_d(const void *q, const void *k, const void *v, const float *beta,
                     const float *log_alpha, const float *h0, void *o, float *hT, int BH, int T,
                     kda_alpha_mode am, uint8_t *ws, cudaStream_t st, LaunchTimer &timer,
-                    int rule, unsigned maps) {
+                    int rule, unsigned maps, bool wide) {
   constexpr int NB = scan_nb<D>();
   const int NC = (T + kC - 1) / kC;
   const uint32_t prep_smem = (D == 128 ? PrepSmem128::BYTES : PrepSmem64::BYTES) + 1024;
@@ -1827,16 +2138,19 @@ kda_status launch_d(const void *q, const void *k, const void *v, const float *be
   if constexpr (D == 128) {
     if (rule == KDA_RULE_LINEAR_NORM) scan = kda_scan_kernel<D, NB, true>;
   }
+  constexpr uint32_t wide_smem = ScanWideSmem::BYTES + 1024;
   if (cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)prep_smem) != cudaSuccess ||
       cudaFuncSetAttribute(scan, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)scan_smem) != cudaSuccess)
     return KDA_ERR_CUDA;
+  if (D == 128 && wide &&
+      cudaFuncSetAttribute(kda_scan_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)wide_smem) != cudaSuccess)
+    return KDA_ERR_CUDA;
   if (NC > 0) {
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return KDA_ERR_CUDA;
+    const int sms = sm_count();
+    if (sms <= 0) return KDA_ERR_CUDA;
     const long long total = (long long)BH * NC;
     if (total > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
     const long long slots = (long long)sms * (D == 128 ? 2 : 1);  // persistent CTAs per SM
@@ -1848,8 +2162,12 @@ kda_status launch_d(const void *q, const void *k, const void *v, const float *be
         rule, maps);
   }
   timer.mark();
-  scan<<<dim3(D / NB, BH), D == 128 ? kScan128Threads : 128, scan_smem, st>>>(
-      h0, static_cast<__nv_bfloat16 *>(o), hT, T, NC, ws);
+  if (D == 128 && wide)
+    kda_scan_wide_kernel<<<BH, kWideThreads, wide_smem, st>>>(
+        h0, static_cast<__nv_bfloat16 *>(o), hT, T, NC, ws);
+  else
+    scan<<<dim3(D / NB, BH), D == 128 ? kScan128Threads : 128, scan_smem, st>>>(
+        h0, static_cast<__nv_bfloat16 *>(o), hT, T, NC, ws);
   timer.mark();
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
@@ -1874,23 +2192,37 @@ int chunk_tc_launches(int BH, int T, bool has_hT) {
   return T > 0 ? 2 : 1;
 }
 
-const char *chunk_tc_kernel_name(int T, int i) {
-  if (T == 0) return i == 0 ? "kda_scan_kernel" : nullptr;
-  return i == 0 ? "kda_prep_kernel" : (i == 1 ? "kda_scan_kernel" : nullptr);
+bool chunk_tc_wide_scan(int BH, int dk, int rule, int scan) {
+  if (dk != 128 || rule == KDA_RULE_LINEAR_NORM || scan == 1) return false;
+  if (scan == 2) return true;
+  // automatic: the wide scan when it needs fewer rounds of CTAs than the
+  // value-column split (one CTA per SM either way)
+  const long long sms = sm_count();
+  if (sms <= 0) return false;
+  const long long split = ((long long)BH * 4 + sms - 1) / sms, wide = (BH + sms - 1) / sms;
+  return wide < split;
+}
+
+const char *chunk_tc_kernel_name(int BH, int T, int dk, int scan, int i) {
+  const char *scan_name = chunk_tc_wide_scan(BH, dk, 0, scan) ? "kda_scan_wide_kernel"
+                                                               : "kda_scan_kernel";
+  if (T == 0) return i == 0 ? scan_name : nullptr;
+  return i == 0 ? "kda_prep_kernel" : (i == 1 ? scan_name : nullptr);
 }
 
 kda_status launch_chunk_tc(const void *q, const void *k, const void *v, const float *beta,
                            const float *log_alpha, const float *h0, void *o, float *hT, int B,
                            int H, int T, int dk, int /*dv*/, int /*C*/, kda_alpha_mode am,
                            void *workspace, size_t /*ws_bytes*/, cudaStream_t stream,
-                           LaunchTimer &timer, int rule, unsigned maps) {
+                           LaunchTimer &timer, int rule, unsigned maps, int scan) {
   const int BH = B * H;
   if (chunk_tc_launches(BH, T, hT != nullptr) == 0) return KDA_OK;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   if (dk == 128)
     return launch_d<128>(q, k, v, beta, log_alpha, h0, o, hT, BH, T, am, ws, stream, timer, rule,
-                         maps);
-  return launch_d<64>(q, k, v, beta, log_alpha, h0, o, hT, BH, T, am, ws, stream, timer, 0, 0u);
+                         maps, chunk_tc_wide_scan(BH, dk, rule, scan));
+  return launch_d<64>(q, k, v, beta, log_alpha, h0, o, hT, BH, T, am, ws, stream, timer, 0, 0u,
+                      false);
 }
 
 }  // namespace kda

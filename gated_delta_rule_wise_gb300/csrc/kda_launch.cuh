@@ -36,7 +36,10 @@ kda_status launch_chunk_ffma(const void *q, const void *k, const void *v, const 
 int chunk_ffma_launches(int BH, int T, bool has_hT);
 const char *chunk_ffma_kernel_name(int i);
 int chunk_tc_launches(int BH, int T, bool has_hT);
-const char *chunk_tc_kernel_name(int T, int i);
+// scan: 0 automatic, 1 the value-column split scan, 2 the one-CTA-per-head
+// scan (d = 128 only; not for the normalised linear-attention rule).
+bool chunk_tc_wide_scan(int BH, int dk, int rule, int scan);
+const char *chunk_tc_kernel_name(int BH, int T, int dk, int scan, int i);
 bool chunk_tc_supported(int dk, int dv, int C, kda_dtype dt);
 size_t chunk_tc_workspace_bytes(int B, int H, int T, int dk, int dv, int C);
 // rule: KDA_RULE_DELTA / KDA_RULE_LINEAR; maps: KDA_MAP_* bits (both other
@@ -45,7 +48,7 @@ kda_status launch_chunk_tc(const void *q, const void *k, const void *v, const fl
                            const float *log_alpha, const float *h0, void *o, float *hT,
                            int B, int H, int T, int dk, int dv, int C, kda_alpha_mode am,
                            void *workspace, size_t workspace_bytes, cudaStream_t stream,
-                           LaunchTimer &timer, int rule = 0, unsigned maps = 0);
+                           LaunchTimer &timer, int rule = 0, unsigned maps = 0, int scan = 0);
 kda_status launch_selftest_wait(WorkspaceHeader *hdr, unsigned spin_limit,
                                 cudaStream_t stream);
 // Every check kda_chunk_fwd_ex makes before it launches anything (shapes,

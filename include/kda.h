@@ -76,8 +76,16 @@ typedef enum {
 typedef enum {
   KDA_PATH_AUTO = 0,     /* tensor-core path where supported, else CUDA cores */
   KDA_PATH_CUDA_CORE = 1,/* fp32 FFMA chunked kernel (every supported shape)   */
-  KDA_PATH_TENSOR = 2    /* tcgen05 prep + scan (bf16, C = 64, dk,dv in {64,128});
-                            KDA_ERR_UNSUPPORTED elsewhere                       */
+  KDA_PATH_TENSOR = 2,   /* tcgen05 prep + scan (bf16, C = 64, dk = dv in {64,128});
+                            KDA_ERR_UNSUPPORTED elsewhere; the scan kernel is
+                            chosen as below                                     */
+  KDA_PATH_TENSOR_SPLIT_SCAN = 3, /* tensor path, the scan split by value columns
+                            (several CTAs per head; the only scan at dk = 64)   */
+  KDA_PATH_TENSOR_WIDE_SCAN = 4   /* tensor path, one scan CTA per (batch, head)
+                            holding all value columns (dk = dv = 128 only, else
+                            KDA_ERR_UNSUPPORTED).  KDA_PATH_AUTO / _TENSOR take
+                            it when it needs fewer rounds of CTAs than the split
+                            scan, i.e. when B*H exceeds a quarter of the SMs    */
 } kda_path;
 
 /* ABI version of this header; kda_abi_version() returns the library's. */

@@ -75,7 +75,13 @@ def test_workspace_size(lib):
     assert ws(-1, 1, 64, 16, 16, 16, kda.KDA_F32, kda.KDA_ALPHA_NONE) == 0     # negative
     assert ws(1, 1, 64, 16, 16, 16, 7, kda.KDA_ALPHA_NONE) == 0                # bad dtype
     assert ws(1, 1, 64, 16, 16, 16, kda.KDA_F32, 9) == 0                       # bad mode
-    assert ws(1, 1, 64, 16, 16, 16, kda.KDA_F32, kda.KDA_ALPHA_NONE, 5) == 0   # bad path
+    assert ws(1, 1, 64, 16, 16, 16, kda.KDA_F32, kda.KDA_ALPHA_NONE, 6) == 0   # bad path
+    wsx = kda.kda_chunk_fwd_workspace_size
+    big = (1, 32, 4096, 128, 128, 64, kda.KDA_BF16, kda.KDA_ALPHA_CHANNEL)
+    # both scans of the tensor path read the same per-chunk records
+    assert wsx(*big, kda.KDA_PATH_TENSOR_SPLIT_SCAN) == wsx(*big, kda.KDA_PATH_TENSOR)
+    assert wsx(*big, kda.KDA_PATH_TENSOR_WIDE_SCAN) == wsx(*big, kda.KDA_PATH_TENSOR)
+    assert wsx(1, 2, 64, 64, 64, 64, kda.KDA_BF16, 0, kda.KDA_PATH_TENSOR_WIDE_SCAN) == 0
 
 
 def test_host_buffer_size(lib):
@@ -131,6 +137,10 @@ def test_chunk_argument_validation(lib):
     assert _chunk(lib, dt=3) == INV
     assert _chunk(lib, B=70000, H=1) == UNS
     assert _chunk(lib, path=2, dt=0) == UNS          # tensor path needs bf16
+    assert _chunk(lib, path=3, dt=0) == UNS          # ... both of its scans
+    assert _chunk(lib, path=4, dt=0) == UNS
+    assert _chunk(lib, path=4, dt=1, dk=64, dv=64, C=64) == UNS   # wide scan: d = 128 only
+    assert _chunk(lib, path=6) == INV                # unknown path
     assert _chunk(lib, nev=2) == INV                 # events requested but NULL
     one = (ctypes.c_void_p * 1)(FAKE)
     assert _chunk(lib, ev=one, nev=1) == INV         # fewer events than launches + 1

@@ -20,7 +20,8 @@ from _margins import case_name, record
 pytestmark = pytest.mark.gpu
 
 PATHS = {"auto": kda.KDA_PATH_AUTO, "cuda_core": kda.KDA_PATH_CUDA_CORE,
-         "tensor": kda.KDA_PATH_TENSOR}
+         "tensor": kda.KDA_PATH_TENSOR, "split": kda.KDA_PATH_TENSOR_SPLIT_SCAN,
+         "wide": kda.KDA_PATH_TENSOR_WIDE_SCAN}
 
 
 def tensor_path_ok(w):
@@ -95,6 +96,53 @@ def test_gdn_bf16_sampled_heads():
 @pytest.mark.slow
 def test_kda_prefill_bf16_full_size_sampled_heads():
     _sampled(W.KDA_PREFILL_BF16, 16, seed=1)
+
+
+@pytest.mark.slow
+def test_kda_prefill_bf16_full_size_wide_scan_sampled_heads():
+    """The full KDA workload through the one-CTA-per-head scan (the automatic
+    choice takes the split scan for its 32 heads)."""
+    _sampled(W.KDA_PREFILL_BF16, 8, path="wide", seed=2)
+
+
+def test_gdn_bf16_split_scan_sampled_heads():
+    """Gated DeltaNet (128 heads: the automatic choice is the one-CTA-per-head
+    scan) through the value-column split scan as well."""
+    _sampled(W.GDN_BF16, 6, path="split", seed=4)
+
+
+# ---------------------------------------------------------------- the two scans of the tensor path
+
+@pytest.mark.parametrize("alpha", ["none", "scalar", "channel"])
+@pytest.mark.parametrize("B,H,T", [(1, 2, 3 * 64 + 33), (2, 3, 64), (1, 1, 1), (1, 5, 700),
+                                   (1, 3, 64 * 7 + 63)])
+def test_wide_scan_matches_oracle(alpha, B, H, T):
+    """One scan CTA per (batch, head): several chunks, ragged last chunk,
+    initial state, every decay mode."""
+    w = W.Prefill("wide", B=B, H=H, T=T, dk=128, dv=128, C=64, dtype="bf16", alpha=alpha,
+                  la_mu=-3.5, h0_sd=0.05, seed=T + 7 * H + len(alpha))
+    check_full(w, "wide")
+
+
+def test_wide_scan_long_sequence_many_chunks():
+    w = W.KDA_PREFILL_BF16.with_(B=1, H=4, T=64 * 300 + 17, h0_sd=0.02, seed=23)
+    check_full(w, "wide")
+
+
+def test_wide_scan_empty_sequence_copies_initial_state():
+    w = W.GDN_BF16.with_(B=2, H=3, T=0)
+    x = W.prefill_inputs(w)
+    d = device_inputs(w, x)
+    o, hT = run(w, d, "wide")
+    np.testing.assert_array_equal(hT.cpu().numpy(), x["h0"])
+
+
+def test_wide_scan_rejected_at_d64():
+    w = W.DELTANET_BF16.with_(B=1, H=1, T=64)
+    d = device_inputs(w, W.prefill_inputs(w))
+    with pytest.raises(kda.KdaError) as e:
+        run(w, d, "wide")
+    assert e.value.status == kda.KDA_ERR_UNSUPPORTED
 
 
 # ---------------------------------------------------------------- shapes and edge cases
