@@ -1789,10 +1789,14 @@ __device__ __forceinline__ void scan_d64(const float *h0, __nv_bfloat16 *__restr
 
 
 // D = 128, one CTA per (batch, head) holding all 128 value columns ("wide"
-// scan).  The value-column split above gives a head four CTAs, each issuing
-// the same sixteen MMAs per chunk on a 32-column slice; when heads outnumber
-// a quarter of the SMs those CTAs run in several rounds, and one CTA per head
-// that issues the sixteen MMAs on N = 128 takes one round.  Roles:
+// scan, KDA_PATH_TENSOR_WIDE_SCAN).  The value-column split above gives a
+// head four CTAs, each issuing the same sixteen MMAs per chunk on a 32-column
+// slice; this CTA issues the sixteen on N = 128 and so needs a quarter of the
+// CTAs (one round where the split needs several when heads outnumber a
+// quarter of the SMs), but streams each whole 98.8 KB record through one SM.
+// Measured on Gated DeltaNet (8 x 16 heads x 8192 tokens) it matched the
+// split scan (0.442 against 0.434 ms: the records' HBM traffic bounds both),
+// so the automatic choice stays with the split scan.  Roles:
 //  - eight state warps: warp w owns key rows 32 (w mod 4) .. +31 (its TMEM
 //    lane quarter) and value columns 64 (w / 4) .. +63, each thread one row
 //    of 64 columns in registers as float;
@@ -2195,12 +2199,11 @@ int chunk_tc_launches(int BH, int T, bool has_hT) {
 bool chunk_tc_wide_scan(int BH, int dk, int rule, int scan) {
   if (dk != 128 || rule == KDA_RULE_LINEAR_NORM || scan == 1) return false;
   if (scan == 2) return true;
-  // automatic: the wide scan when it needs fewer rounds of CTAs than the
-  // value-column split (one CTA per SM either way)
-  const long long sms = sm_count();
-  if (sms <= 0) return false;
-  const long long split = ((long long)BH * 4 + sms - 1) / sms, wide = (BH + sms - 1) / sms;
-  return wide < split;
+  // automatic: the split scan.  The wide scan streams each whole record
+  // through one SM; measured on Gated DeltaNet (128 heads, 128 chunks) it
+  // took 0.442 ms against 0.434 ms for the split scan in four rounds: there
+  // the records' HBM traffic, not the rounds, sets the scan's time.
+  return false;
 }
 
 const char *chunk_tc_kernel_name(int BH, int T, int dk, int scan, int i) {

@@ -83,9 +83,8 @@ typedef enum {
                             (several CTAs per head; the only scan at dk = 64)   */
   KDA_PATH_TENSOR_WIDE_SCAN = 4   /* tensor path, one scan CTA per (batch, head)
                             holding all value columns (dk = dv = 128 only, else
-                            KDA_ERR_UNSUPPORTED).  KDA_PATH_AUTO / _TENSOR take
-                            it when it needs fewer rounds of CTAs than the split
-                            scan, i.e. when B*H exceeds a quarter of the SMs    */
+                            KDA_ERR_UNSUPPORTED).  KDA_PATH_AUTO / _TENSOR use
+                            the split scan                                       */
 } kda_path;
 
 /* ABI version of this header; kda_abi_version() returns the library's. */

@@ -105,10 +105,10 @@ def test_kda_prefill_bf16_full_size_wide_scan_sampled_heads():
     _sampled(W.KDA_PREFILL_BF16, 8, path="wide", seed=2)
 
 
-def test_gdn_bf16_split_scan_sampled_heads():
-    """Gated DeltaNet (128 heads: the automatic choice is the one-CTA-per-head
-    scan) through the value-column split scan as well."""
-    _sampled(W.GDN_BF16, 6, path="split", seed=4)
+def test_gdn_bf16_wide_scan_sampled_heads():
+    """Gated DeltaNet (128 heads, h0 given) through the one-CTA-per-head scan
+    as well (the automatic choice is the value-column split scan)."""
+    _sampled(W.GDN_BF16, 6, path="wide", seed=4)
 
 
 # ---------------------------------------------------------------- the two scans of the tensor path
