@@ -676,8 +676,10 @@ __device__ __forceinline__ uint4 pack8(const float *x) {
 // 2 is for the linear rules only (no solve compiled in) and adds the ELU + 1
 // map and the normalised rule's sums.  The modes are separate instantiations
 // because the prep runs at the register limit: code that only one mode needs
-// would cost the others spills.
-template <int kMode>
+// would cost the others spills.  kRowDecay: scalar or no decay (one factor per
+// token row) rather than one per key channel; a separate instantiation too
+// (both decay paths in one kernel made the per-channel one 4 % slower).
+template <int kMode, bool kRowDecay>
 __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
                                           const __nv_bfloat16 *__restrict__ k,
                                           const __nv_bfloat16 *__restrict__ v,
@@ -717,7 +719,7 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
     report_error(hdr, KDA_ERR_TIMEOUT, where);
   };
 
-  const bool la_bulk = alpha_mode == KDA_ALPHA_CHANNEL;  // per-channel rows: 512 B each
+  constexpr bool la_bulk = !kRowDecay;  // per-channel log_alpha rows (512 B each), bulk-copied
   auto rows_of = [&](int idx, int &valid, size_t &row0) {
     const int t0 = (idx % NC) * kC;
     valid = min(kC, T - t0);
@@ -819,28 +821,22 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
     // ---- (0) decay
     if (tid < kC) betas[tid] = b_next;
     if (ok && !ptx::mbar_wait(lbar, it & 1, kWaitLimit)) fail(0x100u);
-    float ld[R];
-    if (la_bulk) {  // one straight run of shared loads
+    // gamma is measured from the middle of the chunk (g at row C/2 - 1 = p0):
+    // the split factors gamma and 1/gamma then stay within exp(|half-chunk
+    // decay|), so float and bf16 hold them up to a decay of about 87 per half
+    // chunk; the chunk-start values are restored where they are needed
+    if (la_bulk) {  // one decay per key channel: a prefix per channel
+      float ld[R];
 #pragma unroll
-      for (int i = 0; i < R; ++i) ld[i] = EG[(r0 + i) * D + c];
-    } else {
+      for (int i = 0; i < R; ++i) ld[i] = EG[(r0 + i) * D + c];  // one straight run of shared loads
+      float psum = 0.f;
 #pragma unroll
-      for (int i = 0; i < R; ++i)
-        ld[i] = alpha_mode == KDA_ALPHA_SCALAR ? log_alpha[row0 + min(r0 + i, valid - 1)] : 0.f;
-    }
-    float psum = 0.f;
-#pragma unroll
-    for (int i = 0; i < R; ++i) {
-      ld[i] = (r0 + i < valid && alpha_mode != KDA_ALPHA_NONE) ? -__expf(ld[i]) : 0.f;
-      psum += ld[i];
-    }
-    part[half * D + c] = psum;
-    __syncthreads();
-    {
-      // gamma measured from the middle of the chunk (g at row C/2 - 1 = p0):
-      // the split factors gamma and 1/gamma then stay within exp(|half-chunk
-      // decay|), so float and bf16 hold them up to a decay of about 87 per
-      // half chunk; the chunk-start values are restored where they are needed
+      for (int i = 0; i < R; ++i) {
+        ld[i] = (r0 + i < valid) ? -__expf(ld[i]) : 0.f;
+        psum += ld[i];
+      }
+      part[half * D + c] = psum;
+      __syncthreads();
       const float p0 = part[c], p1 = part[D + c];
       float g = half ? 0.f : -p0;
 #pragma unroll
@@ -853,6 +849,33 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
         gcs[c] = __expf(p1);   // gamma_C / gamma_mid: scales (K/gamma)^T into Kbar^T
         gmid[c] = __expf(p0);  // gamma_mid: turns Q*gamma (mid-referenced) into Q*gamma
         reinterpret_cast<float *>(recg + Rr::GC)[c] = __expf(p0 + p1);
+      }
+    } else {
+      // one decay per token (scalar mode) or none: the prefix over the chunk's
+      // rows runs once, one thread per row in the first two warps (a warp scan
+      // each, the first warp's total carried into the second), and the tiles
+      // take gamma and 1/gamma per row from EG[r] and EG[C + r]
+      float x = 0.f;
+      if (tid < kC) {
+        if (alpha_mode == KDA_ALPHA_SCALAR && tid < valid) x = -__expf(log_alpha[row0 + tid]);
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, x, off);
+          if (lane >= off) x += y;
+        }
+        if (lane == 31) part[warp] = x;  // rows 0-31 (= g at row C/2 - 1) and rows 32-63
+      }
+      __syncthreads();
+      const float p0 = part[0], p1 = part[1];
+      if (tid < kC) {
+        const float g = warp == 0 ? x - p0 : x;  // g_r - g_mid
+        EG[tid] = __expf(g);
+        EG[kC + tid] = __expf(-g);
+      }
+      if (tid < D) {
+        gcs[tid] = __expf(p1);
+        gmid[tid] = __expf(p0);
+        reinterpret_cast<float *>(recg + Rr::GC)[tid] = __expf(p0 + p1);
       }
     }
     if (ok && !ptx::mbar_wait(qbar, it & 1, kWaitLimit)) fail(0x105u);
@@ -909,11 +932,19 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
           kf[e] *= ik;
         }
       }
-      const float4 e0 = *reinterpret_cast<const float4 *>(EG + r * (D / 2) + c8 * 4);
-      const float4 e1 =
-          *reinterpret_cast<const float4 *>(EG + L::EG_PLANE / 4 + r * (D / 2) + c8 * 4);
-      eg[0] = e0.x; eg[1] = e0.y; eg[2] = e0.z; eg[3] = e0.w;
-      eg[4] = e1.x; eg[5] = e1.y; eg[6] = e1.z; eg[7] = e1.w;
+      float igr = 0.f;  // per-row 1 / gamma (scalar or no decay)
+      if (la_bulk) {
+        const float4 e0 = *reinterpret_cast<const float4 *>(EG + r * (D / 2) + c8 * 4);
+        const float4 e1 =
+            *reinterpret_cast<const float4 *>(EG + L::EG_PLANE / 4 + r * (D / 2) + c8 * 4);
+        eg[0] = e0.x; eg[1] = e0.y; eg[2] = e0.z; eg[3] = e0.w;
+        eg[4] = e1.x; eg[5] = e1.y; eg[6] = e1.z; eg[7] = e1.w;
+      } else {  // per-row factors
+        const float gr = EG[r];
+        igr = EG[kC + r];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) eg[e] = gr;
+      }
       const float bt = betas[r];
       float kb[8], qg[8], vb[8], kh[8];
 #pragma unroll
@@ -925,7 +956,7 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
                        : bt * kf[e] * eg[e];
         qg[e] = qf[e] * eg[e];
         vb[e] = bt * vf[e];
-        kh[e] = kf[e] * __fdividef(1.f, eg[e]);
+        kh[e] = kf[e] * (la_bulk ? __fdividef(1.f, eg[e]) : igr);
       }
       st_chunk(X1, r, c8, 128, kb);                 // K_beta          (blocks 0-1, rows 0-63)
       st_chunk(X1, kC + r, c8, 128, qg);            // Q * gamma       (blocks 0-1, rows 64-127)
@@ -1201,7 +1232,7 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
   }
 }
 
-template <int D, int kMode>
+template <int D, int kMode, bool kRowDecay>
 __global__ void __launch_bounds__(256, D == 128 ? 2 : 1)
 kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                 const __nv_bfloat16 *__restrict__ v, const float *__restrict__ beta,
@@ -1211,7 +1242,8 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));
   if constexpr (D == 128)
-    prep_d128<kMode>(q, k, v, beta, log_alpha, alpha_mode, T, NC, total, ws, sm, rule, maps);
+    prep_d128<kMode, kRowDecay>(q, k, v, beta, log_alpha, alpha_mode, T, NC, total, ws, sm, rule,
+                                maps);
   else
     prep_d64(q, k, v, beta, log_alpha, alpha_mode, T, NC, total, ws, sm);
 }
@@ -2131,12 +2163,15 @@ kda_status launch_d(const void *q, const void *k, const void *v, const float *be
   const uint32_t prep_smem = (D == 128 ? PrepSmem128::BYTES : PrepSmem64::BYTES) + 1024;
   const uint32_t scan_smem =
       (D == 128 ? ScanSmem128<NB>::BYTES : ScanSmem64<NB>::BYTES) + 1024;
-  auto prep = kda_prep_kernel<D, 0>;
+  auto prep = kda_prep_kernel<D, 0, false>;
   if constexpr (D == 128) {
+    const bool row = am != KDA_ALPHA_CHANNEL;  // scalar or no decay: one factor per token
     if (rule == KDA_RULE_LINEAR_NORM || (maps & KDA_MAP_QK_ELU1))
-      prep = kda_prep_kernel<D, 2>;
+      prep = row ? kda_prep_kernel<D, 2, true> : kda_prep_kernel<D, 2, false>;
     else if (rule != 0 || maps != 0u)
-      prep = kda_prep_kernel<D, 1>;
+      prep = row ? kda_prep_kernel<D, 1, true> : kda_prep_kernel<D, 1, false>;
+    else
+      prep = row ? kda_prep_kernel<D, 0, true> : kda_prep_kernel<D, 0, false>;
   }
   auto scan = kda_scan_kernel<D, NB, false>;
   if constexpr (D == 128) {
