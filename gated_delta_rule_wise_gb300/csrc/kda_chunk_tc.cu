@@ -1250,19 +1250,36 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
 
 // ============================================================== scan kernel
 
-// D = 64: double-buffered records, one commit per chunk, merged accumulator
-// (lanes 0..63 state, lanes 64..127 output).
+// D = 64: the scan's two products share one M = 128 accumulator: [Ap; Qp] S
+// and [Kbar^T; M] U are adjacent 64-row tiles of the record, so one group of
+// eight MMAs (K = 64 each way) leaves P + Kbar^T U in lanes 0-63 (key rows)
+// and o = Qp S + M U in lanes 64-127 (token rows).  Roles as in the d = 128
+// scan: two state warps (thread = key row, its NB columns in registers), two
+// output warps (the accumulator's lanes 64-127), a producer streaming the
+// CTA's share of each record through a 3-stage ring, an issuer.  Three
+// accumulators in turn let the output warps trail the state chain.
+constexpr int kS64Stages = 3;
+constexpr int kS64Acc = 3;
+constexpr int kScan64Threads = 192;  // 2 state warps, 2 output warps, producer, issuer
 template <int NB>
 struct ScanSmem64 {
   using B = Rec<64>;
   static constexpr int D = 64;
-  static constexpr uint32_t STAGE_BYTES = B::PRE + NB * 128 + D * 4;  // Ap|Qp|Kbar^T|M, U^T block, gamma_C
+  static constexpr uint32_t UT_S = B::PRE;                   // U^T block [NB rows][C]
+  static constexpr uint32_t GC_S = UT_S + NB * kC * 2;       // gamma_C [D]
+  static constexpr uint32_t STAGE_BYTES = GC_S + D * 4;      // Ap|Qp|Kbar^T|M, U^T block, gamma_C
   static constexpr uint32_t STAGE = align1k(STAGE_BYTES);
-  static constexpr uint32_t SB = 2 * STAGE;                 // bf16 state operand [NB rows][D]
-  static constexpr uint32_t BAR = SB + NB * D * 2;          // full[2], mma
-  static constexpr uint32_t TMEMP = BAR + 3 * 8;
+  static constexpr uint32_t SB = kS64Stages * STAGE;         // 2 x bf16 S [D keys][64 cols]
+  static constexpr uint32_t SB_BYTES = D * 64 * 2;
+  // full[kS64Stages], empty[kS64Stages], done[kS64Acc], ofree[kS64Acc]
+  static constexpr uint32_t BAR = SB + 2 * SB_BYTES;
+  static constexpr uint32_t TMEMP = BAR + (2 * kS64Stages + 2 * kS64Acc) * 8;
+  static constexpr uint32_t ABORT = TMEMP + 4;               // CTA-wide abort word
   static constexpr uint32_t BYTES = TMEMP + 8;
-  static constexpr uint32_t TMEM_COLS = NB <= 32 ? 32 : 64;
+  static constexpr uint32_t TMEM_COLS = 128;                 // acc[0..2], NB columns each
+  static_assert(NB * kS64Acc <= (int)TMEM_COLS, "TMEM columns");
+  static_assert((STAGE & 1023u) == 0 && (SB & 1023u) == 0, "operand tiles need 1024-byte alignment");
+  static_assert(BYTES + 1024 <= 232448, "scan shared memory");
 };
 
 // D = 128: four roles.  A producer warp streams records through a ring of
@@ -1610,33 +1627,40 @@ __device__ __forceinline__ void scan_d64(const float *h0, __nv_bfloat16 *__restr
                                          float *hT, int T, int NC,
                                          uint8_t *__restrict__ ws, uint8_t *sm) {
   constexpr int D = 64;
-  using B = Rec<64>;
+  constexpr uint32_t kSyncThreads = 64 + 32;  // state warps + issuer warp
+  using R = Rec<64>;
   using L = ScanSmem64<NB>;
-  uint8_t *SB = sm + L::SB;
   uint64_t *full = reinterpret_cast<uint64_t *>(sm + L::BAR);
-  uint64_t *mbar = full + 2;
+  uint64_t *empty = full + kS64Stages;
+  uint64_t *done = empty + kS64Stages;
+  uint64_t *ofree = done + kS64Acc;
   uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(sm + L::TMEMP);
+  uint32_t *abort_f = reinterpret_cast<uint32_t *>(sm + L::ABORT);
   WorkspaceHeader *hdr = reinterpret_cast<WorkspaceHeader *>(ws);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (warp >= 4) return;  // 128 threads on this path
-  const int bh = blockIdx.y, j0 = blockIdx.x * NB;
-  const int dv = D;
-  const uint8_t *rec0 = ws + sizeof(WorkspaceHeader) + (size_t)bh * NC * B::BYTES;
-  // Every thread waits on the same barriers; the chunk's hand-off barrier
-  // ORs the outcome of the waits so that all leave together after one gave
-  // up, and thread 0 then drains its last record copy and its products.
+  const int bh = blockIdx.y, blk = blockIdx.x, j0 = blk * NB;
+  const uint8_t *rec0 = ws + sizeof(WorkspaceHeader) + (size_t)bh * NC * R::BYTES;
+  // after a failed wait, as in the d = 128 scan: the abort word is set, the
+  // producer stops copying and drains its copies, the issuer drains its
+  // products, the other roles run out their loops without waiting
   bool ok = true;
-  int loads_issued = 0, commits = 0;  // thread 0's record copies and MMA commits
   auto fail = [&](unsigned where) {
     ok = false;
+    ptx::set_abort(abort_f);
     report_error(hdr, KDA_ERR_TIMEOUT, where);
   };
 
   if (tid == 0) {
-    ptx::mbar_init(&full[0], 1);
-    ptx::mbar_init(&full[1], 1);
-    ptx::mbar_init(mbar, 1);
+    for (int s = 0; s < kS64Stages; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 2);  // lane 0 of each state warp, once its products completed
+    }
+    for (int b = 0; b < kS64Acc; ++b) {
+      ptx::mbar_init(&done[b], 1);
+      ptx::mbar_init(&ofree[b], 2);  // lane 0 of each output warp
+    }
+    *abort_f = 0u;
     ptx::fence_mbar_init();
   }
   if (warp == 0) {
@@ -1644,181 +1668,164 @@ __device__ __forceinline__ void scan_d64(const float *h0, __nv_bfloat16 *__restr
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
-  ptx::named_barrier(1, 128);
+  __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_ptr;
-  const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
-  const uint32_t tS = t_lane;                       // state columns [0, NB)
-  const uint32_t tO = t_lane + (D == 128 ? NB : 0); // output columns (D = 64: same as state)
-  const bool state_row = (D == 128) || (tid < D);   // this thread's lane holds a state row
-  const int srow = tid;                              // key channel of that row
+  const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+  auto sb_of = [&](int chunk) { return sm + L::SB + (chunk & 1) * L::SB_BYTES; };
 
-  auto issue_loads = [&](int chunk, int s) {
-    uint8_t *st = sm + s * L::STAGE;
-    const uint8_t *rec = rec0 + (size_t)chunk * B::BYTES;
-    ptx::fence_proxy_async_smem();
-    ptx::mbar_arrive_expect_tx(&full[s], L::STAGE_BYTES);
-    ptx::bulk_g2s(st, rec, B::PRE, &full[s]);
-    ptx::bulk_g2s(st + B::PRE, rec + B::UT + (size_t)j0 * 128, NB * 128, &full[s]);
-    ptx::bulk_g2s(st + B::PRE + NB * 128, rec + B::GC, D * 4, &full[s]);
-  };
-
-  // initial state -> TMEM (rows that are not state rows get zeros)
-  {
-    const size_t s0 = (size_t)bh * D * dv;
-#pragma unroll
-    for (int cb = 0; cb < NB; cb += 16) {
-      float x[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        x[j] = (state_row && h0) ? h0[s0 + (size_t)srow * dv + j0 + cb + j] : 0.f;
-      ptx::tmem_st16(tS + cb, x);
+  if (warp == 4) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      int j = 0;
+      for (; j < NC; ++j) {
+        const int s = j % kS64Stages;
+        if (j >= kS64Stages && ok &&
+            !ptx::mbar_wait_fast(&empty[s], ((j / kS64Stages) - 1) & 1, kWaitLimit))
+          fail(0x410u);
+        if (!ok) break;
+        if (j + kPrefetchAhead < NC) {  // a later record into L2 (the shared part by one CTA)
+          const uint8_t *rp = rec0 + (size_t)(j + kPrefetchAhead) * R::BYTES;
+          if (blk == 0) ptx::prefetch_l2(rp, R::PRE);
+          ptx::prefetch_l2(rp + R::UT + (size_t)j0 * (kC * 2), NB * kC * 2);
+          ptx::prefetch_l2(rp + R::GC, D * 4);
+        }
+        uint8_t *st = sm + s * L::STAGE;
+        const uint8_t *rec = rec0 + (size_t)j * R::BYTES;
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive_expect_tx(&full[s], L::STAGE_BYTES);
+        ptx::bulk_g2s(st, rec, R::PRE, &full[s]);
+        ptx::bulk_g2s(st + L::UT_S, rec + R::UT + (size_t)j0 * (kC * 2), NB * kC * 2, &full[s]);
+        ptx::bulk_g2s(st + L::GC_S, rec + R::GC, D * 4, &full[s]);
+      }
+      if (!ok)  // drain (bounded): the copies still in flight (j were issued)
+        for (int i = j > kS64Stages ? j - kS64Stages : 0; i < j; ++i)
+          if (!ptx::mbar_wait(&full[i % kS64Stages], (i / kS64Stages) & 1, kWaitLimit)) break;
     }
-    ptx::tmem_st_wait();
-  }
-  if (tid == 0 && NC > 0) {
-    issue_loads(0, 0);
-    loads_issued = 1;
-  }
-  ptx::tc_fence_before();
-  ptx::named_barrier(1, 128);
-
-  auto store_o_rows = [&](int chunk) {
-    // D = 128: output rows sit in lanes 32w + (0..15) (M = 64 layout); D = 64: lanes 64..127.
-    const bool has = (D == 128) ? (lane < 16) : (tid >= D);
-    const int r = (D == 128) ? (warp * 16 + lane) : (tid - D);
-    const int t = chunk * kC + r;
+  } else if (warp == 5) {
+    // ---------------------------------------------------------- issuer
+    uint64_t dAs[kS64Stages], dKs[kS64Stages], dUs[kS64Stages], dSBs[2];
 #pragma unroll
-    for (int cb = 0; cb < NB; cb += 16) {
-      float x[16];
-      ptx::tmem_ld16(tO + cb, x);
+    for (int q = 0; q < kS64Stages; ++q) {
+      uint8_t *st = sm + q * L::STAGE;
+      dAs[q] = umma::sdesc(ptx::smem_u32(st + R::AP));   // [Ap; Qp]     128 rows, K = D
+      dKs[q] = umma::sdesc(ptx::smem_u32(st + R::KBT));  // [Kbar^T; M]  128 rows, K = C
+      dUs[q] = umma::sdesc(ptx::smem_u32(st + L::UT_S)); // U^T block    NB rows, K = C
+    }
+#pragma unroll
+    for (int q = 0; q < 2; ++q) dSBs[q] = umma::sdesc_mn(ptx::smem_u32(sb_of(q)), D, 0);
+    static_assert(kS64Stages == 3 && kS64Acc == 3, "six-chunk issuer period");
+    for (int i0 = 0; i0 < NC; i0 += 6)
+#pragma unroll
+    for (int u = 0; u < 6; ++u) {
+      const int i = i0 + u;
+      if (i >= NC) break;
+      const int b = u % kS64Acc;
+      const uint64_t dA = dAs[u % kS64Stages], dK = dKs[u % kS64Stages],
+                     dU = dUs[u % kS64Stages], dSB = dSBs[u & 1];
+      ptx::named_barrier(1, kSyncThreads);  // S_i written, record i landed, acc b free
+      if (lane == 0) {
+        ptx::tc_fence_after();
+        const uint32_t tA = tmem + NB * b;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)  // [Ap; Qp] S   (S read MN-major)
+          ptx::mma_bf16_ss(tA, dA + (uint64_t)((ks * 32) >> 4), dSB + (uint64_t)(ks * 2048 >> 4),
+                           umma::idesc_bf16_bmn(128, NB), ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < kC / 16; ++ks)  // + [Kbar^T; M] U
+          ptx::mma_bf16_ss(tA, dK + (uint64_t)((ks * 32) >> 4), dU + (uint64_t)((ks * 32) >> 4),
+                           umma::idesc_bf16(128, NB), 1);
+        ptx::mma_commit(&done[b]);
+      }
+      __syncwarp();
+    }
+    if (lane == 0 && ptx::aborted(abort_f)) {  // let this thread's MMAs finish before TMEM is freed
+      ptx::mma_commit(&done[0]);
+      ptx::mbar_wait(&done[0], ((NC + kS64Acc - 1) / kS64Acc) & 1, kWaitLimit);
+    }
+  } else if (warp >= 2) {
+    // ---------------------------------------------------------- output warps
+    const int row = (warp - 2) * 32 + lane;  // token row of the chunk (accumulator lane 64 + row)
+    for (int j = 0; j < NC; ++j) {
+      const int b = j % kS64Acc;
+      if (ok && !ptx::mbar_wait(&done[b], (j / kS64Acc) & 1, kWaitLimit)) fail(0x421u);
+      ptx::tc_fence_after();
+      float x[NB];
+      ptx::tmem_ld32(t_lane + NB * b, *reinterpret_cast<float(*)[32]>(x));
       ptx::tmem_ld_wait();
-      if (has && t < T) {
-        uint4 *dst = reinterpret_cast<uint4 *>(o + ((size_t)bh * T + t) * dv + j0 + cb);
-        uint4 a, b;
-        a.x = pack_bf16x2(x[0], x[1]); a.y = pack_bf16x2(x[2], x[3]);
-        a.z = pack_bf16x2(x[4], x[5]); a.w = pack_bf16x2(x[6], x[7]);
-        b.x = pack_bf16x2(x[8], x[9]); b.y = pack_bf16x2(x[10], x[11]);
-        b.z = pack_bf16x2(x[12], x[13]); b.w = pack_bf16x2(x[14], x[15]);
-        dst[0] = a;
-        dst[1] = b;
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&ofree[b]);
+      const int t = j * kC + row;
+      if (t < T) {
+        uint4 *dst = reinterpret_cast<uint4 *>(o + ((size_t)bh * T + t) * D + j0);
+#pragma unroll
+        for (int c8 = 0; c8 < NB / 8; ++c8) {
+          const float *v8 = x + 8 * c8;
+          dst[c8] = make_uint4(pack_bf16x2(v8[0], v8[1]), pack_bf16x2(v8[2], v8[3]),
+                               pack_bf16x2(v8[4], v8[5]), pack_bf16x2(v8[6], v8[7]));
+        }
       }
     }
-  };
-
-  for (int i = 0; i < NC; ++i) {
-    const int s = i & 1;
-    uint8_t *st = sm + s * L::STAGE;
-    if (i > 0 && ok && !ptx::mbar_wait(mbar, (i - 1) & 1, kWaitLimit)) fail(0x201u);
-    ptx::tc_fence_after();
-    if (tid == 0 && i + 1 < NC) {
-      issue_loads(i + 1, (i + 1) & 1);
-      loads_issued = i + 2;
-    }
-    if (ok && !ptx::mbar_wait(&full[s], (i >> 1) & 1, kWaitLimit)) fail(0x202u);
-    // state row: bf16 copy as the MMA operand, then scale by gamma_C in place
-    if (state_row) {
-      const float gam = reinterpret_cast<const float *>(st + B::PRE + NB * 128)[srow];
+  } else {
+    // ---------------------------------------------------------- state warps
+    const int r = tid;  // key row = accumulator lane
+    float sr[NB];
 #pragma unroll
-      for (int cb = 0; cb < NB; cb += 16) {
-        float x[16];
-        ptx::tmem_ld16(tS + cb, x);
+    for (int j = 0; j < NB; ++j) sr[j] = 0.f;
+    if (h0) {
+      const float4 *src = reinterpret_cast<const float4 *>(h0 + (size_t)bh * D * D + (size_t)r * D + j0);
+#pragma unroll
+      for (int j4 = 0; j4 < NB / 4; ++j4) {
+        const float4 a = src[j4];
+        sr[4 * j4] = a.x; sr[4 * j4 + 1] = a.y; sr[4 * j4 + 2] = a.z; sr[4 * j4 + 3] = a.w;
+      }
+    }
+    for (int i = 0; i < NC; ++i) {
+      const int s = i % kS64Stages, b = i % kS64Acc;
+      const uint8_t *st = sm + s * L::STAGE;
+      uint8_t *sb = sb_of(i);
+#pragma unroll
+      for (int c8 = 0; c8 < NB / 8; ++c8) st_chunk(sb, r, c8, D, sr + 8 * c8);
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      // record i landed (gamma_C is read below); accumulator b read by the
+      // output warps (chunk i - 3)
+      if (ok && !ptx::mbar_wait_fast(&full[s], (i / kS64Stages) & 1, kWaitLimit)) fail(0x404u);
+      if (r == 0 && i >= kS64Acc && ok &&
+          !ptx::mbar_wait_fast(&ofree[b], ((i / kS64Acc) - 1) & 1, kWaitLimit))
+        fail(0x422u);
+      __syncwarp();
+      ptx::named_arrive(1, kSyncThreads);
+      const float gam = reinterpret_cast<const float *>(st + L::GC_S)[r];
+#pragma unroll
+      for (int j = 0; j < NB; ++j) sr[j] *= gam;  // gamma_C S while the products run
+      if (ok && !ptx::mbar_wait(&done[b], (i / kS64Acc) & 1, kWaitLimit)) fail(0x401u);
+      ptx::tc_fence_after();
+      {
+        float x[NB];
+        ptx::tmem_ld32(t_lane + NB * b, *reinterpret_cast<float(*)[32]>(x));
         ptx::tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          st_bf16(SB, umma::sw128_off(cb + j, srow, NB), x[j]);
-          x[j] *= gam;
-        }
-        ptx::tmem_st16(tS + cb, x);
+        for (int j = 0; j < NB; ++j) sr[j] += x[j];  // + Ap S + Kbar^T U
       }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&empty[s]);  // the products and this warp's reads are done
     }
-    if (i > 0) store_o_rows(i - 1);
-    if (D == 64 && !state_row) {  // output lanes restart from zero each chunk
-      float z[16];
+    if (hT) {
+      float4 *dst = reinterpret_cast<float4 *>(hT + (size_t)bh * D * D + (size_t)r * D + j0);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) z[j] = 0.f;
-#pragma unroll
-      for (int cb = 0; cb < NB; cb += 16) ptx::tmem_st16(tO + cb, z);
+      for (int j4 = 0; j4 < NB / 4; ++j4)
+        dst[j4] = make_float4(sr[4 * j4], sr[4 * j4 + 1], sr[4 * j4 + 2], sr[4 * j4 + 3]);
     }
-    ptx::tmem_st_wait();
-    ptx::fence_proxy_async_smem();
-    ptx::tc_fence_before();
-    if (ptx::named_barrier_or(1, 128, !ok)) break;  // a wait gave up
-    if (tid == 0) {
-      ptx::tc_fence_after();
-      const uint32_t sAP = ptx::smem_u32(st + B::AP), sQP = ptx::smem_u32(st + B::QP);
-      const uint32_t sKB = ptx::smem_u32(st + B::KBT), sMM = ptx::smem_u32(st + B::MM);
-      const uint32_t sUT = ptx::smem_u32(st + B::PRE), sSB = ptx::smem_u32(SB);
-      if (D == 128) {
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          ptx::mma_bf16_ss(tmem, umma::sdesc_k(sAP, D, ks), umma::sdesc_k(sSB, NB, ks),
-                           umma::idesc_bf16(128, NB), 1);
-#pragma unroll
-        for (int ks = 0; ks < kC / 16; ++ks)
-          ptx::mma_bf16_ss(tmem, umma::sdesc_k(sKB, D, ks), umma::sdesc_k(sUT, NB, ks),
-                           umma::idesc_bf16(128, NB), 1);
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)  // Qp is stored transposed: MN-major A
-          ptx::mma_bf16_ss(tmem + NB, umma::sdesc_mn(sQP, D, ks), umma::sdesc_k(sSB, NB, ks),
-                           umma::idesc_bf16_amn(64, NB), ks > 0);
-#pragma unroll
-        for (int ks = 0; ks < kC / 16; ++ks)
-          ptx::mma_bf16_ss(tmem + NB, umma::sdesc_k(sMM, kC, ks), umma::sdesc_k(sUT, NB, ks),
-                           umma::idesc_bf16(64, NB), 1);
-      } else {
-        // [Ap; Qp] and [Kbar^T; M] are adjacent 64-row tiles: one M = 128 operand each
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          ptx::mma_bf16_ss(tmem, umma::sdesc_k(sAP, 128, ks), umma::sdesc_k(sSB, NB, ks),
-                           umma::idesc_bf16(128, NB), 1);
-#pragma unroll
-        for (int ks = 0; ks < kC / 16; ++ks)
-          ptx::mma_bf16_ss(tmem, umma::sdesc_k(sKB, 128, ks), umma::sdesc_k(sUT, NB, ks),
-                           umma::idesc_bf16(128, NB), 1);
-      }
-      ptx::mma_commit(mbar);
-      ++commits;
-    }
-  }
-
-  // epilogue: last chunk's output, final state
-  if (NC > 0) {
-    if (ok && !ptx::mbar_wait(mbar, (NC - 1) & 1, kWaitLimit)) fail(0x203u);
-    ptx::tc_fence_after();
-    store_o_rows(NC - 1);
-  }
-  if (hT) {
-    const size_t s0 = (size_t)bh * D * dv;
-#pragma unroll
-    for (int cb = 0; cb < NB; cb += 16) {
-      float x[16];
-      ptx::tmem_ld16(tS + cb, x);
-      ptx::tmem_ld_wait();
-      if (state_row) {
-        float4 *dst = reinterpret_cast<float4 *>(hT + s0 + (size_t)srow * dv + j0 + cb);
-#pragma unroll
-        for (int j4 = 0; j4 < 4; ++j4)
-          dst[j4] = make_float4(x[4 * j4], x[4 * j4 + 1], x[4 * j4 + 2], x[4 * j4 + 3]);
-      }
-    }
-  }
-  if (tid == 0 && !ok) {  // drain (bounded): the last copy, the products
-    if (loads_issued > 0) {
-      const int j = loads_issued - 1;
-      ptx::mbar_wait(&full[j & 1], (j >> 1) & 1, kWaitLimit);
-    }
-    ptx::mma_commit(mbar);
-    ptx::mbar_wait(mbar, commits & 1, kWaitLimit);
   }
   ptx::tc_fence_before();
-  ptx::named_barrier(1, 128);
+  __syncthreads();
   if (warp == 0) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, L::TMEM_COLS);
   }
 }
-
 
 // D = 128, one CTA per (batch, head) holding all 128 value columns ("wide"
 // scan, KDA_PATH_TENSOR_WIDE_SCAN).  The value-column split above gives a
@@ -2205,7 +2212,7 @@ kda_status launch_d(const void *q, const void *k, const void *v, const float *be
     kda_scan_wide_kernel<<<BH, kWideThreads, wide_smem, st>>>(
         h0, static_cast<__nv_bfloat16 *>(o), hT, T, NC, ws);
   else
-    scan<<<dim3(D / NB, BH), D == 128 ? kScan128Threads : 128, scan_smem, st>>>(
+    scan<<<dim3(D / NB, BH), D == 128 ? kScan128Threads : kScan64Threads, scan_smem, st>>>(
         h0, static_cast<__nv_bfloat16 *>(o), hT, T, NC, ws);
   timer.mark();
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
