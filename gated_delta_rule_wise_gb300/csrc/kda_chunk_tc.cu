@@ -1069,13 +1069,19 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
     // ---- (8) lane = key channel: Ap = -gamma_C (K/gamma)^T W (warps 0-3),
     // B = gamma_C (K/gamma)^T U (warps 4-7).  A warp's rows form contiguous
     // pieces of the record (4 KB of Ap per K atom, 2 KB of B per 32-column
-    // block): each piece is assembled in a per-warp staging slot (the consumed
-    // K/gamma rows, the T tile) and leaves with 512-byte coalesced stores.
+    // block): each piece is assembled in one of two staging slots of the warp
+    // (shared memory no longer needed by this chunk: the consumed K/gamma rows,
+    // the T tile, A's and T's float space past the M tile) and handed by lane 0
+    // to a bulk store, so no warp waits for its global writes; a slot is
+    // written again only after its earlier store has read it, and all stores
+    // have read their slots before the next chunk's rows land there (after
+    // (9)).  Copied out by the warps themselves, the 64 KB took about a
+    // microsecond of this phase.
     {
       const int key = quarter * 32 + lane;
       const float gk = colhalf == 0 ? -gcs[key] : gcs[key];
       if (colhalf == 0) {
-        uint8_t *stg = X1 + 32768 + (quarter >> 1) * 16384 + kC * 128 + (quarter & 1) * 4096;
+        uint8_t *slots = quarter < 2 ? X1 + 40960 + quarter * 16384 : sm + L::RA + 8192 * (quarter - 1);
 #pragma unroll 1
         for (int a = 0; a < 2; ++a) {
           float x[64];
@@ -1089,19 +1095,19 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
           }
 #pragma unroll
           for (int j = 0; j < 64; ++j) x[j] *= gk;
+          uint8_t *stg = slots + a * 4096;
 #pragma unroll
           for (int j8 = 0; j8 < 8; ++j8)  // same swizzle as the record tile (rows 32q + lane)
             *reinterpret_cast<uint4 *>(stg + lane * 128 + ((j8 ^ (lane & 7)) << 4)) = pack8(x + 8 * j8);
+          ptx::fence_proxy_async_smem();
           __syncwarp();
-          uint8_t *dst = recg + Rr::AP + a * (D * 128) + quarter * 4096;
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            *reinterpret_cast<uint4 *>(dst + i * 512 + lane * 16) =
-                *reinterpret_cast<const uint4 *>(stg + i * 512 + lane * 16);
-          __syncwarp();
+          if (lane == 0) {
+            ptx::bulk_s2g(recg + Rr::AP + a * (D * 128) + quarter * 4096, stg, 4096);
+            ptx::bulk_commit();
+          }
         }
       } else {
-        uint8_t *stg = TT + quarter * 2048;
+        uint8_t *slots = quarter < 2 ? TT + quarter * 4096 : sm + L::RA + 24576 + (quarter - 2) * 4096;
 #pragma unroll 1
         for (int h2 = 0; h2 < 2; ++h2) {
           float x[64];
@@ -1112,16 +1118,20 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
           for (int j = 0; j < 64; ++j) x[j] *= gk;
 #pragma unroll
           for (int hb = 0; hb < 2; ++hb) {
+            uint8_t *stg = slots + hb * 2048;
+            if (h2 == 1) {  // this slot's store (piece hb of h2 = 0) has read it
+              if (lane == 0) ptx::bulk_wait_read<1>();
+              __syncwarp();
+            }
 #pragma unroll
             for (int j8 = 0; j8 < 4; ++j8)  // record layout: rotated chunks (conflict-free writes)
               *reinterpret_cast<uint4 *>(stg + rotated_chunk(lane, j8)) = pack8(x + 32 * hb + 8 * j8);
+            ptx::fence_proxy_async_smem();
             __syncwarp();
-            uint8_t *dst = recg + Rr::BI + (h2 * 2 + hb) * (128 * 64) + quarter * 2048;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              *reinterpret_cast<uint4 *>(dst + i * 512 + lane * 16) =
-                  *reinterpret_cast<const uint4 *>(stg + i * 512 + lane * 16);
-            __syncwarp();
+            if (lane == 0) {
+              ptx::bulk_s2g(recg + Rr::BI + (h2 * 2 + hb) * (128 * 64) + quarter * 2048, stg, 2048);
+              ptx::bulk_commit();
+            }
           }
         }
       }
@@ -1140,7 +1150,10 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
       ptx::mma_commit(bar);
     }
     wait_mma(0x104u);
-    // A's space and blocks 2-3 are free: fetch the next chunk's log_alpha, k, v
+    // A's space and blocks 2-3 are free once the record stores of (8) have read
+    // their slots there: fetch the next chunk's log_alpha, k, v
+    if (lane == 0) ptx::bulk_wait_read<0>();
+    __syncthreads();
     if (has_next) {
       if (tid == 0) issue_lkv(idx_next);
       if (tid < kC) b_next = beta_of(idx_next);
@@ -1224,6 +1237,7 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
     }
     if (tid == 0 && has_next) issue_q(idx_next);
   }
+  if (lane == 0) ptx::bulk_wait_all();  // this warp's record stores complete
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 0) {
