@@ -608,7 +608,8 @@ __device__ __forceinline__ void prep_d64(const __nv_bfloat16 *__restrict__ q,
 //  (9) M [W | U]                                        4 MMAs (M = 64, N = 256)
 // (10) Qp = Q*gamma - M W and O = M U to the record.
 // Each warp assembles its contiguous pieces of the record tiles in staging
-// slots of consumed shared memory and stores them with coalesced writes.
+// slots of consumed shared memory, and bulk stores copy them out while the
+// CTA goes on.
 // The next chunk's input rows are prefetched into L2 during (5); its log_alpha,
 // k and v rows are bulk-copied as soon as the last product has read A's space
 // and blocks 2-3 (after (9)), its q rows after (10).
@@ -894,6 +895,9 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
       rk[m] = in ? *reinterpret_cast<const uint4 *>(rawk + off) : make_uint4(0u, 0u, 0u, 0u);
       rv[m] = in ? *reinterpret_cast<const uint4 *>(rawv + off) : make_uint4(0u, 0u, 0u, 0u);
     }
+    // the previous chunk's Qp and O stores have read their slots in block 1
+    // and the T tile before the tiles below overwrite block 1
+    if (lane == 0) ptx::bulk_wait_read<0>();
     __syncthreads();
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
@@ -1161,9 +1165,15 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
 
     // ---- (10) token rows: Qp = Q*gamma - M W (warps 0-3), O = M U (warps 4-7).
     // M = 64 layout read as in (6): threads 0-15 hold columns 0-63 of the
-    // warp's 16 rows, threads 16-31 columns 64-127.  Staged per warp (the
-    // consumed W rows, the T tile) as in (8): Qp as two 2 KB pieces (one per
-    // K atom), O as 1 KB pieces (one per 32-column block).
+    // warp's 16 rows, threads 16-31 columns 64-127.  As in (8) each warp
+    // assembles contiguous record pieces in staging slots and lane 0 hands
+    // them to bulk stores.  Qp: one 2 KB piece per K atom, K atom 0 in the
+    // consumed W rows of block 1 and K atom 1 in place over the warp's own
+    // Q*gamma rows of block 1 (each thread rewrites the 16 bytes it read);
+    // both stay untouched until the next chunk's tiles.  O: two 1 KB pieces
+    // per 32-column block, block hb + 1 first into block 0's consumed W rows
+    // (the next chunk's q rows land there after this phase, so that store
+    // is waited for here), block hb into the T tile.
     {
       const int rr = quarter * 16 + (lane & 15), side = lane >> 4, row = lane & 15;
       float x[64];
@@ -1176,7 +1186,8 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
           reinterpret_cast<float *>(nrm0 + (size_t)idx * NormRec::BYTES + NormRec::MR)[rr] = x[0];
           x[0] = 0.f;
         }
-        uint8_t *stg = X1 + (quarter >> 1) * 16384 + (quarter & 1) * 4096;  // 4 KB
+        uint8_t *const qslot = X1 + 16384 + quarter * 2048;  // K atom a at + a * 8192
+        uint8_t *stg = qslot + side * 8192;
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {  // this thread's K atom is `side`
           float qg[8];
@@ -1186,35 +1197,36 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
           const float gm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
 #pragma unroll
           for (int j = 0; j < 8; ++j) qg[j] = qg[j] * gm[j] - x[8 * cc + j];
-          *reinterpret_cast<uint4 *>(stg + side * 2048 + row * 128 + ((cc ^ (row & 7)) << 4)) =
-              pack8(qg);
+          *reinterpret_cast<uint4 *>(stg + row * 128 + ((cc ^ (row & 7)) << 4)) = pack8(qg);
         }
+        ptx::fence_proxy_async_smem();
         __syncwarp();
+        if (lane == 0) {
 #pragma unroll
-        for (int a = 0; a < 2; ++a) {
-          uint8_t *dst = recg + Rr::QP + a * (kC * 128) + quarter * 2048;
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            *reinterpret_cast<uint4 *>(dst + i * 512 + lane * 16) =
-                *reinterpret_cast<const uint4 *>(stg + a * 2048 + i * 512 + lane * 16);
+          for (int a = 0; a < 2; ++a)
+            ptx::bulk_s2g(recg + Rr::QP + a * (kC * 128) + quarter * 2048, qslot + a * 8192, 2048);
+          ptx::bulk_commit();
         }
       } else {
-        uint8_t *stg = TT + quarter * 2048;  // two 1 KB pieces: blocks hb (side 0), hb + 2 (side 1)
 #pragma unroll
-        for (int hb = 0; hb < 2; ++hb) {
+        for (int i = 0; i < 2; ++i) {
+          const int hb = 1 - i;
+          uint8_t *stg = i == 0 ? X1 + quarter * 2048 : TT + quarter * 2048;
 #pragma unroll
           for (int j8 = 0; j8 < 4; ++j8)  // record layout: rotated chunks (conflict-free writes)
             *reinterpret_cast<uint4 *>(stg + side * 1024 + rotated_chunk(row, j8)) =
                 pack8(x + 32 * hb + 8 * j8);
+          ptx::fence_proxy_async_smem();
           __syncwarp();
+          if (lane == 0) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int p = i * 512 + lane * 16, piece = p >> 10;
-            *reinterpret_cast<uint4 *>(recg + Rr::OI + (hb + 2 * piece) * (kC * 64) + quarter * 1024 +
-                                       (p & 1023)) = *reinterpret_cast<const uint4 *>(stg + p);
+            for (int piece = 0; piece < 2; ++piece)
+              ptx::bulk_s2g(recg + Rr::OI + (hb + 2 * piece) * (kC * 64) + quarter * 1024,
+                            stg + piece * 1024, 1024);
+            ptx::bulk_commit();
           }
-          __syncwarp();
         }
+        if (lane == 0) ptx::bulk_wait_read<1>();  // the piece in block 0 has been read
       }
     }
     // block 0 and the TMEM columns are free again: fetch the next chunk's q
