@@ -30,7 +30,7 @@ __all__ = [
     "chunk_fwd", "decode_step", "workspace_for",
     "KDA_F32", "KDA_BF16", "KDA_ALPHA_NONE", "KDA_ALPHA_SCALAR", "KDA_ALPHA_CHANNEL",
     "KDA_PATH_AUTO", "KDA_PATH_CUDA_CORE", "KDA_PATH_TENSOR", "KDA_PATH_TENSOR_SPLIT_SCAN",
-    "KDA_PATH_TENSOR_WIDE_SCAN",
+    "KDA_PATH_TENSOR_WIDE_SCAN", "KDA_PATH_TENSOR_PIPELINED",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -39,7 +39,7 @@ KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT 
 KDA_F32, KDA_BF16 = 0, 1
 KDA_ALPHA_NONE, KDA_ALPHA_SCALAR, KDA_ALPHA_CHANNEL = 0, 1, 2
 KDA_PATH_AUTO, KDA_PATH_CUDA_CORE, KDA_PATH_TENSOR = 0, 1, 2
-KDA_PATH_TENSOR_SPLIT_SCAN, KDA_PATH_TENSOR_WIDE_SCAN = 3, 4
+KDA_PATH_TENSOR_SPLIT_SCAN, KDA_PATH_TENSOR_WIDE_SCAN, KDA_PATH_TENSOR_PIPELINED = 3, 4, 5
 ABI_VERSION = 1
 
 _lib = None

@@ -22,15 +22,17 @@ kda_status check_chunk_shape(int B, int H, int T, int dk, int dv, int C, kda_dty
   if (B < 0 || H < 0 || T < 0) return KDA_ERR_INVALID_ARG;
   if (!valid_dtype(dt) || !valid_alpha(am)) return KDA_ERR_INVALID_ARG;
   if (path != KDA_PATH_AUTO && path != KDA_PATH_CUDA_CORE && path != KDA_PATH_TENSOR &&
-      path != KDA_PATH_TENSOR_SPLIT_SCAN && path != KDA_PATH_TENSOR_WIDE_SCAN)
+      path != KDA_PATH_TENSOR_SPLIT_SCAN && path != KDA_PATH_TENSOR_WIDE_SCAN &&
+      path != KDA_PATH_TENSOR_PIPELINED)
     return KDA_ERR_INVALID_ARG;
   if (!is_pow2_dim(dk) || !is_pow2_dim(dv)) return KDA_ERR_UNSUPPORTED;
   if (C != 16 && C != 32 && C != 64) return KDA_ERR_UNSUPPORTED;
   if ((long long)B * H > 65535) return KDA_ERR_UNSUPPORTED;
   const bool tensor_only = path == KDA_PATH_TENSOR || path == KDA_PATH_TENSOR_SPLIT_SCAN ||
-                           path == KDA_PATH_TENSOR_WIDE_SCAN;
+                           path == KDA_PATH_TENSOR_WIDE_SCAN || path == KDA_PATH_TENSOR_PIPELINED;
   if (tensor_only && !chunk_tc_supported(dk, dv, C, dt)) return KDA_ERR_UNSUPPORTED;
-  if (path == KDA_PATH_TENSOR_WIDE_SCAN && dk != 128) return KDA_ERR_UNSUPPORTED;
+  if ((path == KDA_PATH_TENSOR_WIDE_SCAN || path == KDA_PATH_TENSOR_PIPELINED) && dk != 128)
+    return KDA_ERR_UNSUPPORTED;
   return KDA_OK;
 }
 
@@ -39,9 +41,15 @@ bool use_tensor(int dk, int dv, int C, kda_dtype dt, kda_path path) {
   return chunk_tc_supported(dk, dv, C, dt);
 }
 
-// Scan choice handed to the tensor path: 0 automatic, 1 split, 2 wide.
+// Scan choice handed to the tensor path: 0 automatic, 1 split, 2 wide,
+// 3 pipelined.
 int scan_choice(kda_path path) {
-  return path == KDA_PATH_TENSOR_SPLIT_SCAN ? 1 : (path == KDA_PATH_TENSOR_WIDE_SCAN ? 2 : 0);
+  switch (path) {
+    case KDA_PATH_TENSOR_SPLIT_SCAN: return 1;
+    case KDA_PATH_TENSOR_WIDE_SCAN: return 2;
+    case KDA_PATH_TENSOR_PIPELINED: return 3;
+    default: return 0;
+  }
 }
 
 size_t workspace_bytes(int B, int H, int T, int dk, int dv, int C, kda_dtype dt,
@@ -112,7 +120,7 @@ int kda_chunk_fwd_launches(int B, int H, int T, int dk, int dv, int C, kda_dtype
   if (check_chunk_shape(B, H, T, dk, dv, C, dt, am, path) != KDA_OK) return -1;
   const int BH = B * H;
   // hT present is the worst case (an empty sequence still copies h0 -> hT)
-  return use_tensor(dk, dv, C, dt, path) ? chunk_tc_launches(BH, T, true)
+  return use_tensor(dk, dv, C, dt, path) ? chunk_tc_launches(BH, T, true, dk, 0, scan_choice(path))
                                          : chunk_ffma_launches(BH, T, true);
 }
 
@@ -135,7 +143,7 @@ kda_status kda_chunk_fwd_ex(const void *q, const void *k, const void *v, const f
   if (st != KDA_OK) return st;
   if (n_events < 0 || (n_events > 0 && !events)) return KDA_ERR_INVALID_ARG;
   const bool tensor = use_tensor(dk, dv, C, dt, path);
-  const int launches = tensor ? chunk_tc_launches(B * H, T, hT != nullptr)
+  const int launches = tensor ? chunk_tc_launches(B * H, T, hT != nullptr, dk, 0, scan_choice(path))
                               : chunk_ffma_launches(B * H, T, hT != nullptr);
   if (n_events > 0 && n_events < launches + 1) return KDA_ERR_INVALID_ARG;
 
@@ -190,7 +198,7 @@ kda_status kda_chunk_fwd_rule(const void *q, const void *k, const void *v, const
   if (!workspace || !aligned256(workspace)) return KDA_ERR_INVALID_ARG;
   if (ws_bytes < workspace_bytes(B, H, T, dk, dv, C, dt, am, KDA_PATH_TENSOR))
     return KDA_ERR_INVALID_ARG;
-  if (chunk_tc_launches(B * H, T, hT != nullptr) == 0) return KDA_OK;
+  if (chunk_tc_launches(B * H, T, hT != nullptr, dk, (int)rule, 0) == 0) return KDA_OK;
   LaunchTimer timer;
   timer.s = reinterpret_cast<cudaStream_t>(stream);
   return launch_chunk_tc(q, k, v, beta, log_alpha, h0, o, hT, B, H, T, dk, dv, C, am, workspace,

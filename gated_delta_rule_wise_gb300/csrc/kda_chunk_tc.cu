@@ -648,6 +648,7 @@ struct PrepSmem128 {
   static constexpr uint32_t LBAR = BAR + 8;   // log_alpha, k, v rows landed
   static constexpr uint32_t QBAR = LBAR + 8;  // q rows landed
   static constexpr uint32_t TMEMP = QBAR + 8;
+  static constexpr uint32_t NEXT = TMEMP + 4;  // the CTA's next work item
   static constexpr uint32_t BYTES = TMEMP + 8;
   static constexpr uint32_t TMEM_COLS = 256;
   static_assert(kC * D * 4 <= 2 * kC * kLD * 4 && EG_PLANE + kC * (D / 2) * 4 <= 2 * kC * kLD * 4,
@@ -686,8 +687,9 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
                                           const __nv_bfloat16 *__restrict__ v,
                                           const float *__restrict__ beta,
                                           const float *__restrict__ log_alpha, int alpha_mode,
-                                          int T, int NC, int total, uint8_t *__restrict__ ws,
-                                          uint8_t *sm, int rule, unsigned maps) {
+                                          int T, int NC, int total, int n0, int nseg, int work,
+                                          unsigned *ctr, uint8_t *__restrict__ ws, uint8_t *sm,
+                                          int rule, unsigned maps) {
   constexpr int D = 128;
   constexpr bool kGeneral = kMode != 0, kExt = kMode == 2;
   using Rr = Rec<128>;
@@ -706,6 +708,7 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
   uint64_t *lbar = reinterpret_cast<uint64_t *>(sm + L::LBAR);
   uint64_t *qbar = reinterpret_cast<uint64_t *>(sm + L::QBAR);
   uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(sm + L::TMEMP);
+  int *next_s = reinterpret_cast<int *>(sm + L::NEXT);
   WorkspaceHeader *hdr = reinterpret_cast<WorkspaceHeader *>(ws);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -721,6 +724,9 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
   };
 
   constexpr bool la_bulk = !kRowDecay;  // per-channel log_alpha rows (512 B each), bulk-copied
+  // The grid's work items are chunks n0 .. n0 + nseg - 1 of every head (all
+  // chunks when n0 = 0 and nseg = NC); item l is record (head, chunk) of index
+  auto chunk_of = [&](int l) { return (l / nseg) * NC + n0 + l % nseg; };
   auto rows_of = [&](int idx, int &valid, size_t &row0) {
     const int t0 = (idx % NC) * kC;
     valid = min(kC, T - t0);
@@ -773,9 +779,9 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
   const uint32_t sX1 = ptx::smem_u32(X1), sTT = ptx::smem_u32(TT), sMM = ptx::smem_u32(MM);
   const uint32_t sWU = sX1;                          // [W | U]: rows 0-63 of the four blocks
   const uint32_t sKH = sX1 + 32768 + kC * 128;       // K/gamma: rows 64-127 of blocks 2-3
-  if (tid == 0 && (int)blockIdx.x < total) {
-    issue_lkv(blockIdx.x);
-    issue_q(blockIdx.x);
+  if (tid == 0 && (int)blockIdx.x < work) {
+    issue_lkv(chunk_of(blockIdx.x));
+    issue_q(chunk_of(blockIdx.x));
   }
   if constexpr (!kGeneral) {
     rule = KDA_RULE_DELTA;
@@ -794,7 +800,7 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
     return (maps & KDA_MAP_BETA_SIGMOID) ? 1.f / (1.f + __expf(-b)) : b;
   };
   float b_next = 0.f;  // beta of the next chunk's row tid (tid < C)
-  if ((int)blockIdx.x < total && tid < kC) b_next = beta_of(blockIdx.x);
+  if ((int)blockIdx.x < work && tid < kC) b_next = beta_of(chunk_of(blockIdx.x));
   uint32_t mma_phase = 0;
 
   auto wait_mma = [&](unsigned code) {
@@ -809,15 +815,22 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
     ptx::tc_fence_after();
   };
 
-  for (int idx = blockIdx.x, it = 0; idx < total; idx += gridDim.x, ++it) {
+  // Work items: the CTA's first is its index; each later one is claimed from
+  // a counter (zero at the call's start), so that the two CTAs of an SM,
+  // which do not run at the same speed (the older one's warps win the issue
+  // slots), finish within a chunk of each other.  The claim for the next
+  // item goes out at the top of a chunk and is read after the decay phase.
+  int l = blockIdx.x;
+  for (int it = 0; l < work; ++it) {
+    int claimed = 0;
+    if (tid == 0) claimed = (int)gridDim.x + (int)atomicAdd(ctr, 1u);
+    const int idx = chunk_of(l);
     const int n = idx % NC;
     const int t0 = n * kC;
     const int valid = min(kC, T - t0);
     const size_t row0 = (size_t)(idx / NC) * T + t0;
     uint8_t *recg = ws + sizeof(WorkspaceHeader) + (size_t)idx * Rr::BYTES;
 
-    const int idx_next = idx + (int)gridDim.x;
-    const bool has_next = idx_next < total;
 
     // ---- (0) decay
     if (tid < kC) betas[tid] = b_next;
@@ -879,8 +892,12 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
         reinterpret_cast<float *>(recg + Rr::GC)[tid] = __expf(p0 + p1);
       }
     }
+    if (tid == 0) *next_s = claimed;
     if (ok && !ptx::mbar_wait(qbar, it & 1, kWaitLimit)) fail(0x105u);
     __syncthreads();
+    const int l_next = *next_s;
+    const bool has_next = l_next < work;
+    const int idx_next = has_next ? chunk_of(l_next) : 0;
 
     // ---- (1) decayed tiles, one thread per (row, 8 channels): raw rows to
     // registers first (the tiles overwrite them), rows past the end as zeros
@@ -1248,6 +1265,7 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
       break;
     }
     if (tid == 0 && has_next) issue_q(idx_next);
+    l = l_next;
   }
   if (lane == 0) ptx::bulk_wait_all();  // this warp's record stores complete
   ptx::tc_fence_before();
@@ -1258,20 +1276,32 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
   }
 }
 
+// n0, nseg, work: the chunk range of a pipelined call (d = 128; the d = 64
+// prep always takes every chunk, n0 = 0, nseg = NC, work = total, in a fixed
+// order: one CTA per SM).  ctr: the d = 128 prep's work counter, zero when
+// the grid starts.  Launched
+// as a programmatic dependent of the previous scan segment, a CTA starts
+// while that scan still runs (its inputs and records are disjoint from the
+// scan's) and waits for the scan only before it exits, so that the prep's
+// completion implies the earlier scan's and the next scan segment, which
+// waits for this grid, sees that scan's final state.
 template <int D, int kMode, bool kRowDecay>
 __global__ void __launch_bounds__(256, D == 128 ? 2 : 1)
 kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                 const __nv_bfloat16 *__restrict__ v, const float *__restrict__ beta,
                 const float *__restrict__ log_alpha, int alpha_mode, int T, int NC, int total,
-                uint8_t *__restrict__ ws, int rule, unsigned maps) {
+                int n0, int nseg, int work, unsigned *ctr, uint8_t *__restrict__ ws, int rule,
+                unsigned maps) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));
+  ptx::grid_dep_launch();
   if constexpr (D == 128)
-    prep_d128<kMode, kRowDecay>(q, k, v, beta, log_alpha, alpha_mode, T, NC, total, ws, sm, rule,
-                                maps);
+    prep_d128<kMode, kRowDecay>(q, k, v, beta, log_alpha, alpha_mode, T, NC, total, n0, nseg,
+                                work, ctr, ws, sm, rule, maps);
   else
     prep_d64(q, k, v, beta, log_alpha, alpha_mode, T, NC, total, ws, sm);
+  ptx::grid_dep_wait();
 }
 
 // ============================================================== scan kernel
@@ -1357,7 +1387,7 @@ struct ScanSmem128 {
 // hT after the last, so neither pointer is declared __restrict__.
 template <int NB, bool kNorm>
 __device__ __forceinline__ void scan_d128(const float *h0, __nv_bfloat16 *__restrict__ o,
-                                          float *hT, int T, int NC,
+                                          float *hT, int T, int NC, int NCh, int n0,
                                           uint8_t *__restrict__ ws, uint8_t *sm) {
   constexpr int D = 128;
   constexpr uint32_t kSyncThreads = 128 + 32;  // state warps + issuer warp
@@ -1378,9 +1408,9 @@ __device__ __forceinline__ void scan_d128(const float *h0, __nv_bfloat16 *__rest
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.y, blk = blockIdx.x, j0 = blk * NB;
-  const uint8_t *rec0 = ws + sizeof(WorkspaceHeader) + (size_t)bh * NC * R::BYTES;
-  const uint8_t *nrm0 = ws + sizeof(WorkspaceHeader) + (size_t)gridDim.y * NC * R::BYTES +
-                        (size_t)bh * NC * NormRec::BYTES;
+  const uint8_t *rec0 = ws + sizeof(WorkspaceHeader) + ((size_t)bh * NCh + n0) * R::BYTES;
+  const uint8_t *nrm0 = ws + sizeof(WorkspaceHeader) + (size_t)gridDim.y * NCh * R::BYTES +
+                        ((size_t)bh * NCh + n0) * NormRec::BYTES;
   // A wait that gives up records the error, sets the CTA's abort word and
   // makes its thread skip its later waits.  The producer then stops copying
   // and waits (bounded) for the copies it started; the issuer, which waits
@@ -1517,7 +1547,7 @@ __device__ __forceinline__ void scan_d128(const float *h0, __nv_bfloat16 *__rest
       ptx::tc_fence_after();
       const uint32_t tO = t_lane + NB + kOW * b;
       const uint8_t *oi = sm + s * L::STAGE + L::OI_S;
-      const int t = j * kC + orow;
+      const int t = (n0 + j) * kC + orow;
       float inv_den = 1.f;
       if (norm) {  // denominator: (Qp z)_t from column NB plus the row sum of M
         float qz;
@@ -1650,7 +1680,7 @@ __device__ __forceinline__ void scan_d128(const float *h0, __nv_bfloat16 *__rest
 
 template <int NB>
 __device__ __forceinline__ void scan_d64(const float *h0, __nv_bfloat16 *__restrict__ o,
-                                         float *hT, int T, int NC,
+                                         float *hT, int T, int NC, int NCh, int n0,
                                          uint8_t *__restrict__ ws, uint8_t *sm) {
   constexpr int D = 64;
   constexpr uint32_t kSyncThreads = 64 + 32;  // state warps + issuer warp
@@ -1666,7 +1696,7 @@ __device__ __forceinline__ void scan_d64(const float *h0, __nv_bfloat16 *__restr
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.y, blk = blockIdx.x, j0 = blk * NB;
-  const uint8_t *rec0 = ws + sizeof(WorkspaceHeader) + (size_t)bh * NC * R::BYTES;
+  const uint8_t *rec0 = ws + sizeof(WorkspaceHeader) + ((size_t)bh * NCh + n0) * R::BYTES;
   // after a failed wait, as in the d = 128 scan: the abort word is set, the
   // producer stops copying and drains its copies, the issuer drains its
   // products, the other roles run out their loops without waiting
@@ -1782,7 +1812,7 @@ __device__ __forceinline__ void scan_d64(const float *h0, __nv_bfloat16 *__restr
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&ofree[b]);
-      const int t = j * kC + row;
+      const int t = (n0 + j) * kC + row;
       if (t < T) {
         uint4 *dst = reinterpret_cast<uint4 *>(o + ((size_t)bh * T + t) * D + j0);
 #pragma unroll
@@ -1914,7 +1944,7 @@ __device__ __forceinline__ void load_row_blocks(const uint8_t *blocks, int rows,
 }
 
 __device__ __forceinline__ void scan_wide_d128(const float *h0, __nv_bfloat16 *__restrict__ o,
-                                               float *hT, int T, int NC,
+                                               float *hT, int T, int NC, int NCh, int n0,
                                                uint8_t *__restrict__ ws, uint8_t *sm) {
   constexpr int D = 128;
   constexpr uint32_t kSyncThreads = 256 + 32;  // state warps + issuer warp
@@ -1932,7 +1962,7 @@ __device__ __forceinline__ void scan_wide_d128(const float *h0, __nv_bfloat16 *_
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.x;
-  const uint8_t *rec0 = ws + sizeof(WorkspaceHeader) + (size_t)bh * NC * R::BYTES;
+  const uint8_t *rec0 = ws + sizeof(WorkspaceHeader) + ((size_t)bh * NCh + n0) * R::BYTES;
   // After a failed wait: the abort word is set and the thread skips its later
   // waits; the producer stops copying and drains its copies, the issuer
   // drains its products before TMEM is released (as in the split scan).
@@ -2042,7 +2072,7 @@ __device__ __forceinline__ void scan_wide_d128(const float *h0, __nv_bfloat16 *_
       if (ok && !ptx::mbar_wait(&mO[b], (j / kWOutBufs) & 1, kWaitLimit)) fail(0x321u);
       ptx::tc_fence_after();
       const uint32_t tO = t_lane + D + D * b;
-      const int t = j * kC + row;
+      const int t = (n0 + j) * kC + row;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {  // 32-column block c of the row
         if (c == 2) load_row_blocks<2>(orec, kC, row, 2, Oc);  // columns 64-127
@@ -2151,26 +2181,37 @@ __device__ __forceinline__ void scan_wide_d128(const float *h0, __nv_bfloat16 *_
   }
 }
 
+// The scans take chunks n0 .. n0 + NC - 1 of each head (NCh chunks per head
+// in the workspace): all of them in one call, or one segment of a pipelined
+// call, where h0 is the state after chunk n0 - 1 (hT of the previous segment,
+// possibly the same buffer) and hT the state after the segment.  Launched as
+// a programmatic dependent of the prep segment that writes its records, a
+// scan lets the next prep segment be scheduled at once and waits for its own
+// prep (and through it for the previous scan segment) before it reads.
 __global__ void __launch_bounds__(kWideThreads, 1)
 kda_scan_wide_kernel(const float *h0, __nv_bfloat16 *__restrict__ o, float *hT, int T, int NC,
-                     uint8_t *__restrict__ ws) {
+                     int NCh, int n0, uint8_t *__restrict__ ws) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));
-  scan_wide_d128(h0, o, hT, T, NC, ws, sm);
+  ptx::grid_dep_launch();
+  ptx::grid_dep_wait();
+  scan_wide_d128(h0, o, hT, T, NC, NCh, n0, ws, sm);
 }
 
 template <int D, int NB, bool kNorm>
 __global__ void __launch_bounds__(kScan128Threads, 1)
 kda_scan_kernel(const float *h0, __nv_bfloat16 *__restrict__ o, float *hT, int T, int NC,
-                uint8_t *__restrict__ ws) {
+                int NCh, int n0, uint8_t *__restrict__ ws) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));
+  ptx::grid_dep_launch();
+  ptx::grid_dep_wait();
   if constexpr (D == 128)
-    scan_d128<NB, kNorm>(h0, o, hT, T, NC, ws, sm);
+    scan_d128<NB, kNorm>(h0, o, hT, T, NC, NCh, n0, ws, sm);
   else
-    scan_d64<NB>(h0, o, hT, T, NC, ws, sm);
+    scan_d64<NB>(h0, o, hT, T, NC, NCh, n0, ws, sm);
 }
 
 // ============================================================== launch
@@ -2186,11 +2227,52 @@ int sm_count() {
   return sms;
 }
 
+// Launch with or without programmatic stream serialization (see the prep and
+// scan kernels for what each side waits for).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, int threads, uint32_t smem,
+                     cudaStream_t st, bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+// The state between the segments of a pipelined call when the caller wants
+// no final state: after the records and their normaliser sums.
+float *segment_state(uint8_t *ws, int BH, int NC) {
+  return reinterpret_cast<float *>(ws + sizeof(WorkspaceHeader) +
+                                   (size_t)BH * NC * (Rec<128>::BYTES + NormRec::BYTES));
+}
+// The d = 128 prep's work counters (one per segment), after the states;
+// zeroed on the stream at the start of every call.
+constexpr int kMaxSegments = 16;
+constexpr size_t kClaimBytes = 256;
+static_assert(kMaxSegments * sizeof(unsigned) <= kClaimBytes, "claim area");
+unsigned *claim_area(uint8_t *ws, int BH, int NC) {
+  return reinterpret_cast<unsigned *>(reinterpret_cast<uint8_t *>(segment_state(ws, BH, NC)) +
+                                      (size_t)BH * 128 * 128 * sizeof(float));
+}
+
+// One prep launch and one scan launch per segment of G (G = 1: the whole
+// sequence, prep then scan).  Pipelined (G > 1, d = 128): segment g's prep
+// (all heads, chunks [g s, g s + s)) then its scan; every launch after the
+// first is a programmatic dependent of the one before, so scan g (the
+// one-CTA-per-head scan, on BH SMs) runs beside prep g + 1 (two CTAs per SM
+// on the other SMs).  The last segment's scan, with no prep beside it, is
+// the split scan.
 template <int D>
 kda_status launch_d(const void *q, const void *k, const void *v, const float *beta,
                     const float *log_alpha, const float *h0, void *o, float *hT, int BH, int T,
                     kda_alpha_mode am, uint8_t *ws, cudaStream_t st, LaunchTimer &timer,
-                    int rule, unsigned maps, bool wide) {
+                    int rule, unsigned maps, bool wide, int G) {
   constexpr int NB = scan_nb<D>();
   const int NC = (T + kC - 1) / kC;
   const uint32_t prep_smem = (D == 128 ? PrepSmem128::BYTES : PrepSmem64::BYTES) + 1024;
@@ -2211,37 +2293,78 @@ kda_status launch_d(const void *q, const void *k, const void *v, const float *be
     if (rule == KDA_RULE_LINEAR_NORM) scan = kda_scan_kernel<D, NB, true>;
   }
   constexpr uint32_t wide_smem = ScanWideSmem::BYTES + 1024;
+  const bool pipelined = D == 128 && G > 1 && NC > 0;
   if (cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)prep_smem) != cudaSuccess ||
       cudaFuncSetAttribute(scan, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)scan_smem) != cudaSuccess)
     return KDA_ERR_CUDA;
-  if (D == 128 && wide &&
+  if (D == 128 && (wide || pipelined) &&
       cudaFuncSetAttribute(kda_scan_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)wide_smem) != cudaSuccess)
     return KDA_ERR_CUDA;
-  if (NC > 0) {
-    const int sms = sm_count();
-    if (sms <= 0) return KDA_ERR_CUDA;
-    const long long total = (long long)BH * NC;
-    if (total > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
-    const long long slots = (long long)sms * (D == 128 ? 2 : 1);  // persistent CTAs per SM
-    const int grid = (int)(total < slots ? total : slots);
+  const int sms = sm_count();
+  if (sms <= 0) return KDA_ERR_CUDA;
+  const long long total = (long long)BH * NC;
+  if (total > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
+  auto *ob = static_cast<__nv_bfloat16 *>(o);
+  auto *qb = static_cast<const __nv_bfloat16 *>(q), *kb = static_cast<const __nv_bfloat16 *>(k),
+       *vb = static_cast<const __nv_bfloat16 *>(v);
+  const int per_sm = D == 128 ? 2 : 1;  // persistent prep CTAs per SM
+  unsigned *claims = D == 128 ? claim_area(ws, BH, NC) : nullptr;
+  if (NC > 0 && D == 128 && cudaMemsetAsync(claims, 0, kClaimBytes, st) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  if (!pipelined) {
+    if (NC > 0) {
+      const long long slots = (long long)sms * per_sm;
+      const int grid = (int)(total < slots ? total : slots);
+      timer.mark();
+      if (launch_k(prep, dim3(grid), 256, prep_smem, st, false, qb, kb, vb, beta, log_alpha,
+                   (int)am, T, NC, (int)total, 0, NC, (int)total, claims, ws, rule,
+                   maps) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    }
     timer.mark();
-    prep<<<grid, 256, prep_smem, st>>>(
-        static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
-        static_cast<const __nv_bfloat16 *>(v), beta, log_alpha, (int)am, T, NC, (int)total, ws,
-        rule, maps);
+    cudaError_t e;
+    if (D == 128 && wide)
+      e = launch_k(kda_scan_wide_kernel, dim3(BH), kWideThreads, wide_smem, st, false, h0, ob,
+                   hT, T, NC, NC, 0, ws);
+    else
+      e = launch_k(scan, dim3(D / NB, BH), D == 128 ? kScan128Threads : kScan64Threads,
+                   scan_smem, st, false, h0, ob, hT, T, NC, NC, 0, ws);
+    timer.mark();
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+  }
+  const int seg = (NC + G - 1) / G;
+  float *hs = hT ? hT : segment_state(ws, BH, NC);
+  // beside a scan segment the prep keeps the SMs the scan leaves free
+  const long long side_slots = (long long)(sms > BH ? sms - BH : 1) * per_sm;
+  for (int g = 0; g < G; ++g) {
+    const int n0 = g * seg;
+    const int ns = NC - n0 < seg ? NC - n0 : seg;
+    if (ns <= 0) break;
+    const bool last = n0 + ns >= NC;
+    const long long work = (long long)BH * ns;
+    const long long slots = g == 0 ? (long long)sms * per_sm : side_slots;
+    timer.mark();
+    if (launch_k(prep, dim3((int)(work < slots ? work : slots)), 256, prep_smem, st, g > 0, qb,
+                 kb, vb, beta, log_alpha, (int)am, T, NC, (int)total, n0, ns, (int)work,
+                 claims + g, ws, rule, maps) != cudaSuccess)
+      return KDA_ERR_CUDA;
+    const float *hin = g == 0 ? h0 : hs;
+    float *hout = last ? hT : hs;
+    timer.mark();
+    cudaError_t e;
+    if (!last)
+      e = launch_k(kda_scan_wide_kernel, dim3(BH), kWideThreads, wide_smem, st, true, hin, ob,
+                   hout, T, ns, NC, n0, ws);
+    else
+      e = launch_k(scan, dim3(D / NB, BH), kScan128Threads, scan_smem, st, true, hin, ob, hout,
+                   T, ns, NC, n0, ws);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
   }
   timer.mark();
-  if (D == 128 && wide)
-    kda_scan_wide_kernel<<<BH, kWideThreads, wide_smem, st>>>(
-        h0, static_cast<__nv_bfloat16 *>(o), hT, T, NC, ws);
-  else
-    scan<<<dim3(D / NB, BH), D == 128 ? kScan128Threads : kScan64Threads, scan_smem, st>>>(
-        h0, static_cast<__nv_bfloat16 *>(o), hT, T, NC, ws);
-  timer.mark();
-  return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+  return KDA_OK;
 }
 
 }  // namespace
@@ -2254,18 +2377,36 @@ size_t chunk_tc_workspace_bytes(int B, int H, int T, int dk, int dv, int C) {
   if (dk != dv || C != kC) return 0;
   const size_t NC = (size_t)(T + kC - 1) / kC;
   // d = 128: each chunk record is followed, after all of them, by its
-  // normaliser sums (read only by the normalised linear-attention rule)
-  const size_t rec = dk == 128 ? Rec<128>::BYTES + NormRec::BYTES : Rec<64>::BYTES;
-  return (size_t)B * H * NC * rec;
+  // normaliser sums (read only by the normalised linear-attention rule),
+  // those by one state per head (the hand-off between the segments of a
+  // pipelined call), and those by the prep's work counters
+  if (dk == 128)
+    return (size_t)B * H * NC * (Rec<128>::BYTES + NormRec::BYTES) +
+           (size_t)B * H * 128 * 128 * sizeof(float) + kClaimBytes;
+  return (size_t)B * H * NC * Rec<64>::BYTES;
 }
 
-int chunk_tc_launches(int BH, int T, bool has_hT) {
+int chunk_tc_segments(int BH, int T, int dk, int rule, int scan) {
+  if (dk != 128 || rule == KDA_RULE_LINEAR_NORM || BH <= 0 || T <= 0) return 1;
+  const int NC = (T + kC - 1) / kC;
+  if (scan == 3) {  // requested: segments of at least 8 chunks, at most 16 of them
+    const int g = NC / 8;
+    return g < 1 ? 1 : (g > kMaxSegments ? kMaxSegments : g);
+  }
+  return 1;
+}
+
+int chunk_tc_launches(int BH, int T, bool has_hT, int dk, int rule, int scan) {
   if (BH == 0 || (T == 0 && !has_hT)) return 0;
-  return T > 0 ? 2 : 1;
+  if (T == 0) return 1;
+  const int G = chunk_tc_segments(BH, T, dk, rule, scan);
+  if (G == 1) return 2;
+  const int NC = (T + kC - 1) / kC, seg = (NC + G - 1) / G;
+  return 2 * ((NC + seg - 1) / seg);
 }
 
 bool chunk_tc_wide_scan(int BH, int dk, int rule, int scan) {
-  if (dk != 128 || rule == KDA_RULE_LINEAR_NORM || scan == 1) return false;
+  if (dk != 128 || rule == KDA_RULE_LINEAR_NORM || scan == 1 || scan == 3) return false;
   if (scan == 2) return true;
   // automatic: the split scan.  The wide scan streams each whole record
   // through one SM; measured on Gated DeltaNet (128 heads, 128 chunks) it
@@ -2275,10 +2416,15 @@ bool chunk_tc_wide_scan(int BH, int dk, int rule, int scan) {
 }
 
 const char *chunk_tc_kernel_name(int BH, int T, int dk, int scan, int i) {
+  const int n = chunk_tc_launches(BH, T, true, dk, 0, scan);
+  if (i < 0 || i >= n) return nullptr;
+  if (chunk_tc_segments(BH, T, dk, 0, scan) > 1)  // prep, wide scan, ..., prep, split scan
+    return (i & 1) == 0 ? "kda_prep_kernel"
+                        : (i == n - 1 ? "kda_scan_kernel" : "kda_scan_wide_kernel");
   const char *scan_name = chunk_tc_wide_scan(BH, dk, 0, scan) ? "kda_scan_wide_kernel"
                                                                : "kda_scan_kernel";
-  if (T == 0) return i == 0 ? scan_name : nullptr;
-  return i == 0 ? "kda_prep_kernel" : (i == 1 ? scan_name : nullptr);
+  if (T == 0) return scan_name;
+  return i == 0 ? "kda_prep_kernel" : scan_name;
 }
 
 kda_status launch_chunk_tc(const void *q, const void *k, const void *v, const float *beta,
@@ -2287,13 +2433,14 @@ kda_status launch_chunk_tc(const void *q, const void *k, const void *v, const fl
                            void *workspace, size_t /*ws_bytes*/, cudaStream_t stream,
                            LaunchTimer &timer, int rule, unsigned maps, int scan) {
   const int BH = B * H;
-  if (chunk_tc_launches(BH, T, hT != nullptr) == 0) return KDA_OK;
+  if (chunk_tc_launches(BH, T, hT != nullptr, dk, rule, scan) == 0) return KDA_OK;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   if (dk == 128)
     return launch_d<128>(q, k, v, beta, log_alpha, h0, o, hT, BH, T, am, ws, stream, timer, rule,
-                         maps, chunk_tc_wide_scan(BH, dk, rule, scan));
+                         maps, chunk_tc_wide_scan(BH, dk, rule, scan),
+                         chunk_tc_segments(BH, T, dk, rule, scan));
   return launch_d<64>(q, k, v, beta, log_alpha, h0, o, hT, BH, T, am, ws, stream, timer, 0, 0u,
-                      false);
+                      false, 1);
 }
 
 }  // namespace kda

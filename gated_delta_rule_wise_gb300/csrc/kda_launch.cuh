@@ -35,9 +35,15 @@ kda_status launch_chunk_ffma(const void *q, const void *k, const void *v, const 
 // Kernel launches a chunk call makes on each path, and their names.
 int chunk_ffma_launches(int BH, int T, bool has_hT);
 const char *chunk_ffma_kernel_name(int i);
-int chunk_tc_launches(int BH, int T, bool has_hT);
+// Launches of a tensor-path call: 2 (prep, scan), 1 for an empty sequence
+// with a final state, 2 per segment when the call is pipelined.
+int chunk_tc_launches(int BH, int T, bool has_hT, int dk, int rule, int scan);
+// Segments of a call: 1, or G > 1 when the prep of each segment overlaps the
+// scan of the one before (d = 128; scan = 3 requests it).
+int chunk_tc_segments(int BH, int T, int dk, int rule, int scan);
 // scan: 0 automatic, 1 the value-column split scan, 2 the one-CTA-per-head
-// scan (d = 128 only; not for the normalised linear-attention rule).
+// scan (d = 128 only; not for the normalised linear-attention rule), 3 the
+// pipelined call (d = 128, same restriction).
 bool chunk_tc_wide_scan(int BH, int dk, int rule, int scan);
 const char *chunk_tc_kernel_name(int BH, int T, int dk, int scan, int i);
 bool chunk_tc_supported(int dk, int dv, int C, kda_dtype dt);

@@ -101,6 +101,21 @@ __device__ __forceinline__ void named_arrive(uint32_t id, uint32_t count) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Lets the next kernel of the stream, if it was launched with programmatic
+// stream serialization, be scheduled once every CTA of this grid has issued
+// this (or exited).  Without such a dependent it has no effect.
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Blocks until the grids this one depends on (the previous kernel of the
+// stream, when this grid was launched with programmatic stream serialization)
+// have completed and their memory operations are visible; returns at once
+// for a grid launched without that attribute.
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA (bulk)
 // 1-D bulk copy global -> shared, completing on an mbarrier (tx bytes).
 // Both addresses 16-byte aligned, size a multiple of 16.

@@ -81,10 +81,19 @@ typedef enum {
                             chosen as below                                     */
   KDA_PATH_TENSOR_SPLIT_SCAN = 3, /* tensor path, the scan split by value columns
                             (several CTAs per head; the only scan at dk = 64)   */
-  KDA_PATH_TENSOR_WIDE_SCAN = 4   /* tensor path, one scan CTA per (batch, head)
+  KDA_PATH_TENSOR_WIDE_SCAN = 4,  /* tensor path, one scan CTA per (batch, head)
                             holding all value columns (dk = dv = 128 only, else
                             KDA_ERR_UNSUPPORTED).  KDA_PATH_AUTO / _TENSOR use
                             the split scan                                       */
+  KDA_PATH_TENSOR_PIPELINED = 5   /* tensor path in up to 16 segments of the
+                            sequence (at least 8 chunks each): the prep of
+                            segment g + 1 runs beside the one-CTA-per-head scan
+                            of segment g, each launch a programmatic dependent
+                            of the one before on the caller's stream; the last
+                            segment's scan is the split scan.  dk = dv = 128,
+                            not the normalised linear-attention rule (else
+                            KDA_ERR_UNSUPPORTED); results as the other tensor
+                            paths.  Fewer than 16 chunks: one segment         */
 } kda_path;
 
 /* ABI version of this header; kda_abi_version() returns the library's. */
@@ -101,7 +110,10 @@ const char *kda_status_string(kda_status s);
  * per-chunk intermediates of the prep kernel (corrected keys and values,
  * decayed queries, the intra-chunk mask and decay factors: 98,816 bytes per
  * (head, chunk) at d = 128, followed at d = 128 by 768 bytes per (head,
- * chunk) that only the normalised linear-attention rule fills).
+ * chunk) that only the normalised linear-attention rule fills, and by one
+ * float32 dk x dv state per head that carries the state between the segments
+ * of a pipelined call when hT is NULL, and by 256 bytes of work counters that
+ * every call resets on its stream).
  */
 size_t kda_chunk_fwd_workspace_size(int B, int H, int T, int dk, int dv, int C,
                                     kda_dtype dt, kda_alpha_mode am);

@@ -82,6 +82,8 @@ def test_workspace_size(lib):
     assert wsx(*big, kda.KDA_PATH_TENSOR_SPLIT_SCAN) == wsx(*big, kda.KDA_PATH_TENSOR)
     assert wsx(*big, kda.KDA_PATH_TENSOR_WIDE_SCAN) == wsx(*big, kda.KDA_PATH_TENSOR)
     assert wsx(1, 2, 64, 64, 64, 64, kda.KDA_BF16, 0, kda.KDA_PATH_TENSOR_WIDE_SCAN) == 0
+    assert wsx(*big, kda.KDA_PATH_TENSOR_PIPELINED) == wsx(*big, kda.KDA_PATH_TENSOR)
+    assert wsx(1, 2, 64, 64, 64, 64, kda.KDA_BF16, 0, kda.KDA_PATH_TENSOR_PIPELINED) == 0
 
 
 def test_host_buffer_size(lib):
@@ -140,6 +142,8 @@ def test_chunk_argument_validation(lib):
     assert _chunk(lib, path=3, dt=0) == UNS          # ... both of its scans
     assert _chunk(lib, path=4, dt=0) == UNS
     assert _chunk(lib, path=4, dt=1, dk=64, dv=64, C=64) == UNS   # wide scan: d = 128 only
+    assert _chunk(lib, path=5, dt=0) == UNS                       # pipelined: tensor path
+    assert _chunk(lib, path=5, dt=1, dk=64, dv=64, C=64) == UNS   # ... at d = 128 only
     assert _chunk(lib, path=6) == INV                # unknown path
     assert _chunk(lib, nev=2) == INV                 # events requested but NULL
     one = (ctypes.c_void_p * 1)(FAKE)
@@ -183,8 +187,29 @@ def test_tensor_path_is_what_auto_picks_for_bf16_c64(lib):
     assert kda.kda_chunk_fwd_kernel_names(1, 1, 0, 128, 128, 64, kda.KDA_BF16, 2) == ["kda_scan_kernel"]
     assert kda.kda_chunk_fwd_kernel_names(1, 1, 64, 16, 16, 16, kda.KDA_F32, 2) == ["chunk_ffma_kernel"]
     big = kda.kda_chunk_fwd_workspace_size(1, 32, 131072, 128, 128, 64, kda.KDA_BF16, 2)
-    # one 98816-byte record per (head, chunk), then its 768 bytes of normaliser sums
-    assert big == 256 + 32 * 2048 * (98816 + 768)
+    # one 98816-byte record per (head, chunk), then its 768 bytes of normaliser
+    # sums, then one float32 128 x 128 state per head and 256 bytes of work counters
+    assert big == 256 + 32 * 2048 * (98816 + 768) + 32 * 128 * 128 * 4 + 256
+
+
+def test_pipelined_launch_plan(lib):
+    """A pipelined call: up to 16 segments of at least 8 chunks, a prep and a
+    scan launch per segment, the one-CTA-per-head scan except for the last
+    segment's split scan; one segment below 16 chunks."""
+    import gated_delta_rule_wise_gb300 as kda
+    P = kda.KDA_PATH_TENSOR_PIPELINED
+
+    def names(T, H=32):
+        return kda.kda_chunk_fwd_kernel_names(1, H, T, 128, 128, 64, kda.KDA_BF16, 2, P)
+    assert names(131072) == ["kda_prep_kernel", "kda_scan_wide_kernel"] * 15 + \
+        ["kda_prep_kernel", "kda_scan_kernel"]                       # 2048 chunks: 16 x 128
+    assert names(64 * 131 + 1) == ["kda_prep_kernel", "kda_scan_wide_kernel"] * 14 + \
+        ["kda_prep_kernel", "kda_scan_kernel"]                       # 131 chunks: 15 x 9, last 5
+    assert names(64 * 15) == ["kda_prep_kernel", "kda_scan_kernel"]  # 15 chunks: one segment
+    assert names(64 * 16) == ["kda_prep_kernel", "kda_scan_wide_kernel",
+                              "kda_prep_kernel", "kda_scan_kernel"]
+    assert names(0) == ["kda_scan_kernel"]                           # empty: h0 -> hT
+    assert lib.kda_chunk_fwd_launches(1, 32, 131072, 128, 128, 64, 1, 2, P) == 32
 
 
 def test_status_and_selftest_validation(lib):

@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 
 PATHS = {"auto": kda.KDA_PATH_AUTO, "cuda_core": kda.KDA_PATH_CUDA_CORE,
          "tensor": kda.KDA_PATH_TENSOR, "split": kda.KDA_PATH_TENSOR_SPLIT_SCAN,
-         "wide": kda.KDA_PATH_TENSOR_WIDE_SCAN}
+         "wide": kda.KDA_PATH_TENSOR_WIDE_SCAN, "pipelined": kda.KDA_PATH_TENSOR_PIPELINED}
 
 
 def tensor_path_ok(w):
@@ -122,6 +122,59 @@ def test_wide_scan_matches_oracle(alpha, B, H, T):
     w = W.Prefill("wide", B=B, H=H, T=T, dk=128, dv=128, C=64, dtype="bf16", alpha=alpha,
                   la_mu=-3.5, h0_sd=0.05, seed=T + 7 * H + len(alpha))
     check_full(w, "wide")
+
+
+# ---------------------------------------------------------------- the pipelined call
+
+@pytest.mark.parametrize("alpha", ["none", "scalar", "channel"])
+@pytest.mark.parametrize("B,H,T", [(1, 3, 64 * 37 + 19), (2, 2, 64 * 16), (1, 2, 64 * 8 + 5),
+                                   (1, 1, 64 * 130 + 1)])
+def test_pipelined_matches_oracle(alpha, B, H, T):
+    """Segments of the sequence, each prep beside the previous segment's
+    scan: 4 segments with a short last one and a partial last chunk, 2
+    segments, a single segment (9 chunks), and 15 segments (14 of 9 chunks,
+    the last of 5 ending in a one-token chunk); initial state, every decay
+    mode."""
+    w = W.Prefill("pipelined", B=B, H=H, T=T, dk=128, dv=128, C=64, dtype="bf16", alpha=alpha,
+                  la_mu=-3.5, h0_sd=0.05, seed=T + 11 * H + len(alpha))
+    check_full(w, "pipelined")
+
+
+def test_pipelined_segment_count():
+    """The launches of a pipelined call: prep and scan per segment, the one-CTA-
+    per-head scan except for the last segment's split scan."""
+    names = kda.kda_chunk_fwd_kernel_names(1, 3, 64 * 37 + 19, 128, 128, 64, kda.KDA_BF16,
+                                           kda.KDA_ALPHA_CHANNEL, kda.KDA_PATH_TENSOR_PIPELINED)
+    assert names == ["kda_prep_kernel", "kda_scan_wide_kernel"] * 3 + \
+        ["kda_prep_kernel", "kda_scan_kernel"]
+
+
+def test_pipelined_without_final_state():
+    """No hT: the state between segments lives in the workspace."""
+    w = W.KDA_PREFILL_BF16.with_(B=1, H=2, T=64 * 40 + 3, h0_sd=0.02, seed=31)
+    x = W.prefill_inputs(w)
+    d = device_inputs(w, x)
+    o, hT = run(w, d, "pipelined", hT_out=False)
+    assert hT is None
+    o_ref, _ = oracle.recurrent_heads(x["q"], x["k"], x["v"], x["beta"], x["log_alpha"], x["h0"])
+    tol = tol_for(w.dtype)
+    eo = rel_err(o.float().cpu().numpy().reshape(o_ref.shape), o_ref)
+    record(case_name(w, "pipelined") + ", no hT", "o", eo, tol)
+    assert eo <= tol, f"o {eo:.3e}"
+
+
+def test_pipelined_rejected_at_d64():
+    w = W.DELTANET_BF16.with_(B=1, H=1, T=64 * 20)
+    d = device_inputs(w, W.prefill_inputs(w))
+    with pytest.raises(kda.KdaError) as e:
+        run(w, d, "pipelined")
+    assert e.value.status == kda.KDA_ERR_UNSUPPORTED
+
+
+@pytest.mark.slow
+def test_kda_prefill_bf16_full_size_pipelined_sampled_heads():
+    """The full KDA workload as a pipelined call (16 segments of 128 chunks)."""
+    _sampled(W.KDA_PREFILL_BF16, 8, path="pipelined", seed=3)
 
 
 def test_wide_scan_long_sequence_many_chunks():
