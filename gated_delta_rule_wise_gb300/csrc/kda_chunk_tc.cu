@@ -1279,7 +1279,8 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
 // n0, nseg, work: the chunk range of a pipelined call (d = 128; the d = 64
 // prep always takes every chunk, n0 = 0, nseg = NC, work = total, in a fixed
 // order: one CTA per SM).  ctr: the d = 128 prep's work counter, zero when
-// the grid starts.  Launched
+// the grid starts.  pdl (segments of a pipelined call only): the grid lets
+// the next launch of the stream, its scan, be scheduled at once.  Launched
 // as a programmatic dependent of the previous scan segment, a CTA starts
 // while that scan still runs (its inputs and records are disjoint from the
 // scan's) and waits for the scan only before it exits, so that the prep's
@@ -1291,11 +1292,11 @@ kda_prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
                 const __nv_bfloat16 *__restrict__ v, const float *__restrict__ beta,
                 const float *__restrict__ log_alpha, int alpha_mode, int T, int NC, int total,
                 int n0, int nseg, int work, unsigned *ctr, uint8_t *__restrict__ ws, int rule,
-                unsigned maps) {
+                unsigned maps, int pdl) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));
-  ptx::grid_dep_launch();
+  if (pdl) ptx::grid_dep_launch();
   if constexpr (D == 128)
     prep_d128<kMode, kRowDecay>(q, k, v, beta, log_alpha, alpha_mode, T, NC, total, n0, nseg,
                                 work, ctr, ws, sm, rule, maps);
@@ -2186,15 +2187,16 @@ __device__ __forceinline__ void scan_wide_d128(const float *h0, __nv_bfloat16 *_
 // call, where h0 is the state after chunk n0 - 1 (hT of the previous segment,
 // possibly the same buffer) and hT the state after the segment.  Launched as
 // a programmatic dependent of the prep segment that writes its records, a
-// scan lets the next prep segment be scheduled at once and waits for its own
-// prep (and through it for the previous scan segment) before it reads.
+// scan waits for its own prep (and through it for the previous scan segment)
+// before it reads; with pdl set (every scan segment but the last) it lets the
+// next prep segment be scheduled at once.
 __global__ void __launch_bounds__(kWideThreads, 1)
 kda_scan_wide_kernel(const float *h0, __nv_bfloat16 *__restrict__ o, float *hT, int T, int NC,
-                     int NCh, int n0, uint8_t *__restrict__ ws) {
+                     int NCh, int n0, uint8_t *__restrict__ ws, int pdl) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));
-  ptx::grid_dep_launch();
+  if (pdl) ptx::grid_dep_launch();
   ptx::grid_dep_wait();
   scan_wide_d128(h0, o, hT, T, NC, NCh, n0, ws, sm);
 }
@@ -2202,11 +2204,11 @@ kda_scan_wide_kernel(const float *h0, __nv_bfloat16 *__restrict__ o, float *hT, 
 template <int D, int NB, bool kNorm>
 __global__ void __launch_bounds__(kScan128Threads, 1)
 kda_scan_kernel(const float *h0, __nv_bfloat16 *__restrict__ o, float *hT, int T, int NC,
-                int NCh, int n0, uint8_t *__restrict__ ws) {
+                int NCh, int n0, uint8_t *__restrict__ ws, int pdl) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));
-  ptx::grid_dep_launch();
+  if (pdl) ptx::grid_dep_launch();
   ptx::grid_dep_wait();
   if constexpr (D == 128)
     scan_d128<NB, kNorm>(h0, o, hT, T, NC, NCh, n0, ws, sm);
@@ -2320,18 +2322,18 @@ kda_status launch_d(const void *q, const void *k, const void *v, const float *be
       const int grid = (int)(total < slots ? total : slots);
       timer.mark();
       if (launch_k(prep, dim3(grid), 256, prep_smem, st, false, qb, kb, vb, beta, log_alpha,
-                   (int)am, T, NC, (int)total, 0, NC, (int)total, claims, ws, rule,
-                   maps) != cudaSuccess)
+                   (int)am, T, NC, (int)total, 0, NC, (int)total, claims, ws, rule, maps,
+                   0) != cudaSuccess)
         return KDA_ERR_CUDA;
     }
     timer.mark();
     cudaError_t e;
     if (D == 128 && wide)
       e = launch_k(kda_scan_wide_kernel, dim3(BH), kWideThreads, wide_smem, st, false, h0, ob,
-                   hT, T, NC, NC, 0, ws);
+                   hT, T, NC, NC, 0, ws, 0);
     else
       e = launch_k(scan, dim3(D / NB, BH), D == 128 ? kScan128Threads : kScan64Threads,
-                   scan_smem, st, false, h0, ob, hT, T, NC, NC, 0, ws);
+                   scan_smem, st, false, h0, ob, hT, T, NC, NC, 0, ws, 0);
     timer.mark();
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
   }
@@ -2349,7 +2351,7 @@ kda_status launch_d(const void *q, const void *k, const void *v, const float *be
     timer.mark();
     if (launch_k(prep, dim3((int)(work < slots ? work : slots)), 256, prep_smem, st, g > 0, qb,
                  kb, vb, beta, log_alpha, (int)am, T, NC, (int)total, n0, ns, (int)work,
-                 claims + g, ws, rule, maps) != cudaSuccess)
+                 claims + g, ws, rule, maps, 1) != cudaSuccess)
       return KDA_ERR_CUDA;
     const float *hin = g == 0 ? h0 : hs;
     float *hout = last ? hT : hs;
@@ -2357,10 +2359,10 @@ kda_status launch_d(const void *q, const void *k, const void *v, const float *be
     cudaError_t e;
     if (!last)
       e = launch_k(kda_scan_wide_kernel, dim3(BH), kWideThreads, wide_smem, st, true, hin, ob,
-                   hout, T, ns, NC, n0, ws);
-    else
+                   hout, T, ns, NC, n0, ws, 1);
+    else  // the call's last kernel: nothing after it starts early
       e = launch_k(scan, dim3(D / NB, BH), kScan128Threads, scan_smem, st, true, hin, ob, hout,
-                   T, ns, NC, n0, ws);
+                   T, ns, NC, n0, ws, 0);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
   }
   timer.mark();

@@ -90,7 +90,10 @@ typedef enum {
                             segment g + 1 runs beside the one-CTA-per-head scan
                             of segment g, each launch a programmatic dependent
                             of the one before on the caller's stream; the last
-                            segment's scan is the split scan.  dk = dv = 128,
+                            segment's scan is the split scan.  To the caller's
+                            stream the call is ordinary: its first launch waits
+                            for earlier work and nothing enqueued after it
+                            starts before its last kernel ends.  dk = dv = 128,
                             not the normalised linear-attention rule (else
                             KDA_ERR_UNSUPPORTED); results as the other tensor
                             paths.  Fewer than 16 chunks: one segment         */
