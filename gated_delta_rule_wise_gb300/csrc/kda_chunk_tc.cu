@@ -1355,23 +1355,27 @@ constexpr int kStages = 3;
 constexpr int kPrefetchAhead = 3;  // scan: records prefetched into L2 this many chunks ahead of their copy
 constexpr int kOutBufs = 3;
 constexpr int kScan128Threads = 320;  // 4 state warps, 4 output warps, producer, issuer
+// A scan CTA owns NB = 32 value columns (one block of B and O), or 64 (two
+// adjacent blocks, when four CTAs per head would not fit the SMs in one
+// round); the 64-column CTA has room for two record stages only.
 template <int NB>
 struct ScanSmem128 {
   using R = Rec<128>;
-  static_assert(NB == R::BLK, "a scan CTA owns one 32-column block");
-  static constexpr uint32_t BI_S = R::PRE;                   // B block [128][NB]
-  static constexpr uint32_t OI_S = BI_S + 128 * NB * 2;      // O block [C][NB]
+  static_assert(NB == R::BLK || NB == 2 * R::BLK, "a scan CTA owns one or two 32-column blocks");
+  static constexpr int STAGES = NB == R::BLK ? kStages : 2;
+  static constexpr uint32_t BI_S = R::PRE;                   // B blocks [NB / 32][128][32]
+  static constexpr uint32_t OI_S = BI_S + 128 * NB * 2;      // O blocks [NB / 32][C][32]
   static constexpr uint32_t GC_S = OI_S + kC * NB * 2;       // gamma_C [128]
   static constexpr uint32_t STAGE_BYTES = GC_S + 128 * 4;
   static constexpr uint32_t NRM_S = STAGE_BYTES;             // NormRec (normalised rule only)
   static constexpr uint32_t STAGE = align1k(NRM_S + NormRec::BYTES);
-  static constexpr uint32_t SB = kStages * STAGE;            // 2 x bf16 S [128 rows][64 cols]
-  // full[kStages], empty[kStages], mS, mO[kOutBufs], ofree[kOutBufs]
+  static constexpr uint32_t SB = STAGES * STAGE;             // 2 x bf16 S [128 rows][64 cols]
+  // full[STAGES], empty[STAGES], mS, mO[kOutBufs], ofree[kOutBufs]
   static constexpr uint32_t BAR = SB + 2 * 128 * 64 * 2;
-  static constexpr uint32_t TMEMP = BAR + (2 * kStages + 1 + 2 * kOutBufs) * 8;
+  static constexpr uint32_t TMEMP = BAR + (2 * STAGES + 1 + 2 * kOutBufs) * 8;
   static constexpr uint32_t ABORT = TMEMP + 4;               // CTA-wide abort word
   static constexpr uint32_t BYTES = TMEMP + 8;
-  static constexpr uint32_t TMEM_COLS = 128;                 // P | o[0] | o[1] | o[2]
+  static constexpr uint32_t TMEM_COLS = NB == R::BLK ? 128 : 256;  // P | o[0] | o[1] | o[2]
   static_assert(NB * (1 + kOutBufs) <= TMEM_COLS, "TMEM columns");
   static_assert(BYTES + 1024 <= 232448, "scan shared memory");
 };
@@ -1394,6 +1398,7 @@ __device__ __forceinline__ void scan_d128(const float *h0, __nv_bfloat16 *__rest
   constexpr uint32_t kSyncThreads = 128 + 32;  // state warps + issuer warp
   using R = Rec<128>;
   using L = ScanSmem128<NB>;
+  constexpr int kStages = L::STAGES;  // record ring
   constexpr bool norm = kNorm;
   constexpr int kOW = kNorm ? NB + 8 : NB;                     // output accumulator width
   constexpr uint32_t kTmemCols = kNorm ? 256 : L::TMEM_COLS;  // P | o[0] | o[1] | o[2]
@@ -1491,7 +1496,7 @@ __device__ __forceinline__ void scan_d128(const float *h0, __nv_bfloat16 *__rest
     // 2^18), and the loop unrolled over six chunks, the period of the 3-stage
     // record ring, the 3 output accumulators and the 2 S copies, so that
     // nothing but the MMAs sits between the hand-off and the first product.
-    static_assert(kStages == 3 && kOutBufs == 3, "six-chunk issuer period");
+    static_assert(6 % kStages == 0 && kOutBufs == 3, "six-chunk issuer period");
     uint64_t dAPs[kStages], dQPs[kStages], dSBs[2];
 #pragma unroll
     for (int q = 0; q < kStages; ++q) {
@@ -1563,8 +1568,10 @@ __device__ __forceinline__ void scan_d128(const float *h0, __nv_bfloat16 *__rest
         ptx::tmem_ld16(tO + cb, x);
         ptx::tmem_ld_wait();
         if (lane < 16 && t < T) {
-          const uint4 a = *reinterpret_cast<const uint4 *>(oi + rotated_chunk(orow, cb / 8));
-          const uint4 c2 = *reinterpret_cast<const uint4 *>(oi + rotated_chunk(orow, cb / 8 + 1));
+          const int q = cb / 8;  // 16-byte chunk of the row: block q / 4, chunk q % 4
+          const uint8_t *ob = oi + (q >> 2) * (kC * 64);
+          const uint4 a = *reinterpret_cast<const uint4 *>(ob + rotated_chunk(orow, q & 3));
+          const uint4 c2 = *reinterpret_cast<const uint4 *>(ob + rotated_chunk(orow, (q & 3) + 1));
           const uint32_t w[8] = {a.x, a.y, a.z, a.w, c2.x, c2.y, c2.z, c2.w};
           uint32_t pk[8];
 #pragma unroll
@@ -1640,7 +1647,8 @@ __device__ __forceinline__ void scan_d128(const float *h0, __nv_bfloat16 *__rest
           zr = gam * zr + reinterpret_cast<const float *>(st + L::NRM_S)[NormRec::KS / 4 + r];
 #pragma unroll
         for (int q4 = 0; q4 < NB / 8; ++q4) {
-          const uint4 a = *reinterpret_cast<const uint4 *>(st + L::BI_S + rotated_chunk(r, q4));
+          const uint4 a = *reinterpret_cast<const uint4 *>(st + L::BI_S + (q4 >> 2) * (128 * 64) +
+                                                           rotated_chunk(r, q4 & 3));
           const uint32_t w[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -1658,7 +1666,9 @@ __device__ __forceinline__ void scan_d128(const float *h0, __nv_bfloat16 *__rest
       ptx::tc_fence_after();
       {
         float x[NB];
-        ptx::tmem_ld32(tP, x);
+#pragma unroll
+        for (int c = 0; c < NB; c += 32)
+          ptx::tmem_ld32(tP + c, *reinterpret_cast<float(*)[32]>(x + c));
         ptx::tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < NB; ++j) sr[j] += x[j];
@@ -2277,9 +2287,16 @@ kda_status launch_d(const void *q, const void *k, const void *v, const float *be
                     int rule, unsigned maps, bool wide, int G) {
   constexpr int NB = scan_nb<D>();
   const int NC = (T + kC - 1) / kC;
+  const int sms = sm_count();
+  if (sms <= 0) return KDA_ERR_CUDA;
+  // d = 128: 64 value columns per scan CTA when four CTAs per head would
+  // take more than one round of the SMs (not the normalised rule)
+  const bool nb64 = D == 128 && rule != KDA_RULE_LINEAR_NORM && (long long)BH * (D / NB) > sms;
+  const int scan_nbv = nb64 ? 2 * NB : NB;
   const uint32_t prep_smem = (D == 128 ? PrepSmem128::BYTES : PrepSmem64::BYTES) + 1024;
   const uint32_t scan_smem =
-      (D == 128 ? ScanSmem128<NB>::BYTES : ScanSmem64<NB>::BYTES) + 1024;
+      (D == 128 ? (nb64 ? ScanSmem128<2 * NB>::BYTES : ScanSmem128<NB>::BYTES)
+                : ScanSmem64<NB>::BYTES) + 1024;
   auto prep = kda_prep_kernel<D, 0, false>;
   if constexpr (D == 128) {
     const bool row = am != KDA_ALPHA_CHANNEL;  // scalar or no decay: one factor per token
@@ -2293,6 +2310,7 @@ kda_status launch_d(const void *q, const void *k, const void *v, const float *be
   auto scan = kda_scan_kernel<D, NB, false>;
   if constexpr (D == 128) {
     if (rule == KDA_RULE_LINEAR_NORM) scan = kda_scan_kernel<D, NB, true>;
+    else if (nb64) scan = kda_scan_kernel<D, 2 * NB, false>;
   }
   constexpr uint32_t wide_smem = ScanWideSmem::BYTES + 1024;
   const bool pipelined = D == 128 && G > 1 && NC > 0;
@@ -2305,8 +2323,6 @@ kda_status launch_d(const void *q, const void *k, const void *v, const float *be
       cudaFuncSetAttribute(kda_scan_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)wide_smem) != cudaSuccess)
     return KDA_ERR_CUDA;
-  const int sms = sm_count();
-  if (sms <= 0) return KDA_ERR_CUDA;
   const long long total = (long long)BH * NC;
   if (total > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
   auto *ob = static_cast<__nv_bfloat16 *>(o);
@@ -2332,7 +2348,7 @@ kda_status launch_d(const void *q, const void *k, const void *v, const float *be
       e = launch_k(kda_scan_wide_kernel, dim3(BH), kWideThreads, wide_smem, st, false, h0, ob,
                    hT, T, NC, NC, 0, ws, 0);
     else
-      e = launch_k(scan, dim3(D / NB, BH), D == 128 ? kScan128Threads : kScan64Threads,
+      e = launch_k(scan, dim3(D / scan_nbv, BH), D == 128 ? kScan128Threads : kScan64Threads,
                    scan_smem, st, false, h0, ob, hT, T, NC, NC, 0, ws, 0);
     timer.mark();
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
@@ -2361,8 +2377,8 @@ kda_status launch_d(const void *q, const void *k, const void *v, const float *be
       e = launch_k(kda_scan_wide_kernel, dim3(BH), kWideThreads, wide_smem, st, true, hin, ob,
                    hout, T, ns, NC, n0, ws, 1);
     else  // the call's last kernel: nothing after it starts early
-      e = launch_k(scan, dim3(D / NB, BH), kScan128Threads, scan_smem, st, true, hin, ob, hout,
-                   T, ns, NC, n0, ws, 0);
+      e = launch_k(scan, dim3(D / scan_nbv, BH), kScan128Threads, scan_smem, st, true, hin, ob,
+                   hout, T, ns, NC, n0, ws, 0);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
   }
   timer.mark();

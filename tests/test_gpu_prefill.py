@@ -177,6 +177,17 @@ def test_kda_prefill_bf16_full_size_pipelined_sampled_heads():
     _sampled(W.KDA_PREFILL_BF16, 8, path="pipelined", seed=3)
 
 
+@pytest.mark.parametrize("alpha", ["none", "scalar", "channel"])
+def test_split_scan_64_columns_matches_oracle(alpha):
+    """48 heads: four 32-column scan CTAs per head would take two rounds of
+    the GPU's SMs, so each head gets two 64-column CTAs (two record stages);
+    every head against the oracle, ragged last chunk, initial state."""
+    w = W.Prefill("split64", B=2, H=24, T=64 * 5 + 7, dk=128, dv=128, C=64, dtype="bf16",
+                  alpha=alpha, la_mu=-3.5, h0_sd=0.05, seed=41 + len(alpha))
+    check_full(w, "split")
+    check_full(w, "pipelined")
+
+
 def test_wide_scan_long_sequence_many_chunks():
     w = W.KDA_PREFILL_BF16.with_(B=1, H=4, T=64 * 300 + 17, h0_sd=0.02, seed=23)
     check_full(w, "wide")
