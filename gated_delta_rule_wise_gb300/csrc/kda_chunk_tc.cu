@@ -1430,7 +1430,7 @@ __device__ __forceinline__ void scan_d128(const float *h0, __nv_bfloat16 *__rest
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&full[s], 1);
-      ptx::mbar_init(&empty[s], 2);  // released by the issuer (state side) and by the output warps
+      ptx::mbar_init(&empty[s], 4 + 1);  // released by each state warp and by the output warps
     }
     ptx::mbar_init(mS, 1);
     for (int b = 0; b < kOutBufs; ++b) {
@@ -1623,8 +1623,9 @@ __device__ __forceinline__ void scan_d128(const float *h0, __nv_bfloat16 *__rest
       // the checks the issuer's products need, made here where they are off
       // its serial path: record i landed (every state thread reads its B and
       // gamma_C below anyway), accumulator (i mod 3) read by the output warps
-      // (chunk i - 3); and stage i-1 released for the state side (its products
-      // completed before P_{i-1} was read, its B was read before that)
+      // (chunk i - 3); and stage i - 1 released by each state warp (its lanes
+      // read their B rows of chunk i - 1 and saw P_{i-1}, the stage's last
+      // product, complete)
       if (ok && !ptx::mbar_wait_fast(&full[s], (i / kStages) & 1, kWaitLimit)) {
         ok = false;
         ptx::set_abort(abort_f);
@@ -1637,9 +1638,9 @@ __device__ __forceinline__ void scan_d128(const float *h0, __nv_bfloat16 *__rest
           ptx::set_abort(abort_f);
           report_error(hdr, KDA_ERR_TIMEOUT, 0x222u);
         }
-        if (i > 0) ptx::mbar_arrive(&empty[(i - 1) % kStages]);
       }
       __syncwarp();
+      if (lane == 0 && i > 0) ptx::mbar_arrive(&empty[(i - 1) % kStages]);
       ptx::named_arrive(1, kSyncThreads);
       {  // gamma_C S + B while the product runs
         const float gam = reinterpret_cast<const float *>(st + L::GC_S)[r];
@@ -1987,7 +1988,7 @@ __device__ __forceinline__ void scan_wide_d128(const float *h0, __nv_bfloat16 *_
   if (tid == 0) {
     for (int s = 0; s < kWStages; ++s) {
       ptx::mbar_init(&full[s], 1);
-      ptx::mbar_init(&empty[s], 2);  // released by the state side and by the output warps
+      ptx::mbar_init(&empty[s], 8 + 1);  // released by each state warp and by the output warps
     }
     ptx::mbar_init(mS, 1);
     for (int b = 0; b < kWOutBufs; ++b) {
@@ -2142,16 +2143,15 @@ __device__ __forceinline__ void scan_wide_d128(const float *h0, __nv_bfloat16 *_
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       // record i landed (gamma_C is read below), output accumulator (i mod 2)
-      // read by the output warps (chunk i - 2), stage i - 1 released for the
-      // state side (its product completed before P_{i-1} was read)
+      // read by the output warps (chunk i - 2); stage i - 1 released by each
+      // state warp (its lanes read their gamma_C of chunk i - 1 and saw
+      // P_{i-1}, the stage's last state-side product, complete)
       if (ok && !ptx::mbar_wait_fast(&full[s], (i / kWStages) & 1, kWaitLimit)) fail(0x304u);
-      if (tid == 0) {
-        if (i >= kWOutBufs && ok &&
-            !ptx::mbar_wait_fast(&ofree[i % kWOutBufs], ((i / kWOutBufs) - 1) & 1, kWaitLimit))
-          fail(0x322u);
-        if (i > 0) ptx::mbar_arrive(&empty[(i - 1) % kWStages]);
-      }
+      if (tid == 0 && i >= kWOutBufs && ok &&
+          !ptx::mbar_wait_fast(&ofree[i % kWOutBufs], ((i / kWOutBufs) - 1) & 1, kWaitLimit))
+        fail(0x322u);
       __syncwarp();
+      if (lane == 0 && i > 0) ptx::mbar_arrive(&empty[(i - 1) % kWStages]);
       ptx::named_arrive(1, kSyncThreads);
       {  // gamma_C S + B while the product runs
         const float gam = gcr[s * 128 + r];

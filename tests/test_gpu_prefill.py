@@ -270,6 +270,35 @@ def test_in_place_state_and_split_resume():
     assert eo <= TOL_BF16 and eh <= TOL_BF16, (eo, eh)
 
 
+def test_pipelined_in_place_state_and_split_resume():
+    """The pipelined call with h0 == hT (its segments then carry the state in
+    the caller's buffer), resumed from that state by a second pipelined call."""
+    w = W.KDA_PREFILL_BF16.with_(B=1, H=3, T=64 * 36 + 9, h0_sd=0.02, seed=78)
+    x = W.prefill_inputs(w)
+    d = device_inputs(w, x)
+    T1 = 64 * 20
+    sl = lambda t, a, b: None if t is None else t[:, :, a:b].contiguous()
+    S = d["h0"].clone()
+    outs = []
+    for a, b in ((0, T1), (T1, w.T)):
+        part = dict(q=sl(d["q"], a, b), k=sl(d["k"], a, b), v=sl(d["v"], a, b),
+                    beta=sl(d["beta"], a, b), log_alpha=sl(d["log_alpha"], a, b))
+        o = torch.empty_like(part["v"])
+        P = kda.KDA_PATH_TENSOR_PIPELINED
+        ws = kda.workspace_for(part["q"], part["v"], w.C, part["log_alpha"], P)
+        kda.kda_chunk_fwd_ex(part["q"], part["k"], part["v"], part["beta"], part["log_alpha"],
+                             S, o, S, w.C, ws, None, P)   # in place: h0 is hT
+        outs.append(o)
+    torch.cuda.synchronize()
+    o_split = torch.cat(outs, dim=2)
+    o_ref, h_ref = oracle.recurrent_heads(x["q"], x["k"], x["v"], x["beta"], x["log_alpha"], x["h0"])
+    eo = rel_err(o_split.float().cpu().numpy().reshape(o_ref.shape), o_ref)
+    eh = rel_err(S.cpu().numpy().reshape(h_ref.shape), h_ref)
+    record(case_name(w, "pipelined") + f", split at {T1}, in place", "o", eo, TOL_BF16)
+    record(case_name(w, "pipelined") + f", split at {T1}, in place", "hT", eh, TOL_BF16)
+    assert eo <= TOL_BF16 and eh <= TOL_BF16, (eo, eh)
+
+
 @pytest.mark.parametrize("T,B,H", [(129, 2, 2), (64, 1, 3), (200, 1, 2)])
 def test_prefill_then_decode_matches_oracle(T, B, H):
     """Prefill of the first T - 1 tokens, then one decode step on the state it
