@@ -21,19 +21,21 @@
 //   S' = (Diag(gamma_C) + Ap) S + Kbar^T U,      Ap = -Kbar^T W   (D x D)
 //   o  = Qp S + M U,                              Qp = Q*gamma - M W  (C x D)
 // Everything except S is known per chunk before the pass starts, so
-//  - kda_prep_kernel (persistent CTAs, chunks taken in turn, fully parallel)
+//  - kda_prep_kernel (persistent CTAs, fully parallel over (head, chunk))
 //    computes the decay prefix, the decayed tiles, A and M (one tcgen05 MMA
 //    group), T by a blocked inverse in shared memory, W and U, then the
 //    chunk's record: for D = 128 Ap and Qp as swizzled operand tiles and the
 //    additive terms B = Kbar^T U and O = M U already multiplied out; for
 //    D = 64 Ap, Qp, Kbar^T, M and U^T tiles.  gamma_C closes each record.
-//  - kda_scan_kernel (one CTA per (head, block of NB value columns)) walks the
+//  - kda_scan_kernel (one CTA per (head, block of 32 or 64 value columns)) walks the
 //    chunks in order with the records streamed in by bulk copies; per chunk
 //    it writes a bf16 copy of S as the MMA operand, forms
 //    S' = gamma_C S + B + Ap S (one group of tcgen05 MMAs) and, off the
 //    serial path, o = Qp S + O.  One MMA round trip per chunk sits on the
 //    serial path.
 // The D = 128 kernels are described in detail above prep_d128 and scan_d128.
+// A call may also run in segments of the sequence, each segment's prep beside
+// the previous segment's scan (the pipelined call, above launch_d).
 // A partial last chunk is padded with k = q = v = 0, beta = 0, a = 1, which
 // adds nothing; padded rows of o are not stored.
 #include <type_traits>
