@@ -676,10 +676,9 @@ __device__ __forceinline__ uint4 pack8(const float *x) {
 }
 
 // kMode 0 compiles the plain gated delta rule (rule and maps fixed at 0, their
-// code folded away); 1 reads the rule and the silu / sigmoid maps at run time;
-// 2 is for the linear rules only (no solve compiled in) and adds the ELU + 1
-// map and the normalised rule's sums; 3 is the delta rule with the silu /
-// sigmoid maps read at run time (the linear rules' code folded away).  The modes are separate instantiations
+// code folded away); 1 the delta rule with the silu / sigmoid maps read at run
+// time (the linear rules' code folded away); 2 the linear rules (no solve
+// compiled in) with the silu and ELU + 1 maps and the normalised rule's sums.  The modes are separate instantiations
 // because the prep runs at the register limit: code that only one mode needs
 // would cost the others spills.  kRowDecay: scalar or no decay (one factor per
 // token row) rather than one per key channel; a separate instantiation too
@@ -790,7 +789,7 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
     rule = KDA_RULE_DELTA;
     maps = 0u;
   }
-  if constexpr (kMode == 3) rule = KDA_RULE_DELTA;
+  if constexpr (kMode == 1) rule = KDA_RULE_DELTA;
   const bool linear = kExt || rule != KDA_RULE_DELTA;  // W = 0, U = V: no beta, no solve
   const bool norm = kExt && rule == KDA_RULE_LINEAR_NORM;  // also the normaliser's sums
   uint8_t *const nrm0 = ws + sizeof(WorkspaceHeader) + (size_t)total * Rr::BYTES;
@@ -2313,11 +2312,9 @@ kda_status launch_d(const void *q, const void *k, const void *v, const float *be
   auto prep = kda_prep_kernel<D, 0, false>;
   if constexpr (D == 128) {
     const bool row = am != KDA_ALPHA_CHANNEL;  // scalar or no decay: one factor per token
-    if (rule == KDA_RULE_LINEAR_NORM || (maps & KDA_MAP_QK_ELU1))
+    if (rule != KDA_RULE_DELTA)
       prep = row ? kda_prep_kernel<D, 2, true> : kda_prep_kernel<D, 2, false>;
-    else if (rule == KDA_RULE_DELTA && maps != 0u)
-      prep = row ? kda_prep_kernel<D, 3, true> : kda_prep_kernel<D, 3, false>;
-    else if (rule != 0 || maps != 0u)
+    else if (maps != 0u)  // silu / sigmoid (ELU + 1 is for the linear rules only)
       prep = row ? kda_prep_kernel<D, 1, true> : kda_prep_kernel<D, 1, false>;
     else
       prep = row ? kda_prep_kernel<D, 0, true> : kda_prep_kernel<D, 0, false>;
