@@ -72,6 +72,19 @@ def test_linear_attention_long_sequence():
     assert _err(w, "hT", hT.cpu().numpy().reshape(rh.shape), rh) <= TOL_BF16
 
 
+def test_linear_attention_many_heads():
+    """48 heads: the scan takes two 64-column CTAs per head (four 32-column
+    ones would need two rounds of the SMs); every head against the oracle."""
+    w = _prefill("lin_heads", 64 * 5 + 9, "channel", 0.05, seed=43, H=24, B=2)
+    x = W.prefill_inputs(w)
+    d = device_inputs(w, x)
+    d["beta"] = None
+    o, hT = _run_rule(d, w.C, kda.KDA_RULE_LINEAR, 0)
+    ro, rh = oracle.linear_heads(x["q"], x["k"], x["v"], x["log_alpha"], x["h0"])
+    assert _err(w, "o", o.float().cpu().numpy().reshape(ro.shape), ro) <= TOL_BF16
+    assert _err(w, "hT", hT.cpu().numpy().reshape(rh.shape), rh) <= TOL_BF16
+
+
 def _raw_projections(w, seed, raw_qk=True):
     """Raw (pre-map) q, k in bf16 with a spread that exercises silu's both sides
     (only with raw_qk: unmapped keys must stay unit-norm for the delta rule to
