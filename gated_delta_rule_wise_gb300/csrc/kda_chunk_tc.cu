@@ -803,7 +803,19 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
     return (maps & KDA_MAP_BETA_SIGMOID) ? 1.f / (1.f + __expf(-b)) : b;
   };
   float b_next = 0.f;  // beta of the next chunk's row tid (tid < C)
-  if ((int)blockIdx.x < work && tid < kC) b_next = beta_of(chunk_of(blockIdx.x));
+  // scalar decay: log_alpha of the next chunk's row tid, loaded with its beta
+  // (not bulk-copied; read at the start of the decay phase it sat on the path)
+  auto la_row_of = [&](int idx) -> float {
+    int vn;
+    size_t rn;
+    rows_of(idx, vn, rn);
+    return (alpha_mode == KDA_ALPHA_SCALAR && tid < vn) ? log_alpha[rn + tid] : 0.f;
+  };
+  float la_next = 0.f;
+  if ((int)blockIdx.x < work && tid < kC) {
+    b_next = beta_of(chunk_of(blockIdx.x));
+    if constexpr (kRowDecay) la_next = la_row_of(chunk_of(blockIdx.x));
+  }
   uint32_t mma_phase = 0;
 
   auto wait_mma = [&](unsigned code) {
@@ -874,7 +886,7 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
       // take gamma and 1/gamma per row from EG[r] and EG[C + r]
       float x = 0.f;
       if (tid < kC) {
-        if (alpha_mode == KDA_ALPHA_SCALAR && tid < valid) x = -__expf(log_alpha[row0 + tid]);
+        if (alpha_mode == KDA_ALPHA_SCALAR && tid < valid) x = -__expf(la_next);
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
           const float y = __shfl_up_sync(0xffffffffu, x, off);
@@ -1180,7 +1192,10 @@ __device__ __forceinline__ void prep_d128(const __nv_bfloat16 *__restrict__ q,
     __syncthreads();
     if (has_next) {
       if (tid == 0) issue_lkv(idx_next);
-      if (tid < kC) b_next = beta_of(idx_next);
+      if (tid < kC) {
+        b_next = beta_of(idx_next);
+        if constexpr (kRowDecay) la_next = la_row_of(idx_next);
+      }
     }
 
     // ---- (10) token rows: Qp = Q*gamma - M W (warps 0-3), O = M U (warps 4-7).
