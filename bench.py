@@ -654,6 +654,25 @@ def run_ours(args, rank, world, local, dist):
         return {"value": world * tokens / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
                 "steps": args.steps}
 
+    def time_path(path):  # the headline call through another path of kda_chunk_fwd_ex
+        def call():
+            kda.kda_chunk_fwd_ex(d["q"], d["k"], d["v"], d["beta"], d["log_alpha"], d["h0"], o, hT,
+                                 w.C, ws, stream, path)
+
+        for _ in range(args.warmup):
+            call()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(dist, torch)
+        a.record(stream)
+        for _ in range(args.steps):
+            call()
+        b.record(stream)
+        barrier(dist, torch)
+        kda.kda_chunk_fwd_status(ws, stream)
+        ms = max_over_ranks(a.elapsed_time(b) / args.steps, dist, dev)
+        return {"value": world * tokens / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+                "steps": args.steps}
+
     variants = {} if "variants" not in sections else {
         "linear_attention": dict(
             time_variant(kda.KDA_RULE_LINEAR, 0),
@@ -665,6 +684,11 @@ def run_ours(args, rank, world, local, dist):
             time_variant(kda.KDA_RULE_LINEAR_NORM, kda.KDA_MAP_QK_ELU1),
             rule="q, k <- elu(.) + 1; S = Diag(a) S + k v^T, z = a z + k, o = S^T q / q.z "
                  "(kda_chunk_fwd_rule, KDA_RULE_LINEAR_NORM, KDA_MAP_QK_ELU1)"),
+        "pipelined_call": dict(
+            time_path(kda.KDA_PATH_TENSOR_PIPELINED),
+            path="the headline call in 16 sequence segments, each segment's prep beside the "
+                 "previous segment's one-CTA-per-head scan (KDA_PATH_TENSOR_PIPELINED); "
+                 "the headline value uses the two-launch call"),
     }
 
     # ---- end to end through the public API with host buffers
